@@ -310,7 +310,7 @@ def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=N
     L = 0 if A1 is None else A1.shape[0]
     ad = np.full(T, -1, dtype=np.int64) if token_adapter is None else as_i64(token_adapter)
     if L == 0:
-        ad = np.where(ad >= 0, -1, ad)
+        ad = np.full(T, -1, dtype=np.int64)  # no adapter resident: adapter ids carry no meaning
     ok = _slots_ok(ids_, ad, E, L)
 
     y = np.zeros((T, X.shape[1]))
@@ -320,16 +320,19 @@ def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=N
     ee = ids_[tt, jj]
     ll = ad[tt]
     keys = ee * (L + 1) + (ll + 1)
-    for key in np.unique(keys):
+    cur_e, W1e, W2e = -1, None, None
+    for key in np.unique(keys):  # ascending: all groups of one expert are adjacent
         sel = keys == key
         e, l = int(key // (L + 1)), int(key % (L + 1)) - 1
+        if e != cur_e:
+            cur_e, W1e, W2e = e, as_f64(W1[e]), as_f64(W2[e])
         ts, js = tt[sel], jj[sel]
         Xg = X[ts]
-        g = Xg @ as_f64(W1[e]).T
+        g = Xg @ W1e.T
         if l >= 0:
             g = g + (Xg @ as_f64(A1[l, e]).T) @ as_f64(B1[l, e]).T
         h = swiglu(g)
-        o = h @ as_f64(W2[e]).T
+        o = h @ W2e.T
         if l >= 0:
             o = o + (h @ as_f64(A2[l, e]).T) @ as_f64(B2[l, e]).T
         np.add.at(y, ts, wf[ts, js][:, None] * o)
@@ -357,10 +360,10 @@ def moe_lora_layer_scalar(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=Non
         A2l, B2l = as_f64(A2).tolist(), as_f64(B2).tolist()
     T = len(X)
     k = len(ids_[0]) if T else 0
-    ad = [-1] * T if token_adapter is None else as_i64(token_adapter).tolist()
+    ad = [-1] * T if (token_adapter is None or L == 0) else as_i64(token_adapter).tolist()
     y = [[0.0] * H for _ in range(T)]
     for t in range(T):
-        l = ad[t] if L else -1
+        l = ad[t]
         if not (-1 <= l < L):
             continue
         for j in range(k):
