@@ -1,0 +1,289 @@
+"""Python entry points with the C ABI's names, over torch tensors on the GPU.
+
+Each function checks its tensors, allocates outputs (torch owns device memory)
+and calls the library on the current stream; nothing here computes. Shapes and
+layouts follow include/moe_lora.h.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib as L_
+from ._lib import AlignDesc, LayerOpts, check, lib, ptr, stream_handle
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (there is no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def moe_topk_softmax(logits: torch.Tensor, k: int):
+    """Top-k experts per token and softmax weights over the chosen logits."""
+    _need(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    check(lib().moe_topk_softmax(ptr(logits), T, E, k, ptr(ids), ptr(w), stream_handle()),
+          "moe_topk_softmax")
+    return ids, w
+
+
+def align_layout(T: int, k: int, E: int, L: int, bm_base: int, bm_lora: int) -> list:
+    offs = (ctypes.c_int64 * L_.ALIGN_NFIELDS)()
+    check(lib().moe_lora_align_layout(T, k, E, L, bm_base, bm_lora, offs), "moe_lora_align_layout")
+    return list(offs)
+
+
+@dataclass
+class Align:
+    """An align buffer (device) plus the host description the library needs."""
+    buf: torch.Tensor
+    T: int
+    k: int
+    E: int
+    L: int
+    bm_base: int
+    bm_lora: int
+
+    @property
+    def S(self) -> int:
+        return self.T * self.k
+
+    def desc(self) -> AlignDesc:
+        return AlignDesc(ptr(self.buf), self.T, self.k, self.E, self.L, self.bm_base, self.bm_lora)
+
+    def _offsets(self):
+        return align_layout(self.T, self.k, self.E, self.L, self.bm_base, self.bm_lora)
+
+    def _i32(self, field: int, n: int) -> torch.Tensor:
+        off = self._offsets()[field]
+        return self.buf[off: off + 4 * n].view(torch.int32)
+
+    def header(self) -> dict:
+        h = self._i32(L_.AF_HEADER, 16).cpu().tolist()
+        return dict(err=h[0] & 0xffffffff, n_valid=h[1], n_tiles=h[2], n_lora_blocks=h[3],
+                    n_lora_rows=h[4])
+
+    def sorted_slots(self):
+        return self._i32(L_.AF_SORTED_SLOTS, self.S)
+
+    def slot_row(self):
+        return self._i32(L_.AF_SLOT_ROW, self.S)
+
+    def row_expert(self):
+        return self._i32(L_.AF_ROW_EXPERT, self.S)
+
+    def row_adapter(self):
+        return self._i32(L_.AF_ROW_ADAPTER, self.S)
+
+    def expert_begin(self):
+        return self._i32(L_.AF_EXPERT_BEGIN, self.E + 1)
+
+    def tiles(self):
+        o = self._offsets()
+        return self._i32(L_.AF_TILES, 4 * o[L_.AF_MAX_TILES]).view(-1, 4)
+
+    def lora_blocks(self):
+        o = self._offsets()
+        return self._i32(L_.AF_LORA_BLOCKS, 4 * o[L_.AF_MAX_LORA_BLOCKS]).view(-1, 4)
+
+
+def new_align(T: int, k: int, E: int, L: int, bm_base: int, bm_lora: int,
+              device="cuda") -> Align:
+    n = lib().moe_lora_align_buffer_size(T, k, E, L, bm_base, bm_lora)
+    if n == 0:
+        raise L_.MoeLoraError(L_.ERR_UNSUPPORTED, "moe_lora_align_buffer_size")
+    buf = torch.zeros(n, dtype=torch.uint8, device=device)
+    return Align(buf, T, k, E, L, bm_base, bm_lora)
+
+
+def moe_lora_align(ids: torch.Tensor, token_adapter: Optional[torch.Tensor], E: int, L: int,
+                   bm_base: int = 64, bm_lora: int = 16, al: Optional[Align] = None) -> Align:
+    """Stable (expert, adapter, slot) sort of the slots, tiles and LoRA blocks."""
+    _need(ids, "ids", torch.int32, 2)
+    T, k = ids.shape
+    if token_adapter is not None:
+        _need(token_adapter, "token_adapter", torch.int32, 1, (T,))
+    if al is None:
+        al = new_align(T, k, E, L, bm_base, bm_lora, ids.device)
+    d = al.desc()
+    check(lib().moe_lora_align(ptr(ids), ptr(token_adapter), ctypes.byref(d), stream_handle()),
+          "moe_lora_align")
+    return al
+
+
+def get_error(buf: torch.Tensor) -> int:
+    v = ctypes.c_uint32(0)
+    st = lib().moe_lora_get_error(ptr(buf), stream_handle(), ctypes.byref(v))
+    if st not in (L_.OK, L_.ERR_TIMEOUT):
+        check(st, "moe_lora_get_error")
+    return int(v.value)
+
+
+def clear_error(buf: torch.Tensor) -> None:
+    check(lib().moe_lora_clear_error(ptr(buf), stream_handle()), "moe_lora_clear_error")
+
+
+def moe_gather_rows(x: torch.Tensor, al: Align, out: Optional[torch.Tensor] = None):
+    _need(x, "x", torch.bfloat16, 2)
+    H = x.shape[1]
+    if out is None:
+        out = torch.zeros((al.S, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, 2, (al.S, H))
+    d = al.desc()
+    check(lib().moe_gather_rows(ptr(x), ctypes.byref(d), H, ptr(out), stream_handle()),
+          "moe_gather_rows")
+    return out
+
+
+def moe_grouped_gemm(a_sorted: torch.Tensor, W: torch.Tensor, al: Align,
+                     out: Optional[torch.Tensor] = None):
+    """out[row] = a_sorted[row] @ W[expert(row)].T for the sorted rows (fp32 out)."""
+    _need(a_sorted, "a_sorted", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 3)
+    E, N, K = W.shape
+    if a_sorted.shape[1] != K or a_sorted.shape[0] != al.S or E != al.E:
+        raise ValueError("shape mismatch between a_sorted, W and the align buffer")
+    if out is None:
+        out = torch.zeros((al.S, N), dtype=torch.float32, device=W.device)
+    _need(out, "out", torch.float32, 2, (al.S, N))
+    d = al.desc()
+    check(lib().moe_grouped_gemm(ptr(a_sorted), ptr(W), ctypes.byref(d), N, K, ptr(out),
+                                 stream_handle()), "moe_grouped_gemm")
+    return out
+
+
+def lora_shrink(X: torch.Tensor, rows_are_slots: bool, A: torch.Tensor, al: Align,
+                out: Optional[torch.Tensor] = None):
+    """Z[s] = X[in(s)] @ A[l(s), e(s)].T for the slots with an adapter (fp32 out)."""
+    _need(X, "X", torch.bfloat16, 2)
+    _need(A, "A", torch.bfloat16, 4)
+    Ln, E, r, K = A.shape
+    if X.shape[1] != K or E != al.E or Ln != al.L:
+        raise ValueError("shape mismatch between X, A and the align buffer")
+    if out is None:
+        out = torch.zeros((al.S, r), dtype=torch.float32, device=X.device)
+    _need(out, "out", torch.float32, 2, (al.S, r))
+    d = al.desc()
+    check(lib().lora_shrink(ptr(X), int(bool(rows_are_slots)), ptr(A), ctypes.byref(d), K, r,
+                            ptr(out), stream_handle()), "lora_shrink")
+    return out
+
+
+def lora_expand_add(Z: torch.Tensor, B: Optional[torch.Tensor], al: Align, epilogue: int,
+                    base: torch.Tensor, out: Optional[torch.Tensor] = None, out_fp32: bool = False,
+                    topk_w: Optional[torch.Tensor] = None, N: Optional[int] = None):
+    """Expand with the base add fused; epilogue 0 (in place), 1 (SwiGLU), 2 (combine)."""
+    _need(base, "base", torch.float32, 2)
+    Nb = base.shape[1]
+    r = 0
+    if B is not None:
+        _need(B, "B", torch.bfloat16, 4)
+        r = B.shape[3]
+        if B.shape[2] != Nb or B.shape[1] != al.E or B.shape[0] != al.L:
+            raise ValueError("shape mismatch between B, base and the align buffer")
+        _need(Z, "Z", torch.float32, 2, (al.S, r))
+    dev = base.device
+    if epilogue == 1 and out is None:
+        out = torch.zeros((al.S, Nb // 2), dtype=torch.bfloat16, device=dev)
+    if epilogue == 2 and out is None:
+        out = torch.zeros((al.T, Nb), dtype=torch.float32 if out_fp32 else torch.bfloat16,
+                          device=dev)
+    if epilogue == 2:
+        _need(topk_w, "topk_w", torch.float32, 2, (al.T, al.k))
+    d = al.desc()
+    check(lib().lora_expand_add(ptr(Z) if B is not None else 0, ptr(B), ctypes.byref(d), Nb, r,
+                                epilogue, ptr(base), ptr(out), int(out_fp32), ptr(topk_w),
+                                stream_handle()), "lora_expand_add")
+    return base if epilogue == 0 else out
+
+
+def moe_lora_workspace_size(T: int, k: int, E: int, L: int, H: int, I: int, r: int) -> int:
+    return int(lib().moe_lora_workspace_size(T, k, E, L, H, I, r))
+
+
+def moe_lora_layer_tiles(T: int, k: int, E: int, L: int, H: int, I: int, r: int):
+    b = ctypes.c_int32(0)
+    l_ = ctypes.c_int32(0)
+    check(lib().moe_lora_layer_tiles(T, k, E, L, H, I, r, ctypes.byref(b), ctypes.byref(l_)),
+          "moe_lora_layer_tiles")
+    return b.value, l_.value
+
+
+def new_workspace(T: int, k: int, E: int, L: int, H: int, I: int, r: int, device="cuda"):
+    n = moe_lora_workspace_size(T, k, E, L, H, I, r)
+    if n == 0:
+        raise L_.MoeLoraError(L_.ERR_UNSUPPORTED, "moe_lora_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:256].zero_()  # the sticky error word starts clear
+    return ws
+
+
+def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
+                   logits: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
+                   topk_w: Optional[torch.Tensor] = None, k: Optional[int] = None,
+                   token_adapter: Optional[torch.Tensor] = None,
+                   A1=None, B1=None, A2=None, B2=None, y: Optional[torch.Tensor] = None,
+                   y_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
+                   bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
+                   events: Optional[Sequence] = None) -> torch.Tensor:
+    """The whole fused MoE-LoRA layer; returns y [T, H]."""
+    _need(x, "x", torch.bfloat16, 2)
+    _need(W1, "W1", torch.bfloat16, 3)
+    _need(W2, "W2", torch.bfloat16, 3)
+    T, H = x.shape
+    E, twoI, H1 = W1.shape
+    I = twoI // 2
+    if H1 != H or tuple(W2.shape) != (E, H, I):
+        raise ValueError("W1/W2 shapes do not match x")
+    if logits is not None:
+        _need(logits, "logits", torch.float32, 2, (T, E))
+        if k is None:
+            raise ValueError("k is required with logits")
+    else:
+        _need(topk_ids, "topk_ids", torch.int32, 2)
+        k = topk_ids.shape[1]
+        _need(topk_w, "topk_w", torch.float32, 2, (T, k))
+    Ln, r = 0, 0
+    if A1 is not None:
+        _need(A1, "A1", torch.bfloat16, 4)
+        Ln, _, r, _ = A1.shape
+        _need(B1, "B1", torch.bfloat16, 4, (Ln, E, twoI, r))
+        _need(A2, "A2", torch.bfloat16, 4, (Ln, E, r, I))
+        _need(B2, "B2", torch.bfloat16, 4, (Ln, E, H, r))
+    if token_adapter is not None:
+        _need(token_adapter, "token_adapter", torch.int32, 1, (T,))
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32 if y_fp32 else torch.bfloat16,
+                        device=x.device)
+    _need(y, "y", torch.float32 if y_fp32 else torch.bfloat16, 2, (T, H))
+    if workspace is None:
+        workspace = new_workspace(T, k, E, Ln, H, I, r, x.device)
+    opts = LayerOpts()
+    opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
+    ev_arr = None
+    if events:
+        ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        opts.num_events = len(events)
+        opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
+    check(lib().moe_lora_layer_ex(
+        ptr(x), ptr(logits), ptr(topk_ids), ptr(topk_w), ptr(token_adapter), T, H, I, E, k,
+        ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2), ptr(B2), Ln, r, ptr(y), int(y_fp32),
+        ptr(workspace), workspace.numel(), ctypes.byref(opts), stream_handle()),
+        "moe_lora_layer")
+    return y

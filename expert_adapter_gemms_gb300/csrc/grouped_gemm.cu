@@ -1,0 +1,349 @@
+// Base expert grouped GEMM (vLLM's fused_moe group GEMM: one GEMM per expert over
+// the tokens routed to it; vllm.com.cn, section "Implementing multi-LoRA
+// inference for MoE models in vLLM") on the sm_103a tensor cores.
+//
+//   out[row, n] = sum_c a[row, c] * W[e(row), n, c]
+//
+// Design (GB300-first):
+// * The weights take the MMA's M side: a CTA owns 128 consecutive rows of W_e
+//   (output features) and one token tile of expert e (at most BN sorted rows) on
+//   the N side. At decode an expert sees a handful of tokens, so N shrinks to a
+//   multiple of 16 that covers the tile while the weight stream, which bounds
+//   the kernel, stays full-width. At prefill the same tile is 128 x 256.
+// * Operands are staged in shared memory by TMA (128-byte swizzle, K-major) in a
+//   STAGES-deep mbarrier ring; one elected thread issues tcgen05.mma
+//   (kind::f16, bf16 in, fp32 accumulate) into a TMEM accumulator of BN columns;
+//   four epilogue warps read TMEM with tcgen05.ld and store fp32 rows.
+// * The weight tensor map is 3-D [E][N][K], so weight rows past N read zeros;
+//   K tails read zeros too (TMA out-of-bounds fill) -- no masks in the main loop.
+// * Token tiles are ordered by expert and CTAs are rasterised in groups of
+//   tiles so CTAs that share a weight block run together (L2 reuse).
+// * Every mbarrier wait is bounded; on timeout the CTA records
+//   MOE_LORA_DEVERR_TIMEOUT, drains its own copies and frees TMEM.
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe_lora {
+
+constexpr int kBM = 128;  // weight rows per CTA (MMA M)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kGemmThreads = 192;
+constexpr int kGroupTiles = 8;
+
+template <int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int kWBytes = kBM * kBK * 2;
+  static constexpr int kABytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kWBytes + kABytes;
+  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
+  static_assert(kABytes % 1024 == 0, "stage alignment");
+};
+
+// ----------------------------------------------------------------------------
+// gather: xs[row] = x[token of sorted slot row]
+// ----------------------------------------------------------------------------
+template <bool kVec>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const int* __restrict__ hdr,
+                                                          const int* __restrict__ sorted_slots,
+                                                          int k, int H,
+                                                          __nv_bfloat16* __restrict__ xs) {
+  pdl_wait();
+  const int n_valid = hdr[HDR_NVALID];
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < n_valid; row += warps) {
+    const int t = sorted_slots[row] / k;
+    if (kVec) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+      uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)row * H);
+      for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+    } else {
+      for (int c = lane; c < H; c += 32) xs[(size_t)row * H + c] = x[(size_t)t * H + c];
+    }
+  }
+}
+
+int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& a, int H, void* xs,
+                  cudaStream_t stream, bool pdl) {
+  if (a.S == 0) return MOE_LORA_OK;
+  AlignView v = align_view(al->buf, a);
+  int blocks = ceil_div(a.S, 8);
+  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+  const auto* xp = static_cast<const __nv_bfloat16*>(x);
+  auto* xsp = static_cast<__nv_bfloat16*>(xs);
+  if (H % 8 == 0 && aligned16(x) && aligned16(xs))
+    return launch_pdl(gather_rows_kernel<true>, blocks, 256, 0, stream, pdl, xp, v.hdr,
+                      v.sorted_slots, al->k, H, xsp);
+  return launch_pdl(gather_rows_kernel<false>, blocks, 256, 0, stream, pdl, xp, v.hdr,
+                    v.sorted_slots, al->k, H, xsp);
+}
+
+// ----------------------------------------------------------------------------
+// grouped GEMM kernel
+// ----------------------------------------------------------------------------
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                        const __grid_constant__ CUtensorMap tm_a, int* __restrict__ hdr,
+                        const int4* __restrict__ tiles, float* __restrict__ out, int N, int K,
+                        int n_wblocks, int max_tiles) {
+  using C = GemmCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tmem_full = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // CTA -> (token tile, weight block): groups of kGroupTiles tiles sweep all
+  // weight blocks before the next group starts.
+  const int lin = blockIdx.x;
+  const int per_group = kGroupTiles * n_wblocks;
+  const int grp = lin / per_group;
+  const int first = grp * kGroupTiles;
+  const int gsz = min(kGroupTiles, max_tiles - first);
+  const int within = lin - grp * per_group;
+  const int wb = within / gsz;
+  const int ti = first + within % gsz;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_a);
+  }
+  __syncthreads();
+
+  pdl_wait();
+  const int n_tiles = hdr[HDR_NTILES];
+  if (ti >= n_tiles) return;
+  pdl_trigger();
+  const int4 tile = tiles[ti];
+  const int e = tile.x, row0 = tile.y, rows = tile.z;
+  const uint32_t nmma = static_cast<uint32_t>((rows + 15) & ~15);
+  const int nk = (K + kBK - 1) / kBK;
+
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer: TMA ring
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_a = l2_policy_evict_last();
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*s_abort || !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+          *s_abort = 1;
+          break;
+        }
+        uint8_t* sw = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        tma_load_3d(sw, &tm_w, &full[s], kb * kBK, wb * kBM, e, pol_w);
+        tma_load_2d(sw + C::kWBytes, &tm_a, &full[s], kb * kBK, row0, pol_a);
+        ++issued;
+      }
+      if (*s_abort) {  // drain own copies in flight before the CTA may exit
+        for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
+          mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(kBM, nmma);
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (kb / STAGES) & 1;
+        if (*s_abort || !mbar_wait_bounded(&full[s], ph)) {
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* sw = smem + s * C::kStageBytes;
+        const uint64_t da = smem_desc_sw128(smem_u32(sw));
+        const uint64_t db = smem_desc_sw128(smem_u32(sw + C::kWBytes));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+        tc_commit(&empty[s]);
+      }
+      tc_commit(tmem_full);  // fires when every MMA issued above has completed
+    }
+  } else {
+    // epilogue: warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
+    const int quad = warp & 3;
+    const int n = wb * kBM + quad * 32 + lane;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(tmem_full, 0) ? 1 : 0);
+    if (!ok) *s_abort = 1;
+    tc_fence_after();
+    if (ok && !*s_abort) {
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(taddr + c0, v);
+        tmem_ld_wait();
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = static_cast<int>(c0) + j;
+            if (tok < rows) out[(size_t)(row0 + tok) * N + n] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *s_abort) set_dev_error(hdr, MOE_LORA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map, innermost dimension K (contiguous), 128-byte swizzle, box {64, box_rows[, 1]}.
+static int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return MOE_LORA_ERR_CUDA;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bd[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bd[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
+}
+
+template <int BN, int STAGES>
+static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const AlignView& v,
+                         int max_tiles, int N, int K, float* out, cudaStream_t stream, bool pdl) {
+  using C = GemmCfg<BN, STAGES>;
+  static int configured[64] = {0};
+  int dev = 0;
+  ML_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 64 && !configured[dev]) {
+    ML_CHECK_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    configured[dev] = 1;
+  }
+  const int n_wblocks = ceil_div(N, kBM);
+  const int64_t grid = (int64_t)max_tiles * n_wblocks;
+  if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
+  return launch_pdl(grouped_gemm_kernel<BN, STAGES>, dim3((unsigned)grid), kGemmThreads,
+                    C::kSmemBytes, stream, pdl, tw, ta, v.hdr, (const int4*)v.tiles, out, N, K,
+                    n_wblocks, max_tiles);
+}
+
+int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,
+                        const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
+                        bool pdl) {
+  if (a.S == 0) return MOE_LORA_OK;
+  AlignView v = align_view(al->buf, a);
+  CUtensorMap tw, ta;
+  {
+    const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)al->E};
+    const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)N * K * 2};
+    const uint32_t box[3] = {kBK, kBM, 1};
+    int st = make_tmap_bf16(&tw, W, 3, dims, strides, box);
+    if (st != MOE_LORA_OK) return st;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)K, (uint64_t)a.S};
+    const uint64_t strides[1] = {(uint64_t)K * 2};
+    const uint32_t box[2] = {kBK, (uint32_t)al->bm_base};
+    int st = make_tmap_bf16(&ta, a_sorted, 2, dims, strides, box);
+    if (st != MOE_LORA_OK) return st;
+  }
+  switch (al->bm_base) {
+    case 16: return launch_gemm_t<16, 6>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+    case 32: return launch_gemm_t<32, 5>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+    case 64: return launch_gemm_t<64, 4>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+    case 128: return launch_gemm_t<128, 6>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+    case 256: return launch_gemm_t<256, 4>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+    default: return MOE_LORA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace moe_lora
+
+extern "C" int moe_gather_rows(const void* x, const moe_lora_align_t* al, int H, void* xs,
+                               moe_lora_stream_t stream) {
+  using namespace moe_lora;
+  AlignLayout a;
+  int st = check_align(al, &a);
+  if (st != MOE_LORA_OK) return st;
+  if (H < 1 || (a.S > 0 && (!x || !xs))) return MOE_LORA_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_LORA_OK) return st;
+  return launch_gather(x, al, a, H, xs, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+extern "C" int moe_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,
+                                int N, int K, float* out, moe_lora_stream_t stream) {
+  using namespace moe_lora;
+  AlignLayout a;
+  int st = check_align(al, &a);
+  if (st != MOE_LORA_OK) return st;
+  if (N < 1 || K < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (a.S > 0 && (!a_sorted || !W || !out)) return MOE_LORA_ERR_INVALID_ARG;
+  if (a.S > 0 && (!aligned16(a_sorted) || !aligned16(W))) return MOE_LORA_ERR_INVALID_ARG;
+  if (K % 8 != 0) return MOE_LORA_ERR_UNSUPPORTED;  // TMA row stride must be a multiple of 16 bytes
+  if ((st = check_device()) != MOE_LORA_OK) return st;
+  return launch_grouped_gemm(a_sorted, W, al, a, N, K, out, reinterpret_cast<cudaStream_t>(stream),
+                             true);
+}

@@ -1,0 +1,265 @@
+// The fused MoE-LoRA expert layer as one chain of launches on the caller's
+// stream (vllm.com.cn, sections "Implementing multi-LoRA inference for MoE
+// models in vLLM" and "Kernel optimizations"; aib.vote, programmatic dependent
+// launch removing the idle gaps between kernels):
+//
+//   route -> align -> gather -> gate_up GEMM -> gate_up shrink ->
+//   gate_up expand + SwiGLU -> down GEMM -> down shrink -> down expand + combine
+//
+// Every launch uses programmatic dependent launch; nothing synchronises with the
+// host, no device count is read back, and every size is a runtime argument, so a
+// new token count never triggers a compile or a module load. Intermediates live
+// in the caller's workspace, carved here.
+#include <atomic>
+#include <cstring>
+
+#include "internal.h"
+
+namespace moe_lora {
+
+// ---------------------------------------------------------------------------
+// device checks
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+std::atomic<int> g_dev_sms[kMaxDevices];
+}  // namespace
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_LORA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_LORA_ERR_UNSUPPORTED;
+  int s = g_dev_state[dev].load(std::memory_order_relaxed);
+  if (s == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_LORA_ERR_CUDA;
+    g_dev_sms[dev].store(sms);
+    s = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_state[dev].store(s);
+  }
+  return s == 1 ? MOE_LORA_OK : MOE_LORA_ERR_UNSUPPORTED;
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = g_dev_sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+    g_dev_sms[dev].store(n);
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// tiles and workspace
+// ---------------------------------------------------------------------------
+static void pick_tiles(int T, int k, int E, int32_t* bm_base, int32_t* bm_lora) {
+  const int64_t S = (int64_t)T * k;
+  const int64_t per_expert = (S + E - 1) / E;
+  int64_t b = (2 * per_expert + 15) / 16 * 16;
+  if (b < 16) b = 16;
+  // the tile sizes with a compiled kernel
+  const int allowed[5] = {16, 32, 64, 128, 256};
+  int pick = 256;
+  for (int i = 0; i < 5; ++i)
+    if (allowed[i] >= b) { pick = allowed[i]; break; }
+  *bm_base = pick;
+  *bm_lora = 16;
+}
+
+struct LayerPlan {
+  AlignLayout al;
+  int bm_base, bm_lora;
+  int64_t off_align, off_ids, off_w, off_xs, off_G, off_Z1, off_h, off_Z2, off_O, total;
+  bool valid;
+};
+
+static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r, int bm_base,
+                            int bm_lora) {
+  LayerPlan p = {};
+  p.valid = false;
+  int32_t hb, hl;
+  pick_tiles(T, k, E, &hb, &hl);
+  p.bm_base = bm_base > 0 ? bm_base : hb;
+  p.bm_lora = bm_lora > 0 ? bm_lora : hl;
+  p.al = align_layout(T, k, E, L, p.bm_base, p.bm_lora);
+  // the align region is sized for the smallest tiles so any tile choice fits
+  AlignLayout worst = align_layout(T, k, E, L, 16, 1);
+  if (!p.al.valid || !worst.valid) return p;
+  const int64_t S = (int64_t)T * k;
+  const int64_t rr = L > 0 ? r : 0;
+  int64_t o = 0;
+  auto take = [&](int64_t bytes) { int64_t at = o; o = (int64_t)round_up(o + bytes, 256); return at; };
+  p.off_align = take(worst.off[MOE_LORA_AF_TOTAL_BYTES]);
+  p.off_ids = take(S * 4);
+  p.off_w = take(S * 4);
+  p.off_xs = take(S * H * 2);
+  p.off_G = take(S * 2 * (int64_t)I * 4);
+  p.off_Z1 = take(S * rr * 4);
+  p.off_h = take(S * (int64_t)I * 2);
+  p.off_Z2 = take(S * rr * 4);
+  p.off_O = take(S * (int64_t)H * 4);
+  p.total = o;
+  p.valid = true;
+  return p;
+}
+
+}  // namespace moe_lora
+
+using namespace moe_lora;
+
+extern "C" const char* moe_lora_status_string(int status) {
+  switch (status) {
+    case MOE_LORA_OK: return "ok";
+    case MOE_LORA_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_LORA_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case MOE_LORA_ERR_CUDA: return "CUDA runtime error";
+    case MOE_LORA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_LORA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int moe_lora_get_error(const void* buf, moe_lora_stream_t stream, uint32_t* err) {
+  if (!buf || !err) return MOE_LORA_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ML_CHECK_CUDA(cudaMemcpyAsync(&v, buf, sizeof(v), cudaMemcpyDeviceToHost, s));
+  ML_CHECK_CUDA(cudaStreamSynchronize(s));
+  *err = v;
+  return (v & MOE_LORA_DEVERR_TIMEOUT) ? MOE_LORA_ERR_TIMEOUT : MOE_LORA_OK;
+}
+
+extern "C" int moe_lora_clear_error(void* buf, moe_lora_stream_t stream) {
+  if (!buf) return MOE_LORA_ERR_INVALID_ARG;
+  ML_CHECK_CUDA(cudaMemsetAsync(buf, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)));
+  return MOE_LORA_OK;
+}
+
+extern "C" int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r,
+                                    int32_t* bm_base, int32_t* bm_lora) {
+  (void)L; (void)H; (void)I; (void)r;
+  if (!bm_base || !bm_lora || T < 0 || k < 1 || E < 1) return MOE_LORA_ERR_INVALID_ARG;
+  pick_tiles(T, k, E, bm_base, bm_lora);
+  return MOE_LORA_OK;
+}
+
+extern "C" size_t moe_lora_workspace_size(int T, int k, int E, int L, int H, int I, int r) {
+  if (T < 0 || k < 1 || E < 1 || L < 0 || H < 1 || I < 1 || (L > 0 && r < 1)) return 0;
+  LayerPlan p = plan_layer(T, k, E, L, H, I, r, 0, 0);
+  return p.valid ? (size_t)p.total : 0;
+}
+
+extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32_t* topk_ids,
+                                 const float* topk_w, const int32_t* token_adapter, int T, int H,
+                                 int I, int E, int k, const void* W1, const void* W2,
+                                 const void* A1, const void* B1, const void* A2, const void* B2,
+                                 int L, int r, void* y, int y_fp32, void* workspace,
+                                 size_t workspace_bytes, const moe_lora_layer_opts* opts,
+                                 moe_lora_stream_t stream_) {
+  // ---- host-side validation: nothing is launched on error ----
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || L < 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (k > 32 || E > 1024) return MOE_LORA_ERR_UNSUPPORTED;
+  if (L > 0 && (r < 1 || !A1 || !B1 || !A2 || !B2)) return MOE_LORA_ERR_INVALID_ARG;
+  if (L > 0 && r > 256) return MOE_LORA_ERR_UNSUPPORTED;
+  if (H % 8 != 0 || I % 8 != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  const bool have_logits = logits != nullptr;
+  const bool have_ids = topk_ids != nullptr || topk_w != nullptr;
+  if (T > 0) {
+    if (have_logits == have_ids) return MOE_LORA_ERR_INVALID_ARG;
+    if (have_ids && (!topk_ids || !topk_w)) return MOE_LORA_ERR_INVALID_ARG;
+    if (!x || !W1 || !W2 || !y || !workspace) return MOE_LORA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W2)) return MOE_LORA_ERR_INVALID_ARG;
+    if (L > 0 && (!aligned16(A1) || !aligned16(B1) || !aligned16(A2) || !aligned16(B2)))
+      return MOE_LORA_ERR_INVALID_ARG;
+  }
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_LORA_ERR_INVALID_ARG;
+  moe_lora_layer_opts o = {};
+  if (opts) o = *opts;
+  if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return MOE_LORA_ERR_INVALID_ARG;
+  LayerPlan p = plan_layer(T, k, E, L, H, I, r, o.bm_base, o.bm_lora);
+  if (!p.valid) return MOE_LORA_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_LORA_OK;
+  if (workspace_bytes < (size_t)p.total) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  int st = check_device();
+  if (st != MOE_LORA_OK) return st;
+
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool pdl = !o.disable_pdl;
+  char* ws = static_cast<char*>(workspace);
+  moe_lora_align_t al;
+  al.buf = ws + p.off_align;
+  al.T = T;
+  al.k = k;
+  al.E = E;
+  al.L = L;
+  al.bm_base = p.bm_base;
+  al.bm_lora = p.bm_lora;
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + p.off_ids);
+  float* w = reinterpret_cast<float*>(ws + p.off_w);
+  void* xs = ws + p.off_xs;
+  float* G = reinterpret_cast<float*>(ws + p.off_G);
+  float* Z1 = reinterpret_cast<float*>(ws + p.off_Z1);
+  void* h = ws + p.off_h;
+  float* Z2 = reinterpret_cast<float*>(ws + p.off_Z2);
+  float* O = reinterpret_cast<float*>(ws + p.off_O);
+  const int rr = L > 0 ? r : 0;
+
+  auto mark = [&](int i) -> int {
+    if (i < o.num_events && o.events[i])
+      if (cudaEventRecord(static_cast<cudaEvent_t>(o.events[i]), stream) != cudaSuccess)
+        return MOE_LORA_ERR_CUDA;
+    return MOE_LORA_OK;
+  };
+#define ML_STEP(expr)                       \
+  do {                                      \
+    int _s = (expr);                        \
+    if (_s != MOE_LORA_OK) return _s;       \
+  } while (0)
+
+  ML_STEP(mark(0));
+  if (have_logits) {
+    ML_STEP(launch_topk_softmax(logits, T, E, k, ids, w, stream, pdl));
+  } else {
+    ids = const_cast<int32_t*>(topk_ids);
+    w = const_cast<float*>(topk_w);
+  }
+  ML_STEP(mark(1));
+  ML_STEP(launch_align(ids, L > 0 ? token_adapter : nullptr, &al, p.al, stream, pdl));
+  ML_STEP(mark(2));
+  ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl));
+  ML_STEP(mark(3));
+  ML_STEP(launch_grouped_gemm(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl));
+  ML_STEP(mark(4));
+  if (L > 0) ML_STEP(launch_shrink(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl));
+  ML_STEP(mark(5));
+  ML_STEP(launch_expand(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, 1, G, h, 0, nullptr,
+                        stream, pdl));
+  ML_STEP(mark(6));
+  ML_STEP(launch_grouped_gemm(h, W2, &al, p.al, H, I, O, stream, pdl));
+  ML_STEP(mark(7));
+  if (L > 0) ML_STEP(launch_shrink(h, 1, A2, &al, p.al, I, r, Z2, stream, pdl));
+  ML_STEP(mark(8));
+  ML_STEP(launch_expand(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w, stream,
+                        pdl));
+  ML_STEP(mark(9));
+#undef ML_STEP
+  return MOE_LORA_OK;
+}
+
+extern "C" int moe_lora_layer(const void* x, const float* logits, const int32_t* topk_ids,
+                              const float* topk_w, const int32_t* token_adapter, int T, int H,
+                              int I, int E, int k, const void* W1, const void* W2, const void* A1,
+                              const void* B1, const void* A2, const void* B2, int L, int r,
+                              void* y, int y_fp32, void* workspace, size_t workspace_bytes,
+                              moe_lora_stream_t stream) {
+  return moe_lora_layer_ex(x, logits, topk_ids, topk_w, token_adapter, T, H, I, E, k, W1, W2, A1,
+                           B1, A2, B2, L, r, y, y_fp32, workspace, workspace_bytes, nullptr,
+                           stream);
+}

@@ -1,0 +1,212 @@
+// LoRA shrink z = xA per (expert, adapter) block (vllm.com.cn, sections
+// "Implementing multi-LoRA inference for MoE models in vLLM" and "Kernel
+// optimizations").
+//
+// The shrink has few outputs (r per row) and long sums (K = h_in), and at decode
+// a block holds one or two rows, so the kernel is a stream of A_{l,e} at HBM
+// speed. One CTA takes one LoRA block and one group of 8*NT ranks; its 8 warps
+// split the K sum (split-K inside the CTA) and reduce their partials through
+// shared memory in a fixed warp order, so results are deterministic and no
+// cross-CTA atomics are needed. Each warp walks K in 32-wide steps; every lane
+// issues one 128-bit load per operand row and the products are formed with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate): the block's rows on M (padded
+// to 16), ranks on N. Which k a lane feeds to which fragment slot is permuted
+// identically for both operands, which leaves the dot products unchanged while
+// keeping every load 16 bytes wide. Masks on K are compiled out when
+// K % 32 == 0 (the EVEN_K specialisation); K % 8 != 0 or unaligned bases fall
+// back to element loads.
+#include "internal.h"
+
+namespace moe_lora {
+
+constexpr int kShrinkWarps = 8;
+
+template <bool kVec, bool kEvenK>
+__device__ __forceinline__ uint4 load8_bf16(const __nv_bfloat16* p, int kofs, int K) {
+  uint4 r = make_uint4(0u, 0u, 0u, 0u);
+  if (p == nullptr) return r;
+  if (kVec) {
+    if (kEvenK || kofs < K) r = __ldg(reinterpret_cast<const uint4*>(p + kofs));
+  } else {
+    const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (kofs + 2 * i < K) ? q[kofs + 2 * i] : 0u;
+      const uint32_t hi = (kofs + 2 * i + 1 < K) ? q[kofs + 2 * i + 1] : 0u;
+      w[i] = lo | (hi << 16);
+    }
+    r = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return r;
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int NT, bool kVec, bool kEvenK>
+__global__ void __launch_bounds__(kShrinkWarps * 32)
+    lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
+                       const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
+                       const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
+                       int K, int r, int E, float* __restrict__ Z, int ngroups) {
+  constexpr int R = 8 * NT;  // ranks per CTA
+  __shared__ float red[kShrinkWarps][16][R + 1];
+
+  pdl_wait();
+  const int nb = hdr[HDR_NBLOCKS];
+  const int b = blockIdx.x / ngroups;
+  const int g = blockIdx.x - b * ngroups;
+  if (b >= nb) return;
+  pdl_trigger();
+  const int4 blk = blocks[b];
+  const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, q = lane & 3;
+
+  const __nv_bfloat16* x0 = nullptr;
+  const __nv_bfloat16* x1 = nullptr;
+  if (gid < rows) {
+    const int row = row0 + gid;
+    const int in = rows_are_slots ? row : sorted_slots[row] / k;
+    x0 = X + (size_t)in * K;
+  }
+  if (gid + 8 < rows) {
+    const int row = row0 + gid + 8;
+    const int in = rows_are_slots ? row : sorted_slots[row] / k;
+    x1 = X + (size_t)in * K;
+  }
+  const __nv_bfloat16* Ab = A + ((size_t)l * E + e) * (size_t)r * K;
+  const __nv_bfloat16* ap[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int rank = g * R + nt * 8 + gid;
+    ap[nt] = rank < r ? Ab + (size_t)rank * K : nullptr;
+  }
+
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+
+  const int nsteps = (K + 31) >> 5;
+  int st = warp;
+  // two steps per iteration: all loads first, then the MMAs
+  for (; st + kShrinkWarps < nsteps; st += 2 * kShrinkWarps) {
+    const int k0 = st * 32 + q * 8, k1 = k0 + kShrinkWarps * 32;
+    const uint4 xa0 = load8_bf16<kVec, kEvenK>(x0, k0, K);
+    const uint4 xb0 = load8_bf16<kVec, kEvenK>(x1, k0, K);
+    const uint4 xa1 = load8_bf16<kVec, kEvenK>(x0, k1, K);
+    const uint4 xb1 = load8_bf16<kVec, kEvenK>(x1, k1, K);
+    uint4 av0[NT], av1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      av0[nt] = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
+      av1[nt] = load8_bf16<kVec, kEvenK>(ap[nt], k1, K);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_16816(acc[nt], xa0.x, xb0.x, xa0.y, xb0.y, av0[nt].x, av0[nt].y);
+      mma_16816(acc[nt], xa0.z, xb0.z, xa0.w, xb0.w, av0[nt].z, av0[nt].w);
+      mma_16816(acc[nt], xa1.x, xb1.x, xa1.y, xb1.y, av1[nt].x, av1[nt].y);
+      mma_16816(acc[nt], xa1.z, xb1.z, xa1.w, xb1.w, av1[nt].z, av1[nt].w);
+    }
+  }
+  if (st < nsteps) {
+    const int k0 = st * 32 + q * 8;
+    const uint4 xa0 = load8_bf16<kVec, kEvenK>(x0, k0, K);
+    const uint4 xb0 = load8_bf16<kVec, kEvenK>(x1, k0, K);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 a = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
+      mma_16816(acc[nt], xa0.x, xb0.x, xa0.y, xb0.y, a.x, a.y);
+      mma_16816(acc[nt], xa0.z, xb0.z, xa0.w, xb0.w, a.z, a.w);
+    }
+  }
+
+  // accumulator fragment: c0,c1 -> (row gid, ranks 2q, 2q+1); c2,c3 -> (row gid+8, ...)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][gid][nt * 8 + 2 * q] = acc[nt][0];
+    red[warp][gid][nt * 8 + 2 * q + 1] = acc[nt][1];
+    red[warp][gid + 8][nt * 8 + 2 * q] = acc[nt][2];
+    red[warp][gid + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * R; idx += blockDim.x) {
+    const int m = idx / R, c = idx - m * R;
+    const int rank = g * R + c;
+    if (rank >= r) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kShrinkWarps; ++w) s += red[w][m][c];
+    Z[(size_t)sorted_slots[row0 + m] * r + rank] = s;
+  }
+}
+
+template <int NT>
+static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
+                            const AlignView& v, int max_blocks, int k, int K, int r, int E,
+                            float* Z, bool vec, cudaStream_t stream, bool pdl) {
+  const int ngroups = ceil_div(r, 8 * NT);
+  const int64_t grid = (int64_t)max_blocks * ngroups;
+  if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
+  const dim3 g((unsigned)grid);
+  if (vec && K % 32 == 0)
+    return launch_pdl(lora_shrink_kernel<NT, true, true>, g, kShrinkWarps * 32, 0, stream, pdl, X,
+                      rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
+                      (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
+  if (vec)
+    return launch_pdl(lora_shrink_kernel<NT, true, false>, g, kShrinkWarps * 32, 0, stream, pdl, X,
+                      rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
+                      (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
+  return launch_pdl(lora_shrink_kernel<NT, false, false>, g, kShrinkWarps * 32, 0, stream, pdl, X,
+                    rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
+                    (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
+}
+
+int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
+                  const AlignLayout& a, int K, int r, float* Z, cudaStream_t stream, bool pdl) {
+  if (a.S == 0 || al->L == 0) return MOE_LORA_OK;
+  AlignView v = align_view(al->buf, a);
+  const auto* Xp = static_cast<const __nv_bfloat16*>(X);
+  const auto* Ap = static_cast<const __nv_bfloat16*>(A);
+  const bool vec = (K % 8 == 0) && aligned16(X) && aligned16(A);
+  // Few blocks (decode): one 8-rank group per CTA to spread the A stream over
+  // many CTAs. Many blocks (prefill): all ranks in one CTA so that X is read once.
+  const int blocks_est = a.max_blocks;
+  const int sms = num_sms();
+  int nt;
+  if ((int64_t)blocks_est * ceil_div(r, 8) <= 8 * sms) nt = 1;
+  else if (r <= 16) nt = 2;
+  else if (r <= 32) nt = 4;
+  else nt = 8;
+  switch (nt) {
+    case 1: return launch_shrink_nt<1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
+    case 2: return launch_shrink_nt<2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
+    case 4: return launch_shrink_nt<4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
+    default: return launch_shrink_nt<8>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
+  }
+}
+
+}  // namespace moe_lora
+
+extern "C" int lora_shrink(const void* X, int rows_are_slots, const void* A,
+                           const moe_lora_align_t* al, int K, int r, float* Z,
+                           moe_lora_stream_t stream) {
+  using namespace moe_lora;
+  AlignLayout a;
+  int st = check_align(al, &a);
+  if (st != MOE_LORA_OK) return st;
+  if (K < 1 || r < 1 || (rows_are_slots != 0 && rows_are_slots != 1)) return MOE_LORA_ERR_INVALID_ARG;
+  if (r > 256) return MOE_LORA_ERR_UNSUPPORTED;
+  if (a.S > 0 && al->L > 0 && (!X || !A || !Z)) return MOE_LORA_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_LORA_OK) return st;
+  return launch_shrink(X, rows_are_slots, A, al, a, K, r, Z, reinterpret_cast<cudaStream_t>(stream),
+                       true);
+}

@@ -1,0 +1,252 @@
+/*
+ * moe_lora.h -- C ABI of the fused MoE-LoRA expert layer for NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes (vLLM blog "multi-LoRA for MoE", vllm.com.cn, section
+ * "Implementing multi-LoRA inference for MoE models in vLLM"; and "vLLM Multi-LoRA
+ * Serving for MoE Models", agentlenshq.com, section "Multi-LoRA Serving for MoE
+ * Models"): a router sends every token to its k most relevant experts; each expert
+ * expands the token with a gate_up projection, applies the gated activation and
+ * compresses it back with a down projection; the outputs are aggregated with the
+ * routing weights. Multi-LoRA adds, per request, a low-rank adapter to both
+ * projections: y = xW + (xA)B, where the shrink op is z = xA (h_in -> r) and the
+ * expand op is zB (r -> h_out). Token routing and adapter selection together pick
+ * an (expert, adapter) pair per token-slot ("compound sparsity").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All array pointers are DEVICE pointers owned by the caller. The library never
+ *   allocates, frees or synchronises on the compute path; intermediates live in a
+ *   caller-provided workspace or align buffer.
+ * - Every call is asynchronous on the caller's stream and returns a status code
+ *   (moe_lora_status below). Arguments are validated on the host before anything
+ *   is launched; on error nothing is launched.
+ * - bf16 arrays are passed as `const void*` holding IEEE bfloat16 bit patterns.
+ * - Arrays are contiguous and row-major; base pointers of bf16 matrices read by
+ *   the tensor-memory-accelerator path must be 16-byte aligned, and their row
+ *   length (the reduction dimension) a multiple of 8 elements.
+ * - Weight layouts keep the reduction dimension innermost (the transpose of the
+ *   pages' h_in x h_out notation, as nn.Linear stores it):
+ *       W1 [E, 2I, H]  gate_up (rows [0,I) gate, [I,2I) up)   W2 [E, H, I] down
+ *       A1 [L, E, r, H]  B1 [L, E, 2I, r]  A2 [L, E, r, I]  B2 [L, E, H, r]
+ *   LoRA scale is 1 (y = xW + xAB); fold any alpha/r into B. Adapters with a
+ *   smaller rank are zero-padded to r.
+ * - Slots: s = t*k + j for token t and routing choice j. A token's adapter id
+ *   -1 means "base model only".
+ * - Ids found out of range on the device never trap: the slot is dropped and a
+ *   bit is set in a sticky device error word, read back with moe_lora_get_error.
+ * - Kernels are chained with programmatic dependent launch on the caller's
+ *   stream. Every size is a runtime argument: nothing is compiled or loaded per
+ *   token count.
+ */
+#ifndef MOE_LORA_H_
+#define MOE_LORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_LORA_API __attribute__((visibility("default")))
+#else
+#define MOE_LORA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; pass a CUDA stream handle (or 0). */
+typedef struct CUstream_st* moe_lora_stream_t;
+
+/* Status codes returned by every entry point. */
+enum moe_lora_status {
+  MOE_LORA_OK = 0,
+  MOE_LORA_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, negative size, k > E, ... */
+  MOE_LORA_ERR_UNSUPPORTED = 2,          /* shape outside the documented limits, or not an sm_103 device */
+  MOE_LORA_ERR_CUDA = 3,                 /* a CUDA runtime call or launch failed */
+  MOE_LORA_ERR_WORKSPACE_TOO_SMALL = 4,  /* workspace/align buffer smaller than required */
+  MOE_LORA_ERR_TIMEOUT = 5               /* reported by moe_lora_get_error when a bounded wait gave up */
+};
+
+/* Bits of the sticky device error word. */
+#define MOE_LORA_DEVERR_EXPERT_RANGE 0x1u  /* an expert id outside [0, E): slot dropped */
+#define MOE_LORA_DEVERR_ADAPTER_RANGE 0x2u /* an adapter id outside [-1, L): the token's slots dropped */
+#define MOE_LORA_DEVERR_TIMEOUT 0x4u       /* a bounded wait inside a kernel gave up; results invalid */
+
+/* Human-readable name of a status code (static string). */
+MOE_LORA_API const char* moe_lora_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * Routing (the router "sends each token to its most relevant experts").
+ *
+ * moe_topk_softmax: for each of T tokens, ids[t, 0..k) are the indices of the k
+ * largest logits[t, :] in decreasing order (equal logits: lower index first; NaN
+ * ranks below every number), and w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ * over the chosen logits l_j (fp32). logits [T, E] fp32; ids [T, k] int32;
+ * w [T, k] fp32. Requires 1 <= k <= E <= 1024 and k <= 32. T = 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int moe_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                     moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Alignment: the compound sparsity of expert routing x adapter selection.
+ *
+ * Slots are stably sorted by the key (expert e, adapter l, slot s), l = -1 first.
+ * The result lives in a caller-allocated "align buffer" described by
+ * moe_lora_align_t. Its layout (byte offsets from moe_lora_align_layout):
+ *   header        int32[64]: [0] error word (uint32, sticky, OR-ed), [1] n_valid,
+ *                 [2] n_tiles, [3] n_lora_blocks, [4] n_lora_rows, [5..] echo of
+ *                 T, k, E, L, bm_base, bm_lora
+ *   sorted_slots  int32[S]    kept slots in key order, -1 after n_valid
+ *   slot_row      int32[S]    sorted position of each slot, -1 if dropped
+ *   row_expert    int32[S]    expert of each sorted row
+ *   row_adapter   int32[S]    adapter of each sorted row (-1: none)
+ *   expert_begin  int32[E+1]  rows of expert e are [expert_begin[e], expert_begin[e+1])
+ *   tiles         int32[max_tiles][4]  {e, row_begin, rows, 0}: each expert's rows cut
+ *                 into chunks of at most bm_base rows (the grouped GEMM's token tiles)
+ *   lora_blocks   int32[max_lora_blocks][4] {row_begin, rows, e, l}: each (e, l >= 0)
+ *                 segment cut into chunks of at most bm_lora rows
+ *   then internal scratch (bucket counts and sort buffers).
+ * Entries past the device-side counts are unspecified. Integer results are
+ * bit-exact and deterministic.
+ * Limits: S = T*k <= 1<<22, E*(L+1)+1 and S together fit 32 key bits,
+ * bm_base a multiple of 16 in [16, 256], 1 <= bm_lora <= 16.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_lora_align_t {
+  void* buf;       /* device pointer to an align buffer of moe_lora_align_buffer_size bytes, 256-byte aligned */
+  int32_t T;       /* tokens */
+  int32_t k;       /* experts per token */
+  int32_t E;       /* experts */
+  int32_t L;       /* resident adapters (0: none) */
+  int32_t bm_base; /* rows per grouped-GEMM token tile */
+  int32_t bm_lora; /* rows per LoRA block */
+} moe_lora_align_t;
+
+#define MOE_LORA_ALIGN_NFIELDS 12
+/* Indices into the offsets array filled by moe_lora_align_layout. */
+enum moe_lora_align_field {
+  MOE_LORA_AF_HEADER = 0, MOE_LORA_AF_SORTED_SLOTS, MOE_LORA_AF_SLOT_ROW, MOE_LORA_AF_ROW_EXPERT,
+  MOE_LORA_AF_ROW_ADAPTER, MOE_LORA_AF_EXPERT_BEGIN, MOE_LORA_AF_TILES, MOE_LORA_AF_LORA_BLOCKS,
+  MOE_LORA_AF_MAX_TILES, MOE_LORA_AF_MAX_LORA_BLOCKS, MOE_LORA_AF_SCRATCH, MOE_LORA_AF_TOTAL_BYTES
+};
+
+/* Bytes of align buffer needed; 0 if the parameters are invalid. */
+MOE_LORA_API size_t moe_lora_align_buffer_size(int T, int k, int E, int L, int bm_base, int bm_lora);
+
+/* Fills offsets[MOE_LORA_ALIGN_NFIELDS] (byte offsets; MAX_* fields hold counts). Host only. */
+MOE_LORA_API int moe_lora_align_layout(int T, int k, int E, int L, int bm_base, int bm_lora, int64_t* offsets);
+
+/* ids [T, k] int32; token_adapter [T] int32 or NULL (all -1). One CTA, deterministic. */
+MOE_LORA_API int moe_lora_align(const int32_t* ids, const int32_t* token_adapter, const moe_lora_align_t* al,
+                   moe_lora_stream_t stream);
+
+/* Copies the sticky error word of an align buffer (or of a layer workspace, whose
+ * first bytes are its align buffer) to *err. Synchronises `stream`. */
+MOE_LORA_API int moe_lora_get_error(const void* align_buf_or_workspace, moe_lora_stream_t stream, uint32_t* err);
+/* Clears the sticky error word (asynchronous). */
+MOE_LORA_API int moe_lora_clear_error(void* align_buf_or_workspace, moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Gather: xs[row, :] = x[sorted_slots[row] / k, :] for the n_valid sorted rows.
+ * x [T, H] bf16; xs [S, H] bf16 (rows past n_valid untouched).
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int moe_gather_rows(const void* x, const moe_lora_align_t* al, int H, void* xs,
+                    moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Base expert grouped GEMM (vLLM's fused_moe group GEMM, one GEMM per expert
+ * over the tokens routed to it; vllm.com.cn, section "Implementing multi-LoRA
+ * inference for MoE models in vLLM").
+ *   out[row, n] = sum_c a[row, c] * W[e(row), n, c]   for row < n_valid
+ * a [S, K] bf16 in sorted-row order; W [E, N, K] bf16; out [S, N] fp32 (rows past
+ * n_valid untouched). bf16 in, fp32 accumulate on the tcgen05 tensor cores with
+ * TMEM accumulators, operands staged by TMA. Requires K % 8 == 0, 16-byte aligned
+ * a and W, N >= 1.
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int moe_grouped_gemm(const void* a, const void* W, const moe_lora_align_t* al, int N, int K,
+                     float* out, moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * LoRA shrink z = xA for every slot whose token has an adapter (vllm.com.cn,
+ * sections "Implementing ..." and "Kernel optimizations": r outputs, each a long
+ * sum over h_in, so the sum over K is split across warps of a CTA).
+ *   Z[s, i] = sum_c X[in(s), c] * A[l(s), e(s), i, c]
+ * rows_are_slots = 0: in(s) = s / k, X is [T, K] (token activations).
+ * rows_are_slots = 1: in(s) = slot_row[s], X is [S, K] (sorted rows, e.g. the
+ *                     SwiGLU output feeding the down projection).
+ * A [L, E, r, K] bf16; Z [S, r] fp32 (slots without adapter untouched).
+ * Any K >= 1 and 1 <= r <= 256; K % 8 == 0 with 16-byte aligned X and A takes the
+ * 128-bit load path, and K % 32 == 0 also drops the bounds masks (EVEN_K).
+ * Deterministic (fixed-order reductions, no atomics).
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int lora_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
+                int K, int r, float* Z, moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * LoRA expand with the base add fused in (vllm.com.cn, section "Kernel
+ * optimizations": the LoRA result is added to the base output inside the expand
+ * kernel), plus the layer's two epilogues:
+ *   delta[row, n] = sum_i Z[s, i] * B[l, e, n, i]      (rows with an adapter)
+ *   epilogue 0: base[row, n] += delta[row, n]           in place, fp32 [S, N]
+ *   epilogue 1: out[row, n] = silu(g) * u with g = base[row, n] + delta[row, n],
+ *               u = base[row, N/2 + n] + delta[row, N/2 + n]; out [S, N/2] bf16,
+ *               every valid row (with or without adapter). N must be even.
+ *   epilogue 2: out[t, n] = sum_j w[t, j] * (base[row(t,j), n] + delta[row(t,j), n]),
+ *               j in increasing order; out [T, N] bf16 (out_fp32 = 0) or fp32.
+ *               base is updated in place as in epilogue 0.
+ * Z [S, r] fp32; B [L, E, N, r] bf16 (NULL or L = 0: no adapter term);
+ * topk_w [T, k] fp32 (epilogue 2 only). Deterministic.
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_align_t* al, int N, int r,
+                    int epilogue, float* base, void* out, int out_fp32, const float* topk_w,
+                    moe_lora_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The whole layer:
+ *   route (if logits != NULL) -> align -> gather -> gate_up grouped GEMM ->
+ *   gate_up shrink -> gate_up expand + SwiGLU -> down grouped GEMM -> down shrink
+ *   -> down expand + weighted top-k combine.
+ * x [T, H] bf16. Routing: either logits [T, E] fp32 (topk_ids/topk_w NULL) or
+ * caller-provided topk_ids [T, k] int32 and topk_w [T, k] fp32 (logits NULL).
+ * token_adapter [T] int32 or NULL. LoRA weights may be NULL with L = 0 (base MoE).
+ * y [T, H]: bf16 (y_fp32 = 0) or fp32. workspace: moe_lora_workspace_size bytes,
+ * 256-byte aligned; its first bytes are the layer's align buffer (error word).
+ * Requires H % 8 == 0, I % 8 == 0, 1 <= k <= min(E, 32), E <= 1024.
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API size_t moe_lora_workspace_size(int T, int k, int E, int L, int H, int I, int r);
+
+MOE_LORA_API int moe_lora_layer(const void* x, const float* logits, const int32_t* topk_ids,
+                   const float* topk_w, const int32_t* token_adapter, int T, int H, int I, int E,
+                   int k, const void* W1, const void* W2, const void* A1, const void* B1,
+                   const void* A2, const void* B2, int L, int r, void* y, int y_fp32,
+                   void* workspace, size_t workspace_bytes, moe_lora_stream_t stream);
+
+/* Optional controls for moe_lora_layer_ex (zero-initialise, then set fields). */
+typedef struct moe_lora_layer_opts {
+  int32_t bm_base;      /* grouped-GEMM token tile; 0 = heuristic */
+  int32_t bm_lora;      /* LoRA block rows; 0 = heuristic */
+  int32_t disable_pdl;  /* 1: plain stream-ordered launches */
+  int32_t num_events;   /* length of `events` (0: none) */
+  void** events;        /* cudaEvent_t handles recorded on `stream` before each stage and
+                           after the last: [0] route, [1] align, [2] gather, [3] gate_up GEMM,
+                           [4] gate_up shrink, [5] gate_up expand+SwiGLU, [6] down GEMM,
+                           [7] down shrink, [8] down expand+combine, [9] end */
+} moe_lora_layer_opts;
+
+#define MOE_LORA_LAYER_NUM_STAGES 9
+
+MOE_LORA_API int moe_lora_layer_ex(const void* x, const float* logits, const int32_t* topk_ids,
+                      const float* topk_w, const int32_t* token_adapter, int T, int H, int I,
+                      int E, int k, const void* W1, const void* W2, const void* A1,
+                      const void* B1, const void* A2, const void* B2, int L, int r, void* y,
+                      int y_fp32, void* workspace, size_t workspace_bytes,
+                      const moe_lora_layer_opts* opts, moe_lora_stream_t stream);
+
+/* Tile sizes the layer picks for a shape (host only): bm_base, bm_lora. */
+MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r, int32_t* bm_base,
+                         int32_t* bm_lora);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H_ */

@@ -1,0 +1,165 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+the header declares (and nothing else), sizes its buffers, and rejects invalid
+arguments on the host before any CUDA call. No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_lora.h")
+
+
+@pytest.fixture(scope="session")
+def L():
+    from expert_adapter_gemms_gb300 import build as b
+    if not os.path.exists(b.LIB_PATH):
+        b.build()
+    import expert_adapter_gemms_gb300 as m
+    return m.lib()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_LORA_API\s+[a-z_0-9 \*]+?\b([a-z_0-9]+)\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ["moe_lora_align", "moe_grouped_gemm", "lora_shrink", "lora_expand_add",
+              "moe_lora_layer", "moe_topk_softmax", "moe_lora_get_error"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_symbols():
+        assert hasattr(L, n), n
+
+
+def test_only_declared_symbols_are_exported(L):
+    from expert_adapter_gemms_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm unavailable")
+    exported = set()
+    for line in out.stdout.splitlines():
+        parts = line.split()
+        if len(parts) == 3 and parts[1] in ("T", "W"):
+            exported.add(parts[2])
+    ours = {s for s in exported if s.startswith(("moe_", "lora_"))}
+    assert ours == set(declared_symbols())
+
+
+def test_no_runtime_compiler_linked():
+    """Every kernel is compiled ahead of time for sm_103a: no JIT library is needed."""
+    from expert_adapter_gemms_gb300 import LIB_PATH, build as b
+    out = subprocess.run(["readelf", "-d", LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("readelf unavailable")
+    assert "nvrtc" not in out.stdout and "nvJitLink" not in out.stdout
+    assert b.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(L):
+    import expert_adapter_gemms_gb300 as m
+    assert m.status_string(0) == "ok"
+    assert "workspace" in m.status_string(4)
+
+
+def test_align_layout_and_sizes(L):
+    import expert_adapter_gemms_gb300 as m
+    for (T, k, E, Ln, bb, bl) in [(8, 2, 4, 2, 16, 16), (64, 4, 32, 8, 16, 16),
+                                  (4096, 4, 32, 16, 256, 16), (256, 8, 128, 128, 32, 16),
+                                  (0, 2, 4, 0, 16, 1), (5000, 4, 8, 3, 64, 7)]:
+        offs = m.align_layout(T, k, E, Ln, bb, bl)
+        S = T * k
+        total = L.moe_lora_align_buffer_size(T, k, E, Ln, bb, bl)
+        assert total == offs[11] > 0
+        field_offs = [offs[i] for i in (0, 1, 2, 3, 4, 5, 6, 7, 10)]
+        assert field_offs == sorted(field_offs)
+        assert all(o % 256 == 0 for o in field_offs)
+        assert offs[2] - offs[1] >= 4 * S
+        max_tiles, max_blocks = offs[8], offs[9]
+        assert max_tiles >= -(-S // bb) + min(E, S) - 1  # covers every expert's ragged tail
+        assert max_blocks >= 1
+
+
+def test_align_rejects_bad_tiles(L):
+    assert L.moe_lora_align_buffer_size(8, 2, 4, 2, 24, 16) == 0     # bm_base not a multiple of 16
+    assert L.moe_lora_align_buffer_size(8, 2, 4, 2, 512, 16) == 0    # bm_base too large
+    assert L.moe_lora_align_buffer_size(8, 2, 4, 2, 16, 0) == 0
+    assert L.moe_lora_align_buffer_size(8, 2, 4, 2, 16, 17) == 0
+    assert L.moe_lora_align_buffer_size(-1, 2, 4, 2, 16, 16) == 0
+    assert L.moe_lora_align_buffer_size(1 << 21, 4, 4, 2, 16, 16) == 0  # more than 1<<22 slots
+
+
+def test_workspace_size(L):
+    import expert_adapter_gemms_gb300 as m
+    a = m.moe_lora_workspace_size(64, 4, 32, 8, 2880, 2880, 32)
+    b = m.moe_lora_workspace_size(128, 4, 32, 8, 2880, 2880, 32)
+    assert 0 < a < b
+    # intermediates: xs, G, h, O (bf16/fp32) dominate
+    S = 64 * 4
+    assert a >= S * (2880 * 2 + 5760 * 4 + 2880 * 2 + 2880 * 4)
+    assert m.moe_lora_workspace_size(64, 4, 32, 0, 2880, 2880, 0) < a
+    assert m.moe_lora_workspace_size(64, 0, 32, 8, 2880, 2880, 32) == 0
+
+
+def test_layer_tiles_heuristic(L):
+    import expert_adapter_gemms_gb300 as m
+    assert m.moe_lora_layer_tiles(64, 4, 32, 8, 2880, 2880, 32)[0] == 16
+    assert m.moe_lora_layer_tiles(4096, 4, 32, 16, 2880, 2880, 16)[0] == 256
+    assert m.moe_lora_layer_tiles(256, 8, 128, 128, 2048, 768, 32)[0] == 32
+    for T in (1, 7, 64, 513, 4096):
+        b, l = m.moe_lora_layer_tiles(T, 4, 32, 8, 2880, 2880, 32)
+        assert b in (16, 32, 64, 128, 256) and 1 <= l <= 16
+
+
+def test_host_validation_before_any_cuda_call(L):
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    assert L.moe_topk_softmax(fake, -1, 4, 2, fake, fake, None) == 1
+    assert L.moe_topk_softmax(fake, 4, 4, 5, fake, fake, None) == 1       # k > E
+    assert L.moe_topk_softmax(fake, 4, 2048, 2, fake, fake, None) == 2    # E > 1024
+    assert L.moe_topk_softmax(None, 4, 4, 2, fake, fake, None) == 1       # null logits
+    from expert_adapter_gemms_gb300._lib import AlignDesc
+    bad = AlignDesc(None, 8, 2, 4, 2, 16, 16)
+    assert L.moe_lora_align(fake, fake, ctypes.byref(bad), None) == 1     # null buffer
+    odd = AlignDesc(0x1010, 8, 2, 4, 2, 16, 16)
+    assert L.moe_lora_align(fake, fake, ctypes.byref(odd), None) == 1     # not 256-byte aligned
+    tiles = AlignDesc(0x1000, 8, 2, 4, 2, 24, 16)
+    assert L.moe_lora_align(fake, fake, ctypes.byref(tiles), None) == 2
+    ok = AlignDesc(0x1000, 8, 2, 4, 2, 16, 16)
+    assert L.moe_grouped_gemm(fake, fake, ctypes.byref(ok), 64, 100, fake, None) == 2  # K % 8
+    assert L.moe_grouped_gemm(P(0x1008), fake, ctypes.byref(ok), 64, 64, fake, None) == 1
+    assert L.lora_shrink(fake, 2, fake, ctypes.byref(ok), 64, 8, fake, None) == 1
+    assert L.lora_shrink(fake, 0, fake, ctypes.byref(ok), 64, 300, fake, None) == 2
+    assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 64, 8, 3, fake, fake, 0, fake,
+                             None) == 1
+    assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 63, 8, 1, fake, fake, 0, fake,
+                             None) == 1                                     # SwiGLU needs even N
+    args = [fake, fake, None, None, None, 8, 256, 512, 4, 2, fake, fake, fake, fake, fake, fake,
+            2, 8, fake, 0, P(0x100000), 1 << 30, None]
+    a = list(args); a[6] = 100                                               # H % 8
+    assert L.moe_lora_layer(*a) == 2
+    a = list(args); a[2] = fake; a[3] = fake                                 # logits and ids
+    assert L.moe_lora_layer(*a) == 1
+    a = list(args); a[9] = 5                                                 # k > E
+    assert L.moe_lora_layer(*a) == 1
+    a = list(args); a[21] = 16                                               # workspace too small
+    assert L.moe_lora_layer(*a) == 4
+    a = list(args); a[14] = None                                             # L > 0 needs A2
+    assert L.moe_lora_layer(*a) == 1
+    a = list(args); a[5] = 0                                                 # T = 0: nothing to do
+    assert L.moe_lora_layer(*a) == 0
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "expert_adapter_gemms_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, f

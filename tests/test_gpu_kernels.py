@@ -1,0 +1,190 @@
+"""Per-kernel parity on the GPU: gather, grouped GEMM, shrink, expand epilogues."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_layer_inputs
+
+from gpu_util import (BF16_REL, KERNEL_RTOL, Guarded, assert_bf16_close, assert_close, dev, f64,
+                      need_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(T, H, I, E, k, L, r, seed, bm_base=16, bm_lora=16, adapters="uniform_with_none",
+           routing="gaussian"):
+    m = need_gpu()
+    inp = make_layer_inputs(T=T, H=H, I=I, E=E, k=k, L=L, r=r, seed=seed, adapters=adapters,
+                            routing=routing, lora_std=None)
+    ids, w = oracle.route_topk_softmax(inp.logits, k)
+    ids_t = torch.as_tensor(ids, dtype=torch.int32)
+    al = m.moe_lora_align(dev(ids_t), dev(inp.token_adapter), E, L, bm_base, bm_lora)
+    ref = oracle.align(ids_t, inp.token_adapter, E, L, bm_base, bm_lora)
+    return m, inp, ids, w, al, ref
+
+
+@pytest.mark.parametrize("H", [256, 136, 8])
+def test_gather_exact(H):
+    m, inp, ids, w, al, ref = _setup(T=19, H=H, I=16, E=5, k=3, L=2, r=8, seed=1)
+    xs = Guarded((al.S, H), torch.bfloat16)
+    m.moe_gather_rows(dev(inp.x), al, out=xs.t)
+    xs.check()
+    n = ref["n_valid"]
+    assert np.array_equal(f64(xs.t)[:n], oracle.gather_rows(inp.x, ref))
+
+
+@pytest.mark.parametrize("bm_base", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("K,N", [(256, 1024), (136, 200), (64, 128)])
+def test_grouped_gemm_vs_oracle(bm_base, K, N):
+    """Several tiles per expert, ragged last tile, K tail (136 = 2*64 + 8), N tail (200)."""
+    m, inp, ids, w, al, ref = _setup(T=150, H=K, I=N // 2, E=6, k=2, L=1, r=8, seed=2,
+                                     bm_base=bm_base)
+    xs = m.moe_gather_rows(dev(inp.x), al)
+    out = Guarded((al.S, N), torch.float32, fill=float("nan"))
+    m.moe_grouped_gemm(xs, dev(inp.W1), al, out=out.t)
+    out.check()
+    n = ref["n_valid"]
+    expect = oracle.grouped_gemm(oracle.gather_rows(inp.x, ref), inp.W1, ref)
+    assert_close(out.t[:n], expect, KERNEL_RTOL, f"gemm bm={bm_base} K={K} N={N}")
+    assert torch.isnan(out.t[n:]).all()  # rows past n_valid untouched
+
+
+def test_grouped_gemm_skewed_experts():
+    """Zipf routing: one expert holds most rows (many tiles), others few or none."""
+    m, inp, ids, w, al, ref = _setup(T=600, H=128, I=64, E=16, k=2, L=0, r=1, seed=3,
+                                     bm_base=64, routing="zipf1.0", adapters="none")
+    xs = m.moe_gather_rows(dev(inp.x), al)
+    out = m.moe_grouped_gemm(xs, dev(inp.W1), al)
+    expect = oracle.grouped_gemm(oracle.gather_rows(inp.x, ref), inp.W1, ref)
+    assert_close(out[: ref["n_valid"]], expect, KERNEL_RTOL, "gemm zipf")
+
+
+def test_grouped_gemm_full_size_sampled_rows():
+    """The decode workload's gate_up shape (E=32, N=5760, K=2880) in the layer's tiling;
+    every output row of a sample of rows against the oracle."""
+    m = need_gpu()
+    T, H, I, E, k = 64, 2880, 2880, 32, 4
+    rng = np.random.default_rng(11)
+    x = torch.from_numpy(rng.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy((rng.standard_normal((E, 2 * I, H), dtype=np.float32) * 0.02)).to(
+        torch.bfloat16)
+    lg = torch.from_numpy(rng.standard_normal((T, E), dtype=np.float32))
+    ids, _ = oracle.route_topk_softmax(lg, k)
+    ids_t = torch.as_tensor(ids, dtype=torch.int32)
+    bm = m.moe_lora_layer_tiles(T, k, E, 8, H, I, 32)[0]
+    al = m.moe_lora_align(dev(ids_t), None, E, 0, bm, 16)
+    ref = oracle.align(ids_t, None, E, 0, bm, 16)
+    xs = m.moe_gather_rows(dev(x), al)
+    out = m.moe_grouped_gemm(xs, dev(W), al).cpu()
+    sample = rng.choice(ref["n_valid"], size=24, replace=False)
+    X = f64(x)
+    for row in sample:
+        s = int(ref["sorted_slots"][row])
+        e = int(ref["row_expert"][row])
+        expect = f64(W[e]) @ X[s // k]
+        assert_close(out[row], expect, KERNEL_RTOL, f"row {row}")
+
+
+# ------------------------------------------------------------------ shrink
+@pytest.mark.parametrize("K", [100, 136, 256, 2880])
+@pytest.mark.parametrize("r", [1, 8, 16, 32, 64])
+def test_shrink_vs_oracle(K, r):
+    m, inp, ids, w, al, ref = _setup(T=90, H=K, I=8, E=3, k=2, L=3, r=r, seed=4, bm_lora=16)
+    Z = Guarded((al.S, r), torch.float32, fill=0.0)
+    m.lora_shrink(dev(inp.x), False, dev(inp.A1), al, out=Z.t)
+    Z.check()
+    expect = oracle.lora_shrink(inp.x, inp.A1, ref, rows_are_slots=False)
+    assert_close(Z.t, expect, KERNEL_RTOL, f"shrink K={K} r={r}")
+
+
+def test_shrink_even_k_example(golden_dir):
+    """The pages' masking example: K = 100 with 64-wide K blocks leaves 28 dead lanes in the
+    second block; the result must match the oracle exactly as for an even K."""
+    with open(os.path.join(golden_dir, "even_k_example.json")) as f:
+        g = json.load(f)
+    K = g["K"]
+    m, inp, ids, w, al, ref = _setup(T=33, H=K, I=8, E=2, k=2, L=2, r=16, seed=5, bm_lora=5)
+    Z = m.lora_shrink(dev(inp.x), False, dev(inp.A1), al)
+    assert_close(Z, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, "K=100")
+
+
+@pytest.mark.parametrize("bm_lora", [1, 3, 16])
+def test_shrink_rows_are_slots(bm_lora):
+    m, inp, ids, w, al, ref = _setup(T=70, H=64, I=96, E=4, k=3, L=5, r=16, seed=6,
+                                     bm_lora=bm_lora)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(0)
+    h = torch.from_numpy(rng.standard_normal((al.S, 96), dtype=np.float32)).to(torch.bfloat16)
+    Z = m.lora_shrink(dev(h), True, dev(inp.A2), al)
+    expect = oracle.lora_shrink(h[:n], inp.A2, ref, rows_are_slots=True)
+    assert_close(Z, expect, KERNEL_RTOL, "shrink sorted rows")
+
+
+def test_shrink_decode_shape():
+    """The decode workload: one or two rows per (expert, adapter) pair, K = 2880, r = 32."""
+    m, inp, ids, w, al, ref = _setup(T=64, H=2880, I=8, E=32, k=4, L=8, r=32, seed=7,
+                                     adapters="round_robin_shuffled")
+    Z = m.lora_shrink(dev(inp.x), False, dev(inp.A1), al)
+    assert_close(Z, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, "decode")
+
+
+# ------------------------------------------------------------------ expand
+@pytest.mark.parametrize("r", [8, 5, 32])
+@pytest.mark.parametrize("bm_lora", [1, 16])
+def test_expand_add_inplace(r, bm_lora):
+    m, inp, ids, w, al, ref = _setup(T=50, H=40, I=72, E=4, k=2, L=3, r=r, seed=8,
+                                     bm_lora=bm_lora)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(1)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, r))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 144))).to(torch.float32)
+    base = Guarded((al.S, 144), torch.float32)
+    base.t.copy_(G)
+    m.lora_expand_add(dev(Zh), dev(inp.B1), al, 0, base.t)
+    base.check()
+    expect = oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=0)
+    assert_close(base.t[:n], expect, KERNEL_RTOL, "expand epilogue 0")
+
+
+@pytest.mark.parametrize("bm_base", [16, 64])
+@pytest.mark.parametrize("r", [8, 32, 0])
+def test_expand_swiglu(bm_base, r):
+    L = 3 if r else 0
+    m, inp, ids, w, al, ref = _setup(T=80, H=40, I=72, E=4, k=2, L=L, r=max(r, 1), seed=9,
+                                     bm_base=bm_base)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(2)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, max(r, 1)))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 144))).to(torch.float32)
+    h = Guarded((al.S, 72), torch.bfloat16)
+    m.lora_expand_add(dev(Zh) if r else None, dev(inp.B1) if r else None, al, 1, dev(G),
+                      out=h.t)
+    h.check()
+    if r:
+        expect = oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1)
+    else:
+        expect = oracle.swiglu(f64(G)[:n])
+    assert_bf16_close(h.t[:n], expect, "expand epilogue 1")
+
+
+@pytest.mark.parametrize("out_fp32", [True, False])
+def test_expand_combine(out_fp32):
+    m, inp, ids, w, al, ref = _setup(T=45, H=40, I=24, E=5, k=3, L=2, r=16, seed=10)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(3)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, 16))).to(torch.float32)
+    O = torch.from_numpy(rng.standard_normal((al.S, 40))).to(torch.float32)
+    wt = torch.as_tensor(w, dtype=torch.float32)
+    y = Guarded((45, 40), torch.float32 if out_fp32 else torch.bfloat16)
+    m.lora_expand_add(dev(Zh), dev(inp.B2), al, 2, dev(O), out=y.t, out_fp32=out_fp32,
+                      topk_w=dev(wt))
+    y.check()
+    expect = oracle.lora_expand_add(Zh, inp.B2, ref, O[:n], epilogue=2, w=wt)
+    if out_fp32:
+        assert_close(y.t, expect, KERNEL_RTOL, "combine fp32")
+    else:
+        assert_bf16_close(y.t, expect, "combine bf16")

@@ -1,0 +1,154 @@
+"""The whole fused MoE-LoRA layer on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import CONFIGS, make_config_inputs, make_layer_inputs
+
+from gpu_util import LAYER_RTOL, Guarded, assert_close, dev, f64, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(m, inp, y_fp32=False, adapters=True, B_zero=False, token_adapter=None, **kw):
+    lora = {}
+    if adapters and inp.L > 0:
+        lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
+        if B_zero:
+            lora["B1"] = torch.zeros_like(lora["B1"])
+            lora["B2"] = torch.zeros_like(lora["B2"])
+    ta = inp.token_adapter if token_adapter is None else token_adapter
+    y = Guarded((inp.T, inp.H), torch.float32 if y_fp32 else torch.bfloat16)
+    m.moe_lora_layer(dev(inp.x), dev(inp.W1), dev(inp.W2), logits=dev(inp.logits), k=inp.k,
+                     token_adapter=dev(ta), y=y.t, y_fp32=y_fp32, **lora, **kw)
+    y.check()
+    return y.t
+
+
+def oracle_layer(inp, tokens=None, adapters=True, token_adapter=None):
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    ta = inp.token_adapter if token_adapter is None else token_adapter
+    sel = slice(None) if tokens is None else tokens
+    lora = (inp.A1, inp.B1, inp.A2, inp.B2) if adapters and inp.L > 0 else (None,) * 4
+    return oracle.moe_lora_layer(inp.x[sel], inp.W1, inp.W2, ids[sel], w[sel], ta[sel], *lora)
+
+
+@pytest.mark.parametrize("idx", range(len(CONFIGS)))
+def test_layer_workloads(idx):
+    """All five workloads; the oracle runs on every token of the small ones and on a
+    sample of 48 tokens of the large ones (tokens are independent of each other)."""
+    m = need_gpu()
+    inp = make_config_inputs(idx)
+    y = run_layer(m, inp).cpu()
+    if inp.T <= 256:
+        tokens = np.arange(inp.T)
+    else:
+        tokens = np.sort(np.random.default_rng(idx).choice(inp.T, size=48, replace=False))
+    ref = oracle_layer(inp, tokens)
+    assert_close(y[tokens], ref, LAYER_RTOL, CONFIGS[idx]["name"])
+
+
+def test_layer_error_word_clean_on_workload():
+    m = need_gpu()
+    inp = make_config_inputs(1)
+    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    run_layer(m, inp, workspace=ws)
+    assert m.get_error(ws) == 0
+
+
+def test_layer_amplified_adapters():
+    """A, B ~ N(0, 1/fan_in): the low-rank term is as large as the base term, so the
+    layer bound pins it."""
+    m = need_gpu()
+    for seed in range(3):
+        inp = make_layer_inputs(T=24, H=128, I=96, E=6, k=2, L=3, r=16, seed=50 + seed,
+                                lora_std=None)
+        y = run_layer(m, inp, y_fp32=True).cpu()
+        ref = oracle_layer(inp)
+        base = oracle_layer(inp, adapters=False)
+        assert np.abs(ref - base).max() > 0.3 * np.abs(ref).max()  # adapters matter here
+        assert_close(y, ref, LAYER_RTOL, f"amplified seed {seed}")
+
+
+def test_layer_lora_delta_matches_oracle():
+    """With the workloads' own N(0, 0.02) adapters on the tiny layer the LoRA term is below
+    the layer bound; check the GPU's delta y_lora - y_base against the oracle's directly."""
+    m = need_gpu()
+    inp = make_config_inputs(0)
+    y_l = run_layer(m, inp, y_fp32=True).cpu().double().numpy()
+    y_b = run_layer(m, inp, y_fp32=True, adapters=False).cpu().double().numpy()
+    d_gpu = y_l - y_b
+    d_ref = oracle_layer(inp) - oracle_layer(inp, adapters=False)
+    cos = float((d_gpu * d_ref).sum() / np.sqrt((d_gpu ** 2).sum() * (d_ref ** 2).sum()))
+    assert cos >= 0.99, cos
+    assert np.abs(d_gpu - d_ref).max() <= 0.1 * np.abs(d_ref).max()
+
+
+def test_layer_base_reductions_bitwise():
+    """Adapter -1 everywhere, or B = 0, give exactly the base-only output."""
+    m = need_gpu()
+    inp = make_config_inputs(0)
+    y_base = run_layer(m, inp, y_fp32=True, adapters=False)
+    none = torch.full((inp.T,), -1, dtype=torch.int32)
+    y_none = run_layer(m, inp, y_fp32=True, token_adapter=none)
+    assert torch.equal(y_none, y_base)
+    y_zero = run_layer(m, inp, y_fp32=True, B_zero=True)
+    assert torch.equal(y_zero, y_base)
+
+
+def test_layer_token_permutation():
+    m = need_gpu()
+    inp = make_layer_inputs(T=40, H=64, I=48, E=8, k=2, L=4, r=8, seed=60, lora_std=None)
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(inp.T))
+    inp2 = make_layer_inputs(T=40, H=64, I=48, E=8, k=2, L=4, r=8, seed=60, lora_std=None)
+    inp2.x = inp.x[perm].contiguous()
+    inp2.logits = inp.logits[perm].contiguous()
+    inp2.token_adapter = inp.token_adapter[perm].contiguous()
+    y2 = run_layer(m, inp2, y_fp32=True).cpu()
+    assert_close(y2, f64(y)[perm.numpy()], 1e-5, "permuted")
+
+
+@pytest.mark.parametrize("T", [1, 7, 64, 513])
+def test_layer_many_token_counts(T):
+    """Back-to-back token counts: every size is a runtime argument (no per-size build)."""
+    m = need_gpu()
+    inp = make_layer_inputs(T=T, H=64, I=32, E=8, k=2, L=3, r=8, seed=70 + T, lora_std=None)
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    tokens = np.arange(T) if T <= 64 else np.arange(0, T, 8)
+    assert_close(y[tokens], oracle_layer(inp, tokens), LAYER_RTOL, f"T={T}")
+
+
+def test_layer_dense_single_expert():
+    """E = 1, k = 1: multi-LoRA on a dense gated MLP."""
+    m = need_gpu()
+    inp = make_layer_inputs(T=33, H=96, I=80, E=1, k=1, L=4, r=16, seed=80, lora_std=None)
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    assert_close(y, oracle_layer(inp), LAYER_RTOL, "dense")
+
+
+def test_layer_bad_adapter_ids_dropped_and_flagged():
+    m = need_gpu()
+    inp = make_layer_inputs(T=10, H=64, I=32, E=4, k=2, L=2, r=8, seed=90, lora_std=None)
+    ta = inp.token_adapter.clone()
+    ta[3] = 7
+    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    y = run_layer(m, inp, y_fp32=True, token_adapter=ta, workspace=ws).cpu()
+    assert m.get_error(ws) == 2
+    ref = oracle_layer(inp, token_adapter=ta)
+    assert np.all(ref[3] == 0.0) and torch.all(y[3] == 0)
+    assert_close(y, ref, LAYER_RTOL, "bad adapter")
+
+
+def test_layer_caller_routing_and_no_pdl():
+    m = need_gpu()
+    inp = make_layer_inputs(T=20, H=64, I=32, E=4, k=2, L=2, r=8, seed=91, lora_std=None)
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    y = torch.empty((inp.T, inp.H), dtype=torch.float32, device="cuda")
+    m.moe_lora_layer(dev(inp.x), dev(inp.W1), dev(inp.W2),
+                     topk_ids=dev(torch.as_tensor(ids, dtype=torch.int32)),
+                     topk_w=dev(torch.as_tensor(w, dtype=torch.float32)),
+                     token_adapter=dev(inp.token_adapter), A1=dev(inp.A1), B1=dev(inp.B1),
+                     A2=dev(inp.A2), B2=dev(inp.B2), y=y, y_fp32=True, disable_pdl=True)
+    assert_close(y.cpu(), oracle_layer(inp), LAYER_RTOL, "caller routing")

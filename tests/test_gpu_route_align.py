@@ -1,0 +1,142 @@
+"""Routing and alignment on the GPU: bit-exact against the oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_config_routing
+
+from gpu_util import dev, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_align(m, ids, ad, E, L, bm_base, bm_lora):
+    """Runs the GPU align and compares every array with the oracle, bit for bit."""
+    ids_t = torch.as_tensor(np.asarray(ids), dtype=torch.int32)
+    ad_t = None if ad is None else torch.as_tensor(np.asarray(ad), dtype=torch.int32)
+    al = m.moe_lora_align(dev(ids_t), dev(ad_t), E, L, bm_base, bm_lora)
+    ref = oracle.align(ids_t, ad_t, E, L, bm_base, bm_lora)
+    h = al.header()
+    n = ref["n_valid"]
+    assert h["err"] == ref["err"]
+    assert h["n_valid"] == n
+    assert h["n_tiles"] == len(ref["tiles"])
+    assert h["n_lora_blocks"] == len(ref["lora_blocks"])
+    assert h["n_lora_rows"] == ref["n_lora_rows"]
+    assert al.sorted_slots().cpu().numpy().tolist() == ref["sorted_slots"].tolist()
+    assert al.slot_row().cpu().numpy().tolist() == ref["slot_row"].tolist()
+    assert al.row_expert().cpu().numpy()[:n].tolist() == ref["row_expert"].tolist()
+    assert al.row_adapter().cpu().numpy()[:n].tolist() == ref["row_adapter"].tolist()
+    assert al.expert_begin().cpu().numpy().tolist() == ref["expert_begin"].tolist()
+    tiles = al.tiles().cpu().numpy()[: h["n_tiles"], :3].tolist()
+    assert tiles == [list(t) for t in ref["tiles"]]
+    blocks = al.lora_blocks().cpu().numpy()[: h["n_lora_blocks"]].tolist()
+    assert blocks == [list(b) for b in ref["lora_blocks"]]
+    return al
+
+
+# ---------------------------------------------------------------- routing
+def test_route_golden_cases(golden_dir):
+    m = need_gpu()
+    with open(os.path.join(golden_dir, "route_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        lg = torch.tensor([[float(v) for v in row] for row in c["logits"]], dtype=torch.float32)
+        ids, w = m.moe_topk_softmax(dev(lg), c["k"])
+        assert ids.cpu().tolist() == c["ids"]
+        np.testing.assert_allclose(w.cpu().numpy(), np.array(c["w"]), rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+def test_route_workloads_bitexact_ids(idx):
+    m = need_gpu()
+    lg, _, c = make_config_routing(idx)
+    ids, w = m.moe_topk_softmax(dev(lg), c["k"])
+    rid, rw = oracle.route_topk_softmax(lg, c["k"])
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (5, 3), (32, 32), (33, 4), (100, 8), (257, 2),
+                                 (1024, 16)])
+def test_route_ties_and_shapes(E, k):
+    m = need_gpu()
+    rng = np.random.default_rng(E * 100 + k)
+    T = 37
+    lg = rng.integers(-2, 3, size=(T, E)).astype(np.float32)  # many ties
+    lg[3, :] = np.nan
+    lg[4, ::2] = -np.inf
+    lgt = torch.from_numpy(lg)
+    ids, w = m.moe_topk_softmax(dev(lgt), k)
+    rid, rw = oracle.route_topk_softmax(lgt, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    fin = np.isfinite(rw).all(axis=1)
+    np.testing.assert_allclose(w.cpu().numpy()[fin], rw[fin], rtol=0, atol=2e-6)
+
+
+def test_route_empty():
+    m = need_gpu()
+    ids, w = m.moe_topk_softmax(torch.empty((0, 8), dtype=torch.float32, device="cuda"), 2)
+    assert ids.shape == (0, 2)
+
+
+# ---------------------------------------------------------------- align
+@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("bm_base,bm_lora", [(16, 16), (64, 1), (256, 7)])
+def test_align_workloads(idx, bm_base, bm_lora):
+    m = need_gpu()
+    lg, ad, c = make_config_routing(idx)
+    ids, _ = oracle.route_topk_softmax(lg, c["k"])
+    _check_align(m, ids, ad, c["E"], c["L"], bm_base, bm_lora)
+
+
+def test_align_edge_cases():
+    m = need_gpu()
+    rng = np.random.default_rng(7)
+    # every token adapter-free
+    ids = rng.integers(0, 8, size=(40, 2))
+    _check_align(m, ids, np.full(40, -1), 8, 4, 16, 16)
+    # no adapter array at all
+    _check_align(m, ids, None, 8, 0, 16, 16)
+    # one expert
+    _check_align(m, np.zeros((33, 1)), rng.integers(-1, 3, size=33), 1, 3, 16, 4)
+    # one (expert, adapter) pair holds every slot; counts divisible by the tiles
+    _check_align(m, np.full((64, 2), 3), np.full(64, 2), 4, 3, 32, 16)
+    # a single token
+    _check_align(m, np.array([[2, 0, 1]]), np.array([1]), 3, 2, 16, 1)
+    # no tokens
+    _check_align(m, np.zeros((0, 2)), np.zeros(0), 4, 2, 16, 16)
+    # more slots than the shared-memory sort holds (global-memory sort path)
+    T = 5000
+    ids = np.stack([rng.permutation(16)[:4] for _ in range(T)])
+    _check_align(m, ids, rng.integers(-1, 5, size=T), 16, 5, 64, 16)
+    # many buckets: E * (L + 1) needs three radix digits
+    ids = rng.integers(0, 256, size=(300, 2))
+    _check_align(m, ids, rng.integers(-1, 255, size=300), 256, 255, 16, 3)
+
+
+def test_align_out_of_range_ids_flagged_not_trapped():
+    m = need_gpu()
+    ids = np.array([[0, 5], [1, -1], [2, 3]])
+    ad = np.array([0, 1, 9])
+    al = _check_align(m, ids, ad, 4, 2, 16, 16)
+    err = m.get_error(al.buf)
+    assert err == 3  # expert and adapter range bits
+    m.clear_error(al.buf)
+    assert m.get_error(al.buf) == 0
+
+
+def test_align_is_deterministic():
+    m = need_gpu()
+    lg, ad, c = make_config_routing(2)
+    ids, _ = oracle.route_topk_softmax(lg, c["k"])
+    ids_d = dev(torch.as_tensor(ids, dtype=torch.int32))
+    a1 = m.moe_lora_align(ids_d, dev(ad), c["E"], c["L"], 256, 16)
+    a2 = m.moe_lora_align(ids_d, dev(ad), c["E"], c["L"], 256, 16)
+    torch.cuda.synchronize()
+    n = a1.header()["n_valid"]
+    assert torch.equal(a1.sorted_slots()[:n], a2.sorted_slots()[:n])
