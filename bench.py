@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Throughput of the fused MoE-LoRA expert layer on GB300; prints one JSON line.
+
+A step is one call of the whole layer (route, align, gather, gate_up GEMM,
+gate_up shrink, expand + SwiGLU, down GEMM, down shrink, expand + combine) on
+one batch of the GPT-OSS-20B-shaped decode workload (T = 64 tokens, one per
+request, hidden 2880, intermediate 2880, 32 experts top-4, 8 adapters r = 32),
+with seeded synthetic inputs and random weights.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank drives its own GPU with an independent replica of the
+layer (the layer has no exchange step); the elapsed time is the maximum over
+ranks and the value counts the tokens of all ranks. ``--impl reference`` times
+the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-LoRA layer tokens/s; shrink/expand HBM GB/s as % of ~8 TB/s peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "gptoss20b_decode"
+STAGES = ["route", "align", "gather", "gate_up_gemm", "gate_up_shrink", "gate_up_expand_swiglu",
+          "down_gemm", "down_shrink", "down_expand_combine"]
+
+
+# ----------------------------------------------------------------------------
+# ranks
+# ----------------------------------------------------------------------------
+def world():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def combine_ranks(elapsed_s: float, units: float):
+    """(max elapsed over ranks, sum of units over ranks); plain values at world size 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return elapsed_s, units
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes / flops per launch (the minimum data each stage must move)
+# ----------------------------------------------------------------------------
+def workload_stats(ids, token_adapter, E: int):
+    """Counts that set the algorithmic traffic: touched experts, (e, l) pairs, rows."""
+    import numpy as np
+    ids = np.asarray(ids)
+    ad = np.asarray(token_adapter)
+    T, k = ids.shape
+    e_touched = len(np.unique(ids))
+    lora_tok = ad >= 0
+    pairs = set()
+    for t in range(T):
+        if ad[t] >= 0:
+            for j in range(k):
+                pairs.add((int(ids[t, j]), int(ad[t])))
+    return dict(T=T, k=k, S=T * k, E_touched=e_touched, P=len(pairs),
+                T_L=int(lora_tok.sum()), S_L=int(lora_tok.sum()) * k)
+
+
+def stage_bytes(st: dict, H: int, I: int, E: int, r: int) -> dict:
+    """Minimum bytes each stage reads + writes (bf16 = 2, fp32/int32 = 4)."""
+    S, T, S_L, T_L, P, Et = st["S"], st["T"], st["S_L"], st["T_L"], st["P"], st["E_touched"]
+    return {
+        "route": T * E * 4 + S * 8,
+        "align": S * 4 + T * 4 + S * 16,
+        "gather": T * H * 2 + S * H * 2,
+        "gate_up_gemm": Et * 2 * I * H * 2 + S * H * 2 + S * 2 * I * 4,
+        "gate_up_shrink": P * r * H * 2 + T_L * H * 2 + S_L * r * 4,
+        "gate_up_expand_swiglu": P * 2 * I * r * 2 + S_L * r * 4 + S * 2 * I * 4 + S * I * 2,
+        "down_gemm": Et * H * I * 2 + S * I * 2 + S * H * 4,
+        "down_shrink": P * r * I * 2 + S_L * I * 2 + S_L * r * 4,
+        "down_expand_combine": P * H * r * 2 + S_L * r * 4 + 2 * S_L * H * 4 + S * H * 4
+        + S * 4 + T * H * 2,
+    }
+
+
+def stage_flops(st: dict, H: int, I: int, r: int) -> dict:
+    S, S_L = st["S"], st["S_L"]
+    return {"gate_up_gemm": 2 * S * 2 * I * H, "down_gemm": 2 * S * H * I,
+            "gate_up_shrink": 2 * S_L * r * H, "down_shrink": 2 * S_L * r * I,
+            "gate_up_expand_swiglu": 2 * S_L * 2 * I * r, "down_expand_combine": 2 * S_L * H * r}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [p.strip() for p in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        win = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        note = None
+        if not win and self.samples:  # timed region shorter than the sampling period
+            mid = 0.5 * (t0 + t1)
+            win = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+            note = "timed region shorter than one sample; nearest sample used"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in win:
+            try:
+                sm.append(float(s[1]))
+                mx.append(float(s[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, s[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def gpu_index_for_smi(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p.strip() for p in vis.split(",") if p.strip()]
+        if local_rank < len(parts):
+            return parts[local_rank]
+    return str(local_rank)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if one matches."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel and parts[1] == workload:
+                try:
+                    return float(parts[2])
+                except ValueError:
+                    return None
+    return None
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+class OracleStep:
+    """One step of the fp64 CPU oracle on the first `tokens` tokens of a batch.
+    Weights are converted to fp64 once, before any timing (conversion excluded)."""
+
+    def __init__(self, inp, tokens=None):
+        import oracle
+        self.oracle = oracle
+        self.inp = inp
+        self.n = inp.T if tokens is None else max(1, min(inp.T, int(tokens)))
+        self.W = {n: oracle.as_f64(getattr(inp, n)) for n in ("W1", "W2", "A1", "B1", "A2", "B2")
+                  if getattr(inp, n) is not None}
+        self.x = oracle.as_f64(inp.x)[: self.n]
+        self.logits = inp.logits.numpy()[: self.n]
+        self.ad = inp.token_adapter.numpy()[: self.n]
+
+    def __call__(self):
+        o, W = self.oracle, self.W
+        ids, w = o.route_topk_softmax(self.logits, self.inp.k)
+        return o.moe_lora_layer(self.x, W["W1"], W["W2"], ids, w, self.ad, W.get("A1"),
+                                W.get("B1"), W.get("A2"), W.get("B2"))
+
+
+def cpu_oracle_rate(inp, seconds: float, max_reps: int = 1000):
+    """Tokens/s of the fp64 oracle on this host: whole batches until `seconds` pass."""
+    step = OracleStep(inp)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        step()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= max_reps:
+            break
+    return inp.T * reps / el, reps, el
+
+
+def cpu_cores():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            n = min(n, int(os.environ[v]))
+    return n
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+def workload_config(inp, extra=None):
+    c = {"workload": inp.name, "T": inp.T, "H": inp.H, "I": inp.I, "E": inp.E, "k": inp.k,
+         "L": inp.L, "r": inp.r, "weights": "random N(0,0.02) bf16", "x": "N(0,1) bf16"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args):
+    """The oracle as the reference arm: exactly `steps` timed steps after `warmup`, each on
+    a token sample sized so the whole run stays within --ref-budget-s."""
+    nw, rank, _ = world()
+    if rank != 0:
+        return 0
+    from workloads import make_config_inputs
+    inp = make_config_inputs(args.workload)
+    full = OracleStep(inp)
+    t0 = time.perf_counter()
+    full()
+    t_full = time.perf_counter() - t0
+    per_step = args.ref_budget_s / max(1, args.steps + args.warmup)
+    n = inp.T if t_full <= per_step else max(1, int(inp.T * per_step / t_full))
+    step = full if n == inp.T else OracleStep(inp, n)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    rate = step.n * args.steps / el
+    line = {"metric": METRIC, "value": rate, "unit": UNIT, "impl": "reference", "n_gpus": nw,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": workload_config(inp, {"parallelism": "host cores"}),
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{step.n} of {inp.T} tokens per step (fp64 NumPy oracle)"},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    nw, rank, local = world()
+    if nw > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    import expert_adapter_gemms_gb300 as m
+    from workloads import make_config_inputs
+
+    inp = make_config_inputs(args.workload)
+    d = lambda t: None if t is None else t.to("cuda").contiguous()  # noqa: E731
+    W1, W2 = d(inp.W1), d(inp.W2)
+    lora = dict(A1=d(inp.A1), B1=d(inp.B1), A2=d(inp.A2), B2=d(inp.B2)) if inp.L else {}
+    x_d, lg_d, ta_d = d(inp.x), d(inp.logits), d(inp.token_adapter)
+    y_d = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    bm_base, bm_lora = m.moe_lora_layer_tiles(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        m.moe_lora_layer(x_d, W1, W2, logits=lg_d, k=inp.k, token_adapter=ta_d, y=y_d,
+                         workspace=ws, events=events, **lora)
+
+    clocks = ClockSampler(gpu_index_for_smi(local))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    el_s = e0.elapsed_time(e1) / 1e3
+    el_max, tokens_all = combine_ranks(el_s, inp.T * args.steps)
+    value = tokens_all / el_max
+    clk = clocks.summary(t0, t1)
+    clocks.stop()
+    err = m.get_error(ws)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed steps")
+
+    # end to end through the same public call, inputs from pinned host memory
+    x_h = inp.x.pin_memory()
+    lg_h = inp.logits.pin_memory()
+    ta_h = inp.token_adapter.pin_memory()
+    y_h = torch.empty((inp.T, inp.H), dtype=torch.bfloat16).pin_memory()
+    h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ta_h.numel() * 4
+    d2h = y_h.numel() * 2
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        ta_d.copy_(ta_h, non_blocking=True)
+        step()
+        y_h.copy_(y_d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_max, e2e_tokens = combine_ranks(e0.elapsed_time(e1) / 1e3, inp.T * args.steps)
+
+    # per-stage durations (events between the launches; a separate instrumented pass)
+    nst = len(STAGES)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+    acc = [0.0] * nst
+    for i in range(args.kernel_steps):
+        step(events=evs)
+        torch.cuda.synchronize()
+        for s in range(nst):
+            acc[s] += evs[s].elapsed_time(evs[s + 1])
+    stage_ms = [a / args.kernel_steps for a in acc]
+
+    ids = torch.topk(inp.logits, inp.k, dim=1).indices.numpy()  # accounting only
+    st = workload_stats(ids, inp.token_adapter.numpy() if inp.L else np.full(inp.T, -1), inp.E)
+    sb = stage_bytes(st, inp.H, inp.I, inp.E, inp.r)
+    sf = stage_flops(st, inp.H, inp.I, inp.r)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    kernels = {}
+    for name, ms in zip(STAGES, stage_ms):
+        gbs = sb[name] / (ms * 1e-3) / 1e9 if ms > 0 else None
+        kernels[name] = {"us": round(ms * 1e3, 2), "alg_bytes": int(sb[name]),
+                         "GB_s": round(gbs, 1) if gbs else None,
+                         "hbm_frac": round(gbs / hbm, 3) if gbs else None}
+        if name in sf and ms > 0:
+            kernels[name]["TFLOP_s"] = round(sf[name] / (ms * 1e-3) / 1e12, 2)
+    dom = max(range(nst), key=lambda i: stage_ms[i])
+    dname = STAGES[dom]
+    bound = "hbm"  # at decode every stage streams weights; see the design notes
+    achieved = sb[dname] / (stage_ms[dom] * 1e-3) / 1e9
+    roof = {"kernel": dname, "bound": bound, "achieved": round(achieved, 1),
+            "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "traffic": profiled_traffic(dname, inp.name),
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+            "alg_bytes_per_launch": int(sb[dname])}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": nw, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * el_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": workload_config(inp, {
+                "parallelism": f"replicas x{nw}" if nw > 1 else "single GPU",
+                "bm_base": bm_base, "bm_lora": bm_lora,
+                "l2": "inputs larger than L2: %.2f GB of weights streamed per step" % (
+                    (sb["gate_up_gemm"] + sb["down_gemm"]) / 1e9)}),
+            "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * (10 if inp.L else 8),
+            "clocks": clk, "roofline": roof, "kernels": kernels}
+    if rank == 0 and nw == 1 and not args.no_cpu_baseline:
+        rate, reps, el = cpu_oracle_rate(inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle",
+                                "sample": f"{reps} whole batches of {inp.T} tokens, "
+                                          f"{el:.1f} s (fp64 NumPy oracle, weights pre-converted)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if nw > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
