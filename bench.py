@@ -378,6 +378,9 @@ def run_ours(args):
     # per-stage durations (events between the launches; a separate instrumented pass)
     nst = len(STAGES)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+    for ev in evs:  # torch creates CUDA events lazily, on first record
+        ev.record(stream)
+    torch.cuda.synchronize()
     acc = [0.0] * nst
     for i in range(args.kernel_steps):
         step(events=evs)

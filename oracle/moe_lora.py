@@ -97,8 +97,9 @@ def route_topk_softmax(logits, k: int):
     ids = np.argsort(-key, axis=1, kind="stable")[:, :k]
     sel = np.take_along_axis(key, ids, axis=1)
     m = sel[:, :1]
-    ex = np.exp(sel - m)
-    w = ex / ex.sum(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore"):  # a row of only NaN/-inf logits has no weights (NaN)
+        ex = np.exp(sel - m)
+        w = ex / ex.sum(axis=1, keepdims=True)
     return ids.astype(np.int32), w
 
 
