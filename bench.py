@@ -188,19 +188,37 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if one matches."""
+STAGE_SOURCES = {
+    "route": ["route.cu"], "align": ["align.cu"], "gather": ["grouped_gemm.cu"],
+    "gate_up_gemm": ["grouped_gemm.cu"], "down_gemm": ["grouped_gemm.cu"],
+    "gate_up_shrink": ["lora_shrink.cu"], "down_shrink": ["lora_shrink.cu"],
+    "gate_up_expand_swiglu": ["lora_expand.cu"], "down_expand_combine": ["lora_expand.cu"],
+}
+
+
+def source_hash(stage: str) -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "expert_adapter_gemms_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in STAGE_SOURCES.get(stage, []) + ["common.cuh"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when there is no
+    capture for this stage and workload or the kernel's source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and parts[0] == kernel and parts[1] == workload:
-                try:
-                    return float(parts[2])
-                except ValueError:
-                    return None
+            if line.startswith("#") or len(parts) < 4:
+                continue
+            if parts[0] == stage and parts[1] == workload:
+                return float(parts[2]) if parts[3] == source_hash(stage) else None
     return None
 
 
