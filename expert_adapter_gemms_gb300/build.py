@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmoe_lora.so")
 SOURCES = ["route.cu", "align.cu", "grouped_gemm.cu", "lora_shrink.cu", "lora_expand.cu",
-           "layer.cu"]
+           "layer.cu", "layer_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

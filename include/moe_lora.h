@@ -245,6 +245,32 @@ MOE_LORA_API int moe_lora_layer_ex(const void* x, const float* logits, const int
 MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r, int32_t* bm_base,
                          int32_t* bm_lora);
 
+/* ---------------------------------------------------------------------------
+ * moe_lora_layer_noalloc: the same layer as moe_lora_layer for callers that cannot
+ * allocate device memory -- e.g. a serving engine that has reserved nearly all HBM
+ * for weights and KV cache and hands out only its own buffers, a plugin interface
+ * that passes inputs and outputs but no allocator, or a latency-critical path
+ * where cudaMalloc/cudaFree may synchronise the device. The pages describe no such
+ * entry point; it has no counterpart there.
+ * Arguments are moe_lora_layer's without the workspace; intermediates live in a
+ * 64 MiB array in device global memory held by the library (every GPU that loads
+ * it keeps the 64 MiB until the process exits). Shapes whose
+ * moe_lora_workspace_size exceeds 64 MiB return MOE_LORA_ERR_WORKSPACE_TOO_SMALL
+ * and launch nothing. err_out: optional device pointer that receives this call's
+ * device error word (MOE_LORA_DEVERR_* bits; cleared at the start of each call).
+ * The function allocates nothing. All calls on a device share the array and it
+ * keeps the last call's contents: calls that overlap on the GPU race, so order
+ * them on one stream. The first call on each device looks up the array's device
+ * address; make that first call before any stream capture.
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int moe_lora_layer_noalloc(const void* x, const float* logits,
+                                        const int32_t* topk_ids, const float* topk_w,
+                                        const int32_t* token_adapter, int T, int H, int I, int E,
+                                        int k, const void* W1, const void* W2, const void* A1,
+                                        const void* B1, const void* A2, const void* B2, int L,
+                                        int r, void* y, int y_fp32, uint32_t* err_out,
+                                        moe_lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
