@@ -3,23 +3,25 @@
 // multi-LoRA inference for MoE models in vLLM"; agentlenshq.com, section
 // "Multi-LoRA Serving for MoE Models").
 //
-// One CTA of 1024 threads. Each slot s gets the packed word (key << slot_bits) | s
-// with key = e * (L + 1) + (l + 1) (dropped slots use the last bucket). A stable
-// least-significant-digit radix sort on the key bits (8-bit digits, per-warp
-// digit histograms, ranks from __match_any_sync) keeps equal keys in slot
-// order, so the result is the unique stable order: deterministic and bit-exact.
-// Bucket counts give the expert and (expert, adapter) segment boundaries, from
-// which the grouped-GEMM token tiles and the LoRA blocks are cut.
+// One CTA (256 threads up to 4096 slots, 1024 beyond). Each slot s gets the
+// packed word (key << slot_bits) | s with key = e * (L + 1) + (l + 1) (dropped
+// slots use the last bucket). A stable least-significant-digit radix sort on the
+// key bits (8-bit digits, per-warp digit histograms, ranks from
+// __match_any_sync) keeps equal keys in slot order, so the result is the unique
+// stable order: deterministic and bit-exact. Bucket counts give the expert and
+// (expert, adapter) segment boundaries, from which the grouped-GEMM token tiles
+// and the LoRA blocks are cut. Working state (bucket counts and starts, the
+// sort buffers) stays in shared memory whenever it fits; only results go out.
 #include "common.cuh"
 
 namespace moe_lora {
 
-constexpr int kAlignThreads = 1024;
-constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kSmemSortMaxSlots = 16384;
+constexpr size_t kAlignSmemBudget = 200 * 1024;
 
 // Exclusive scan of one int per thread across the CTA; returns the prefix and
-// writes the total to *total. `tmp` holds kAlignWarps + 1 ints.
+// writes the total to *total. `tmp` holds NW + 1 ints.
+template <int NW>
 __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -31,66 +33,80 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
   if (lane == 31) tmp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int x = tmp[lane];
+    const int x = lane < NW ? tmp[lane] : 0;
     int xi = x;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int u = __shfl_up_sync(0xffffffffu, xi, off);
       if (lane >= off) xi += u;
     }
-    tmp[lane] = xi - x;  // exclusive prefix of warp totals
-    if (lane == 31) tmp[kAlignWarps] = xi;
+    if (lane < NW) tmp[lane] = xi - x;  // exclusive prefix of warp totals
+    if (lane == 31) tmp[NW] = xi;
   }
   __syncthreads();
   const int r = tmp[warp] + incl - v;
-  *total = tmp[kAlignWarps];
+  *total = tmp[NW];
   __syncthreads();
   return r;
 }
 
-// Exclusive scan of a global int array in place-free form: out[i] = sum in[0..i).
-__device__ void block_scan_array(const int* in, int* out, int n, int* tmp) {
-  const int chunk = (n + kAlignThreads - 1) / kAlignThreads;
-  const int b = threadIdx.x * chunk;
-  const int e = min(n, b + chunk);
-  int s = 0;
-  for (int i = b; i < e; ++i) s += in[i];
-  int total;
-  int run = block_exclusive_scan(s, tmp, &total);
-  for (int i = b; i < e; ++i) {
-    const int x = in[i];
-    out[i] = run;
-    run += x;
-  }
+// Shared-memory plan of one align launch (host and device agree through this).
+struct AlignSmem {
+  int hist_off, tmp_off, bcount_off, bstart_off, sort_off;  // in ints
+  size_t bytes;
+  bool smem_buckets, smem_sort;
+};
+
+__host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nthreads) {
+  AlignSmem p;
+  const int nw = nthreads / 32;
+  p.hist_off = 0;
+  p.tmp_off = 256 * nw;
+  int o = p.tmp_off + 64;
+  const size_t sort_b = (size_t)2 * S * 4;
+  const size_t bucket_b = (size_t)2 * nbuckets * 4;
+  p.smem_sort = S <= kSmemSortMaxSlots;
+  const size_t base = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
+  p.smem_buckets = base + bucket_b <= kAlignSmemBudget;
+  p.bcount_off = o;
+  p.bstart_off = o + (p.smem_buckets ? nbuckets : 0);
+  o = p.bstart_off + (p.smem_buckets ? nbuckets : 0);
+  p.sort_off = o;
+  p.bytes = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
+  return p;
 }
 
-__global__ void __launch_bounds__(kAlignThreads, 1)
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
     align_kernel(const int* __restrict__ ids, const int* __restrict__ token_adapter, AlignView v,
                  int T, int k, int E, int L, int bm_base, int bm_lora, int S, int nbuckets,
-                 int key_bits, int slot_bits, int smem_sort) {
+                 int key_bits, int slot_bits) {
+  constexpr int NW = NT / 32;
   extern __shared__ __align__(16) int smem[];
-  int* hist = smem;                       // [256 digits][32 warps]
-  int* tmp = smem + 256 * kAlignWarps;    // scan scratch
+  const AlignSmem plan = align_smem_plan(S, nbuckets, NT);
+  int* hist = smem + plan.hist_off;  // [256 digits][NW warps]
+  int* tmp = smem + plan.tmp_off;
+  int* bcount = plan.smem_buckets ? smem + plan.bcount_off : v.bucket_count;
+  int* bstart = plan.smem_buckets ? smem + plan.bstart_off : v.bucket_start;
+  uint32_t* bufA = plan.smem_sort ? reinterpret_cast<uint32_t*>(smem + plan.sort_off) : v.sort0;
+  uint32_t* bufB = plan.smem_sort ? bufA + S : v.sort1;
   __shared__ unsigned int s_err;
-  __shared__ int s_nvalid, s_ntiles, s_nblocks, s_nlora;
-
-  uint32_t* bufA = smem_sort ? reinterpret_cast<uint32_t*>(smem + 256 * kAlignWarps + 64) : v.sort0;
-  uint32_t* bufB = smem_sort ? bufA + S : v.sort1;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int drop = nbuckets - 1;
   const uint32_t smask = (slot_bits >= 32) ? 0xffffffffu : ((1u << slot_bits) - 1u);
 
+  // the next launch waits before reading any of this launch's results
+  pdl_trigger();
   pdl_wait();
   if (tid == 0) s_err = 0u;
-  for (int i = tid; i < nbuckets; i += kAlignThreads) v.bucket_count[i] = 0;
   __syncthreads();
 
-  // 1. keys and bucket counts
-  for (int s = tid; s < S; s += kAlignThreads) {
+  // 1. keys
+  for (int s = tid; s < S; s += NT) {
     const int t = s / k;
-    const int e = ids[s];
-    const int l = token_adapter ? token_adapter[t] : -1;
+    const int e = __ldcg(ids + s);
+    const int l = token_adapter ? __ldcg(token_adapter + t) : -1;
     unsigned int bad = 0;
     if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
     if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
@@ -98,17 +114,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     if (bad) atomicOr(&s_err, bad);
     else key = e * (L + 1) + (l + 1);
     bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
-    atomicAdd(&v.bucket_count[key], 1);
   }
   __syncthreads();
 
-  // 2. stable LSD radix sort on the key bits
+  // 2. stable LSD radix sort on the key bits (8-bit digits)
   uint32_t* src = bufA;
   uint32_t* dst = bufB;
-  const int chunk = (S + kAlignWarps - 1) / kAlignWarps;
+  const int chunk = (S + NW - 1) / NW;
   const int wb = min(S, warp * chunk), we = min(S, wb + chunk);
+  const unsigned lt = (1u << lane) - 1u;
   for (int shift = slot_bits; shift < slot_bits + key_bits; shift += 8) {
-    for (int d = lane; d < 256; d += 32) hist[d * kAlignWarps + warp] = 0;
+    for (int d = lane; d < 256; d += 32) hist[d * NW + warp] = 0;
     __syncwarp();
     for (int base = wb; base < we; base += 32) {
       const int i = base + lane;
@@ -117,29 +133,29 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       if (act) {
         const int d = (src[i] >> shift) & 255;
         const unsigned peers = __match_any_sync(mask, d);
-        if (lane == __ffs(peers) - 1) hist[d * kAlignWarps + warp] += __popc(peers);
+        if (lane == __ffs(peers) - 1) hist[d * NW + warp] += __popc(peers);
       }
       __syncwarp();
     }
     __syncthreads();
-    {  // exclusive scan over (digit, warp) in digit-major order: 8 entries per thread
-      int loc[8];
+    {  // exclusive scan over (digit, warp) in digit-major order
+      constexpr int PER = 256 * NW / NT;
+      int loc[PER];
       int s = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        loc[q] = hist[tid * 8 + q];
+      for (int q = 0; q < PER; ++q) {
+        loc[q] = hist[tid * PER + q];
         s += loc[q];
       }
       int total;
-      int run = block_exclusive_scan(s, tmp, &total);
+      int run = block_exclusive_scan<NW>(s, tmp, &total);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        hist[tid * 8 + q] = run;
+      for (int q = 0; q < PER; ++q) {
+        hist[tid * PER + q] = run;
         run += loc[q];
       }
     }
     __syncthreads();
-    const unsigned lt = (1u << lane) - 1u;
     for (int base = wb; base < we; base += 32) {
       const int i = base + lane;
       const bool act = i < we;
@@ -150,10 +166,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
         const uint32_t x = src[i];
         d = (x >> shift) & 255;
         peers = __match_any_sync(mask, d);
-        dst[hist[d * kAlignWarps + warp] + __popc(peers & lt)] = x;
+        dst[hist[d * NW + warp] + __popc(peers & lt)] = x;
       }
       __syncwarp();
-      if (act && lane == __ffs(peers) - 1) hist[d * kAlignWarps + warp] += __popc(peers);
+      if (act && lane == __ffs(peers) - 1) hist[d * NW + warp] += __popc(peers);
       __syncwarp();
     }
     __syncthreads();
@@ -162,9 +178,25 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     dst = sw;
   }
 
-  // 3. sorted rows
-  const int n_valid = S - v.bucket_count[drop];
-  for (int i = tid; i < S; i += kAlignThreads) {
+  // 3. segment starts: bucket c starts at the first sorted word with key >= c
+  //    (bucket order is expert-major, adapter -1 first); counts are differences.
+  for (int c = tid; c < nbuckets; c += NT) {
+    int lo = 0, hi = S;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int>(src[mid] >> slot_bits) < c) lo = mid + 1;
+      else hi = mid;
+    }
+    bstart[c] = lo;
+  }
+  __syncthreads();
+  for (int c = tid; c < nbuckets; c += NT)
+    bcount[c] = (c + 1 < nbuckets ? bstart[c + 1] : S) - bstart[c];
+  __syncthreads();
+  const int n_valid = bstart[drop];
+
+  // 4. sorted rows, expert starts
+  for (int i = tid; i < S; i += NT) {
     const uint32_t x = src[i];
     const int s = static_cast<int>(x & smask);
     const int key = static_cast<int>(x >> slot_bits);
@@ -179,54 +211,43 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       v.row_adapter[i] = l;
     }
   }
-  // 4. segment starts
-  block_scan_array(v.bucket_count, v.bucket_start, nbuckets, tmp);
-  __syncthreads();
-  for (int e = tid; e <= E; e += kAlignThreads) v.expert_begin[e] = v.bucket_start[e * (L + 1)];
-  __syncthreads();
+  for (int e = tid; e <= E; e += NT) v.expert_begin[e] = bstart[e * (L + 1)];
+  if (!plan.smem_buckets) __syncthreads();  // global bucket arrays: make the scan visible
 
   // 5. token tiles (per expert, bm_base rows) and LoRA blocks (per (e, l>=0), bm_lora rows)
-  {
-    const int c = (n_valid + kAlignThreads - 1) / kAlignThreads;
-    const int b = tid * c, en = min(n_valid, b + c);
-    int nt = 0, nb = 0, nl = 0;
-    for (int i = b; i < en; ++i) {
-      const int e = v.row_expert[i], l = v.row_adapter[i];
-      if ((i - v.expert_begin[e]) % bm_base == 0) ++nt;
-      if (l >= 0) {
-        ++nl;
-        if ((i - v.bucket_start[e * (L + 1) + l + 1]) % bm_lora == 0) ++nb;
-      }
-    }
-    int tot_t, tot_b, tot_l;
-    int ti = block_exclusive_scan(nt, tmp, &tot_t);
-    int bi = block_exclusive_scan(nb, tmp, &tot_b);
-    block_exclusive_scan(nl, tmp, &tot_l);
-    for (int i = b; i < en; ++i) {
-      const int e = v.row_expert[i], l = v.row_adapter[i];
-      const int eb = v.expert_begin[e];
-      if ((i - eb) % bm_base == 0) v.tiles[ti++] = make_int4(e, i, min(bm_base, v.expert_begin[e + 1] - i), 0);
-      if (l >= 0) {
-        const int key = e * (L + 1) + l + 1;
-        const int sb = v.bucket_start[key];
-        if ((i - sb) % bm_lora == 0)
-          v.blocks[bi++] = make_int4(i, min(bm_lora, sb + v.bucket_count[key] - i), e, l);
-      }
-    }
-    if (tid == 0) {
-      s_nvalid = n_valid;
-      s_ntiles = tot_t;
-      s_nblocks = tot_b;
-      s_nlora = tot_l;
+  const int c = (n_valid + NT - 1) / NT;
+  const int b = tid * c, en = min(n_valid, b + c);
+  int nt = 0, nb = 0, nl = 0;
+  for (int i = b; i < en; ++i) {
+    const int key = static_cast<int>(src[i] >> slot_bits);
+    const int e = key / (L + 1), l = key % (L + 1) - 1;
+    if ((i - bstart[e * (L + 1)]) % bm_base == 0) ++nt;
+    if (l >= 0) {
+      ++nl;
+      if ((i - bstart[key]) % bm_lora == 0) ++nb;
     }
   }
-  __syncthreads();
+  int tot_t, tot_b, tot_l;
+  int ti = block_exclusive_scan<NW>(nt, tmp, &tot_t);
+  int bi = block_exclusive_scan<NW>(nb, tmp, &tot_b);
+  block_exclusive_scan<NW>(nl, tmp, &tot_l);
+  for (int i = b; i < en; ++i) {
+    const int key = static_cast<int>(src[i] >> slot_bits);
+    const int e = key / (L + 1), l = key % (L + 1) - 1;
+    const int eb = bstart[e * (L + 1)];
+    if ((i - eb) % bm_base == 0)
+      v.tiles[ti++] = make_int4(e, i, min(bm_base, bstart[(e + 1) * (L + 1)] - i), 0);
+    if (l >= 0) {
+      const int sb = bstart[key];
+      if ((i - sb) % bm_lora == 0) v.blocks[bi++] = make_int4(i, min(bm_lora, sb + bcount[key] - i), e, l);
+    }
+  }
   if (tid == 0) {
     if (s_err) atomicOr(reinterpret_cast<unsigned int*>(v.hdr + HDR_ERR), s_err);
-    v.hdr[HDR_NVALID] = s_nvalid;
-    v.hdr[HDR_NTILES] = s_ntiles;
-    v.hdr[HDR_NBLOCKS] = s_nblocks;
-    v.hdr[HDR_NLORAROWS] = s_nlora;
+    v.hdr[HDR_NVALID] = n_valid;
+    v.hdr[HDR_NTILES] = tot_t;
+    v.hdr[HDR_NBLOCKS] = tot_b;
+    v.hdr[HDR_NLORAROWS] = tot_l;
     v.hdr[HDR_T] = T;
     v.hdr[HDR_K] = k;
     v.hdr[HDR_E] = E;
@@ -234,31 +255,31 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     v.hdr[HDR_BMB] = bm_base;
     v.hdr[HDR_BML] = bm_lora;
   }
-  pdl_trigger();
 }
 
-static size_t align_smem_bytes(int S, bool smem_sort) {
-  size_t b = (size_t)(256 * kAlignWarps + 64) * 4;
-  if (smem_sort) b += (size_t)2 * S * 4;
-  return b;
-}
-
-int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
-                 const AlignLayout& a, cudaStream_t stream, bool pdl) {
+template <int NT>
+static int launch_align_t(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
+                          const AlignLayout& a, cudaStream_t stream, bool pdl) {
   AlignView v = align_view(al->buf, a);
-  const bool smem_sort = a.S <= kSmemSortMaxSlots;
-  const size_t smem = align_smem_bytes(a.S, smem_sort);
+  const AlignSmem plan = align_smem_plan(a.S, a.nbuckets, NT);
   static int configured[64] = {0};
   int dev = 0;
   ML_CHECK_CUDA(cudaGetDevice(&dev));
   if (dev < 64 && !configured[dev]) {
-    ML_CHECK_CUDA(cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)align_smem_bytes(kSmemSortMaxSlots, true)));
+    ML_CHECK_CUDA(cudaFuncSetAttribute(align_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(kAlignSmemBudget + 16 * 1024)));
     configured[dev] = 1;
   }
-  return launch_pdl(align_kernel, 1, kAlignThreads, smem, stream, pdl, ids, token_adapter, v,
+  return launch_pdl(align_kernel<NT>, 1, NT, plan.bytes, stream, pdl, ids, token_adapter, v,
                     al->T, al->k, al->E, al->L, al->bm_base, al->bm_lora, a.S, a.nbuckets,
-                    a.key_bits, a.slot_bits, smem_sort ? 1 : 0);
+                    a.key_bits, a.slot_bits);
+}
+
+int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
+                 const AlignLayout& a, cudaStream_t stream, bool pdl) {
+  // few slots: a small CTA keeps the many barriers of the sort cheap
+  if (a.S <= 4096) return launch_align_t<256>(ids, token_adapter, al, a, stream, pdl);
+  return launch_align_t<1024>(ids, token_adapter, al, a, stream, pdl);
 }
 
 }  // namespace moe_lora

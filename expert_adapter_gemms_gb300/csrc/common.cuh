@@ -166,6 +166,11 @@ inline int check_align(const moe_lora_align_t* al, AlignLayout* out) {
 // MOE_LORA_DEVERR_TIMEOUT instead of spinning forever.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 
+// Under programmatic dependent launch a kernel is already running while earlier
+// launches write their results. Everything produced by an earlier launch is
+// therefore read with ld.global.cg (__ldcg, coherent at L2) or through TMA, never
+// through the read-only path (__ldg / const __restrict__ loads), whose contents
+// may be stale; only weights and caller inputs take the read-only path.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
 
@@ -198,6 +203,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t done;

@@ -38,6 +38,7 @@ struct GemmCfg {
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static_assert((2 * STAGES + 2) * 8 + 16 <= 256, "barrier area");
   static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kABytes % 1024 == 0, "stage alignment");
@@ -51,26 +52,30 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
                                                           const int* __restrict__ hdr,
                                                           const int* __restrict__ sorted_slots,
                                                           int k, int H,
-                                                          __nv_bfloat16* __restrict__ xs) {
+                                                          __nv_bfloat16* __restrict__ xs,
+                                                          int trigger_first) {
+  // trigger_first: the next launch reads nothing of the align step before its own
+  // wait (the expert-major GEMM), so it may start streaming weights right away
+  if (trigger_first) pdl_trigger();
   pdl_wait();
-  const int n_valid = hdr[HDR_NVALID];
-  pdl_trigger();
+  const int n_valid = __ldcg(hdr + HDR_NVALID);
+  if (!trigger_first) pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < n_valid; row += warps) {
-    const int t = sorted_slots[row] / k;
+    const int t = __ldcg(sorted_slots + row) / k;
     if (kVec) {
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
       uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)row * H);
-      for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+      for (int c = lane; c < H / 8; c += 32) dst[c] = __ldcg(src + c);
     } else {
-      for (int c = lane; c < H; c += 32) xs[(size_t)row * H + c] = x[(size_t)t * H + c];
+      for (int c = lane; c < H; c += 32) xs[(size_t)row * H + c] = __ldcg(x + (size_t)t * H + c);
     }
   }
 }
 
 int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& a, int H, void* xs,
-                  cudaStream_t stream, bool pdl) {
+                  cudaStream_t stream, bool pdl, bool trigger_first) {
   if (a.S == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   int blocks = ceil_div(a.S, 8);
@@ -79,9 +84,9 @@ int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& 
   auto* xsp = static_cast<__nv_bfloat16*>(xs);
   if (H % 8 == 0 && aligned16(x) && aligned16(xs))
     return launch_pdl(gather_rows_kernel<true>, blocks, 256, 0, stream, pdl, xp, v.hdr,
-                      v.sorted_slots, al->k, H, xsp);
+                      v.sorted_slots, al->k, H, xsp, trigger_first ? 1 : 0);
   return launch_pdl(gather_rows_kernel<false>, blocks, 256, 0, stream, pdl, xp, v.hdr,
-                    v.sorted_slots, al->k, H, xsp);
+                    v.sorted_slots, al->k, H, xsp, trigger_first ? 1 : 0);
 }
 
 // ----------------------------------------------------------------------------
@@ -91,8 +96,9 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_a, int* __restrict__ hdr,
-                        const int4* __restrict__ tiles, float* __restrict__ out, int N, int K,
-                        int n_wblocks, int max_tiles) {
+                        const int4* __restrict__ tiles, const int* __restrict__ expert_begin,
+                        float* __restrict__ out, int N, int K, int n_wblocks, int max_tiles,
+                        int expert_major, int early) {
   using C = GemmCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -100,29 +106,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + STAGES;
   uint64_t* tmem_full = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_full + 1);
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // first row and row count of the CTA's work
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // CTA -> (token tile, weight block): groups of kGroupTiles tiles sweep all
-  // weight blocks before the next group starts.
-  const int lin = blockIdx.x;
-  const int per_group = kGroupTiles * n_wblocks;
-  const int grp = lin / per_group;
-  const int first = grp * kGroupTiles;
-  const int gsz = min(kGroupTiles, max_tiles - first);
-  const int within = lin - grp * per_group;
-  const int wb = within / gsz;
-  const int ti = first + within % gsz;
+  // Which weight block and which expert.
+  //  tile-major: CTA -> (token tile, weight block); groups of kGroupTiles tiles
+  //              sweep all weight blocks before the next group starts.
+  //  expert-major: CTA -> (expert, weight block); the CTA takes every token of the
+  //              expert, in chunks of BN rows, so it knows its weights before any
+  //              table of the align step exists.
+  int wb, ti = 0, e;
+  if (expert_major) {
+    e = blockIdx.x / n_wblocks;
+    wb = blockIdx.x - e * n_wblocks;
+  } else {
+    const int lin = blockIdx.x;
+    const int per_group = kGroupTiles * n_wblocks;
+    const int grp = lin / per_group;
+    const int first = grp * kGroupTiles;
+    const int gsz = min(kGroupTiles, max_tiles - first);
+    const int within = lin - grp * per_group;
+    wb = within / gsz;
+    ti = first + within % gsz;
+    e = 0;
+  }
 
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // one arrival for the weight copy, one for the token copy
       mbar_init(&empty[s], 1);
     }
     mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);  // one arrival per epilogue warp
     *s_abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -133,92 +153,152 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
 
-  pdl_wait();
-  const int n_tiles = hdr[HDR_NTILES];
-  if (ti >= n_tiles) return;
-  pdl_trigger();
-  const int4 tile = tiles[ti];
-  const int e = tile.x, row0 = tile.y, rows = tile.z;
-  const uint32_t nmma = static_cast<uint32_t>((rows + 15) & ~15);
+  // Tile-major with `early`: the tile table (from the align launch, two or more
+  // launches back) is read before griddepcontrol.wait. Expert-major: nothing of the
+  // align step is read before the wait.
+  int row0 = 0, rows = 0;
+  if (!expert_major) {
+    if (!early) pdl_wait();
+    const int n_tiles = __ldcg(hdr + HDR_NTILES);
+    if (ti >= n_tiles) {
+      if (early) pdl_wait();
+      return;
+    }
+    const int4 tile = __ldcg(tiles + ti);
+    e = tile.x;
+    row0 = tile.y;
+    rows = tile.z;
+  }
   const int nk = (K + kBK - 1) / kBK;
+  const int pre = nk < STAGES ? nk : STAGES;
 
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // the first ring of weight stages (a weight never depends on a launch)
+  if (threadIdx.x == 0) {
+    const uint64_t pol_w = l2_policy_evict_first();
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], C::kWBytes);
+      tma_load_3d(smem + kb * C::kStageBytes, &tm_w, &full[kb], kb * kBK, wb * kBM, e, pol_w);
+    }
+  }
+  if (expert_major || early) pdl_wait();
+  if (threadIdx.x == 0) {
+    pdl_trigger();
+    if (expert_major) {
+      const int eb = __ldcg(expert_begin + e), ee = __ldcg(expert_begin + e + 1);
+      s_job[0] = eb;
+      s_job[1] = ee - eb;
+    } else {
+      s_job[0] = row0;
+      s_job[1] = rows;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int jrow0 = s_job[0], jrows = s_job[1];
+  const int njobs = expert_major ? (jrows + BN - 1) / BN : 1;
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: TMA ring
+      // producer: TMA ring over every k-block of every job
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_a = l2_policy_evict_last();
       int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (*s_abort || !mbar_wait_bounded(&empty[s], ph ^ 1)) {
-          *s_abort = 1;
-          break;
+      if (njobs == 0) {  // no token for this expert: complete the prefetched stages, drain
+        for (int kb = 0; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
+        for (int kb = 0; kb < pre; ++kb) mbar_wait_bounded(&full[kb], 0);
+      }
+      for (int j = 0; j < njobs && !*s_abort; ++j) {
+        const int r0 = jrow0 + j * BN;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int g = j * nk + kb;
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          uint8_t* sw = smem + s * C::kStageBytes;
+          if (g >= pre) {
+            if (*s_abort || !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+              *s_abort = 1;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], C::kWBytes);
+            tma_load_3d(sw, &tm_w, &full[s], kb * kBK, wb * kBM, e, pol_w);
+          }
+          mbar_arrive_expect_tx(&full[s], C::kABytes);
+          tma_load_2d(sw + C::kWBytes, &tm_a, &full[s], kb * kBK, r0, pol_a);
+          ++issued;
         }
-        uint8_t* sw = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_3d(sw, &tm_w, &full[s], kb * kBK, wb * kBM, e, pol_w);
-        tma_load_2d(sw + C::kWBytes, &tm_a, &full[s], kb * kBK, row0, pol_a);
-        ++issued;
       }
       if (*s_abort) {  // drain own copies in flight before the CTA may exit
-        for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
-          mbar_wait_bounded(&full[kb % STAGES], (kb / STAGES) & 1);
+        for (int g = issued - 1; g >= 0 && g >= issued - STAGES; --g)
+          mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(kBM, nmma);
-      int kb = 0;
-      for (; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (kb / STAGES) & 1;
-        if (*s_abort || !mbar_wait_bounded(&full[s], ph)) {
-          *s_abort = 1;
-          break;
+      for (int j = 0; j < njobs && !*s_abort; ++j) {
+        const int jr = min(BN, jrows - j * BN);
+        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>((jr + 15) & ~15));
+        if (j > 0) {  // the epilogue must have read the previous job's accumulator
+          if (!mbar_wait_bounded(tmem_empty, (j - 1) & 1)) {
+            *s_abort = 1;
+            break;
+          }
+          tc_fence_after();
         }
-        tc_fence_after();
-        const uint8_t* sw = smem + s * C::kStageBytes;
-        const uint64_t da = smem_desc_sw128(smem_u32(sw));
-        const uint64_t db = smem_desc_sw128(smem_u32(sw + C::kWBytes));
+        for (int kb = 0; kb < nk; ++kb) {
+          const int g = j * nk + kb;
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          if (*s_abort || !mbar_wait_bounded(&full[s], ph)) {
+            *s_abort = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* sw = smem + s * C::kStageBytes;
+          const uint64_t da = smem_desc_sw128(smem_u32(sw));
+          const uint64_t db = smem_desc_sw128(smem_u32(sw + C::kWBytes));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
-        tc_commit(&empty[s]);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+          tc_commit(&empty[s]);
+        }
+        tc_commit(tmem_full);  // fires when every MMA issued above has completed
       }
-      tc_commit(tmem_full);  // fires when every MMA issued above has completed
     }
   } else {
     // epilogue: warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
     const int quad = warp & 3;
     const int n = wb * kBM + quad * 32 + lane;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(tmem_full, 0) ? 1 : 0);
-    if (!ok) *s_abort = 1;
-    tc_fence_after();
-    if (ok && !*s_abort) {
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    for (int j = 0; j < njobs; ++j) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(tmem_full, j & 1) ? 1 : 0);
+      if (!ok) *s_abort = 1;
+      if (!ok || *s_abort) break;
+      tc_fence_after();
+      const int r0 = jrow0 + j * BN;
+      const int jr = min(BN, jrows - j * BN);
+      const uint32_t nmma = static_cast<uint32_t>((jr + 15) & ~15);
       for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
         uint32_t v[16];
         tmem_ld_x16(taddr + c0, v);
         tmem_ld_wait();
         if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = static_cast<int>(c0) + j;
-            if (tok < rows) out[(size_t)(row0 + tok) * N + n] = __uint_as_float(v[j]);
+          for (int q = 0; q < 16; ++q) {
+            const int tok = static_cast<int>(c0) + q;
+            if (tok < jr) out[(size_t)(r0 + tok) * N + n] = __uint_as_float(v[q]);
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
     }
   }
   tc_fence_before();
@@ -272,7 +352,8 @@ static int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint
 
 template <int BN, int STAGES>
 static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const AlignView& v,
-                         int max_tiles, int N, int K, float* out, cudaStream_t stream, bool pdl) {
+                         int max_tiles, int E, int N, int K, float* out, cudaStream_t stream,
+                         bool pdl, int expert_major, int early) {
   using C = GemmCfg<BN, STAGES>;
   static int configured[64] = {0};
   int dev = 0;
@@ -283,18 +364,22 @@ static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const Ali
     configured[dev] = 1;
   }
   const int n_wblocks = ceil_div(N, kBM);
-  const int64_t grid = (int64_t)max_tiles * n_wblocks;
+  const int64_t grid = (int64_t)(expert_major ? E : max_tiles) * n_wblocks;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
   return launch_pdl(grouped_gemm_kernel<BN, STAGES>, dim3((unsigned)grid), kGemmThreads,
-                    C::kSmemBytes, stream, pdl, tw, ta, v.hdr, (const int4*)v.tiles, out, N, K,
-                    n_wblocks, max_tiles);
+                    C::kSmemBytes, stream, pdl, tw, ta, v.hdr, (const int4*)v.tiles,
+                    (const int*)v.expert_begin, out, N, K, n_wblocks, max_tiles, expert_major,
+                    early);
 }
 
-int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,
-                        const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
-                        bool pdl) {
+int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora_align_t* al,
+                             const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
+                             bool pdl, bool early, int expert_major_bn) {
   if (a.S == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
+  const int em = expert_major_bn > 0 ? 1 : 0;
+  const int bn = em ? expert_major_bn : al->bm_base;
+  const int ea = early ? 1 : 0;
   CUtensorMap tw, ta;
   {
     const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)al->E};
@@ -306,18 +391,24 @@ int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_alig
   {
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)a.S};
     const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {kBK, (uint32_t)al->bm_base};
+    const uint32_t box[2] = {kBK, (uint32_t)bn};
     int st = make_tmap_bf16(&ta, a_sorted, 2, dims, strides, box);
     if (st != MOE_LORA_OK) return st;
   }
-  switch (al->bm_base) {
-    case 16: return launch_gemm_t<16, 6>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
-    case 32: return launch_gemm_t<32, 5>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
-    case 64: return launch_gemm_t<64, 4>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
-    case 128: return launch_gemm_t<128, 6>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
-    case 256: return launch_gemm_t<256, 4>(tw, ta, v, a.max_tiles, N, K, out, stream, pdl);
+  switch (bn) {
+    case 16: return launch_gemm_t<16, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
+    case 32: return launch_gemm_t<32, 5>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
+    case 64: return launch_gemm_t<64, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
+    case 128: return launch_gemm_t<128, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
+    case 256: return launch_gemm_t<256, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
+}
+
+int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,
+                        const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
+                        bool pdl) {
+  return launch_grouped_gemm_impl(a_sorted, W, al, a, N, K, out, stream, pdl, false, 0);
 }
 
 }  // namespace moe_lora
@@ -330,7 +421,7 @@ extern "C" int moe_gather_rows(const void* x, const moe_lora_align_t* al, int H,
   if (st != MOE_LORA_OK) return st;
   if (H < 1 || (a.S > 0 && (!x || !xs))) return MOE_LORA_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_LORA_OK) return st;
-  return launch_gather(x, al, a, H, xs, reinterpret_cast<cudaStream_t>(stream), true);
+  return launch_gather(x, al, a, H, xs, reinterpret_cast<cudaStream_t>(stream), true, false);
 }
 
 extern "C" int moe_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,

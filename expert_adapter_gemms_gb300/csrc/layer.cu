@@ -164,7 +164,7 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
                                  moe_lora_stream_t stream_) {
   // ---- host-side validation: nothing is launched on error ----
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || L < 0) return MOE_LORA_ERR_INVALID_ARG;
-  if (k > 32 || E > 1024) return MOE_LORA_ERR_UNSUPPORTED;
+  if (k > 32 || E > 1024 || L >= 65535) return MOE_LORA_ERR_UNSUPPORTED;
   if (L > 0 && (r < 1 || !A1 || !B1 || !A2 || !B2)) return MOE_LORA_ERR_INVALID_ARG;
   if (L > 0 && r > 256) return MOE_LORA_ERR_UNSUPPORTED;
   if (H % 8 != 0 || I % 8 != 0) return MOE_LORA_ERR_UNSUPPORTED;
@@ -233,21 +233,25 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(mark(1));
   ML_STEP(launch_align(ids, L > 0 ? token_adapter : nullptr, &al, p.al, stream, pdl));
   ML_STEP(mark(2));
-  ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl));
+  // Few rows per expert (decode): the gate_up GEMM runs expert-major, so its weights
+  // stream from the start of the layer while routing, align and gather finish.
+  const int64_t per_expert = ((int64_t)T * k + E - 1) / E;
+  const int em_bn = !pdl ? 0 : per_expert <= 16 ? 32 : per_expert <= 32 ? 64 : 0;
+  ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, em_bn > 0));
   ML_STEP(mark(3));
-  ML_STEP(launch_grouped_gemm(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl));
+  ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, pdl, em_bn));
   ML_STEP(mark(4));
-  if (L > 0) ML_STEP(launch_shrink(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl));
+  if (L > 0) ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
   ML_STEP(mark(5));
-  ML_STEP(launch_expand(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, 1, G, h, 0, nullptr,
-                        stream, pdl));
+  ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, 1, G, h, 0,
+                             nullptr, stream, pdl, pdl && L > 0));
   ML_STEP(mark(6));
-  ML_STEP(launch_grouped_gemm(h, W2, &al, p.al, H, I, O, stream, pdl));
+  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, 0));
   ML_STEP(mark(7));
-  if (L > 0) ML_STEP(launch_shrink(h, 1, A2, &al, p.al, I, r, Z2, stream, pdl));
+  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, Z2, stream, pdl, pdl));
   ML_STEP(mark(8));
-  ML_STEP(launch_expand(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w, stream,
-                        pdl));
+  ML_STEP(launch_expand_impl(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w,
+                             stream, pdl, pdl && L > 0));
   ML_STEP(mark(9));
 #undef ML_STEP
   return MOE_LORA_OK;

@@ -5,208 +5,419 @@
 // (the router "aggregates" the experts' outputs; section "Implementing multi-LoRA
 // inference for MoE models in vLLM").
 //
-// Each thread owns one output column n, so the rows of B_{l,e} (r contiguous
-// bf16, 128-bit loads) and the base output are read coalesced across the warp;
-// the block's z rows are staged in shared memory and broadcast. Sums over the
-// rank run in a fixed order: deterministic.
+// The expand is a stream: every touched B_{l,e} (N x r bf16) is read, each output
+// element needs r multiply-adds. Threads own output columns, so B rows (r
+// contiguous bf16, 128-bit loads) and base rows are read coalesced across a warp,
+// and every thread issues all its loads before it consumes any. z rows are staged
+// in shared memory and broadcast. Sums over the rank run in a fixed order:
+// deterministic.
+//
+// Launch ordering: every kernel of the library triggers its dependents only after
+// its own griddepcontrol.wait, so when a kernel starts, everything launched two or
+// more steps earlier has completed. With `early` set (the layer sets it where it
+// holds), a kernel reads such older data -- B weights, align tables, the base
+// output of the GEMM two launches back -- before its own wait, and waits only for
+// the z produced by its immediate predecessor.
 #include "internal.h"
 
 namespace moe_lora {
 
 constexpr int kExpandThreads = 256;
 constexpr int kMaxBmLora = 16;
-constexpr int kSwigluRowChunk = 32;
+constexpr int kMaxRegRank = 64;  // ranks held in registers; larger r reads B from L1
 
-// dot(z[0..r), B row) with the B row read 8 bf16 at a time when aligned.
-template <bool kVecB>
-__device__ __forceinline__ float dot_zb(const float* zs, const __nv_bfloat16* brow, int r) {
+__device__ __forceinline__ void fma8(float& acc, const float* z, uint4 u) {
+  acc = fmaf(z[0], bf16_lo(u.x), acc);
+  acc = fmaf(z[1], bf16_hi(u.x), acc);
+  acc = fmaf(z[2], bf16_lo(u.y), acc);
+  acc = fmaf(z[3], bf16_hi(u.y), acc);
+  acc = fmaf(z[4], bf16_lo(u.z), acc);
+  acc = fmaf(z[5], bf16_hi(u.z), acc);
+  acc = fmaf(z[6], bf16_lo(u.w), acc);
+  acc = fmaf(z[7], bf16_hi(u.w), acc);
+}
+
+// dot(z[0..r), B row) reading the B row from memory (any r, any alignment when !kVec).
+template <bool kVec>
+__device__ __forceinline__ float dot_zb_mem(const float* zs, const __nv_bfloat16* brow, int r) {
   float acc = 0.f;
-  if (kVecB) {
+  if (kVec) {
     const uint4* b4 = reinterpret_cast<const uint4*>(brow);
-    for (int i = 0; i < r; i += 8) {
-      const uint4 u = __ldg(b4 + (i >> 3));
-      acc = fmaf(zs[i + 0], bf16_lo(u.x), acc);
-      acc = fmaf(zs[i + 1], bf16_hi(u.x), acc);
-      acc = fmaf(zs[i + 2], bf16_lo(u.y), acc);
-      acc = fmaf(zs[i + 3], bf16_hi(u.y), acc);
-      acc = fmaf(zs[i + 4], bf16_lo(u.z), acc);
-      acc = fmaf(zs[i + 5], bf16_hi(u.z), acc);
-      acc = fmaf(zs[i + 6], bf16_lo(u.w), acc);
-      acc = fmaf(zs[i + 7], bf16_hi(u.w), acc);
-    }
+    for (int i = 0; i < r; i += 8) fma8(acc, zs + i, __ldg(b4 + (i >> 3)));
   } else {
     for (int i = 0; i < r; ++i) acc = fmaf(zs[i], __bfloat162float(brow[i]), acc);
   }
   return acc;
 }
 
-// epilogue 0: base[row, n] += z[s] . B[l, e, n, :] over the rows of each LoRA block.
-template <bool kVecB>
+// ----------------------------------------------------------------------------
+// epilogue 0: base[row, n] += z[s] . B[l, e, n, :] over the rows of each LoRA
+// block; two columns per thread, B rows loaded once per block.
+// ----------------------------------------------------------------------------
+template <int RV>  // r / 8 when the B rows sit in registers (r % 8 == 0, r <= 64); 0 otherwise
 __global__ void __launch_bounds__(kExpandThreads)
     expand_add_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                       const int* __restrict__ hdr, const int4* __restrict__ blocks,
                       const int* __restrict__ sorted_slots, int N, int r, int E,
-                      float* __restrict__ base) {
+                      float* __restrict__ base, int early) {
   extern __shared__ float zs[];  // [rows][r]
-  pdl_wait();
-  const int nb = hdr[HDR_NBLOCKS];
+  if (!early) pdl_wait();
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
   const int b = blockIdx.x;
-  if (b >= nb) return;
-  pdl_trigger();
-  const int4 blk = blocks[b];
+  if (b >= nb) {
+    if (early) pdl_wait();
+    return;
+  }
+  const int4 blk = __ldcg(blocks + b);
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
+  const int n0 = blockIdx.y * (2 * kExpandThreads) + threadIdx.x;
+  const int n1 = n0 + kExpandThreads;
+  const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
+  uint4 b0[RV > 0 ? RV : 1], b1[RV > 0 ? RV : 1];
+  if (RV > 0) {
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+      b0[i] = n0 < N ? __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n0 * r) + i) : make_uint4(0, 0, 0, 0);
+      b1[i] = n1 < N ? __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n1 * r) + i) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (early) pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < rows * r; i += blockDim.x) {
     const int m = i / r, c = i - m * r;
-    zs[i] = Z[(size_t)sorted_slots[row0 + m] * r + c];
+    zs[i] = __ldcg(Z + (size_t)__ldcg(sorted_slots + row0 + m) * r + c);
+  }
+  __syncthreads();
+  float acc0[kMaxBmLora], acc1[kMaxBmLora];
+#pragma unroll
+  for (int m = 0; m < kMaxBmLora; ++m) {
+    acc0[m] = 0.f;
+    acc1[m] = 0.f;
+    if (m < rows) {
+      if (RV > 0) {
+#pragma unroll
+        for (int i = 0; i < RV; ++i) {
+          fma8(acc0[m], zs + m * r + 8 * i, b0[i]);
+          fma8(acc1[m], zs + m * r + 8 * i, b1[i]);
+        }
+      } else {
+        if (n0 < N) acc0[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n0 * r, r);
+        if (n1 < N) acc1[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n1 * r, r);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxBmLora; ++m) {
+    if (m < rows) {
+      float* o = base + (size_t)(row0 + m) * N;
+      if (n0 < N) o[n0] += acc0[m];
+      if (n1 < N) o[n1] += acc1[m];
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// epilogue 1: h[row, n] = silu(g) * u for every valid sorted row, with
+//   g = G[row, n] + z.B[l, e, n],  u = G[row, I + n] + z.B[l, e, I + n].
+// A CTA owns `rows_per_cta` consecutive sorted rows and 256 columns. With one row
+// per CTA (short (expert, adapter) segments, e.g. decode) every load of a thread
+// -- the G pair and both B rows -- is in flight at once, before the wait for z.
+// With more rows (long segments, e.g. prefill) rows sorted by (e, l) share the B
+// row pair, which stays in registers, and G is fetched four rows at a time.
+// ----------------------------------------------------------------------------
+template <int RV>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_swiglu_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+                         const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
+                         const int* __restrict__ row_expert, const int* __restrict__ row_adapter,
+                         int I, int r, int E, const float* __restrict__ G,
+                         __nv_bfloat16* __restrict__ h, int rows_per_cta, int early) {
+  extern __shared__ float zs[];  // [rows_per_cta][r]
+  __shared__ int s_key[64];      // e * 65536 + (l + 1), or -1 without adapter
+  __shared__ int s_slot[64];
+  if (!early) pdl_wait();
+  const int n_valid = __ldcg(hdr + HDR_NVALID);
+  const int r0 = blockIdx.x * rows_per_cta;
+  if (r0 >= n_valid) {
+    if (early) pdl_wait();
+    return;
+  }
+  const int rows = min(rows_per_cta, n_valid - r0);
+  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
+  const bool col = n < I;
+  const size_t twoI = 2 * (size_t)I;
+  if (threadIdx.x < rows) {
+    const int row = r0 + threadIdx.x;
+    const int l = B ? __ldcg(row_adapter + row) : -1;
+    s_key[threadIdx.x] = l < 0 ? -1 : __ldcg(row_expert + row) * 65536 + l + 1;
+    s_slot[threadIdx.x] = __ldcg(sorted_slots + row);
+  }
+  __syncthreads();
+  uint4 bg[RV > 0 ? RV : 1], bu[RV > 0 ? RV : 1];
+  int cur = -1;
+  auto load_b = [&](int key) {
+    const int e = key >> 16, l = (key & 0xffff) - 1;
+    const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+      bg[i] = __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n * r) + i);
+      bu[i] = __ldg(reinterpret_cast<const uint4*>(bl + (size_t)(I + n) * r) + i);
+    }
+  };
+  // G values are fetched four rows at a time; the first batch and the first B rows
+  // are older than the predecessor and go out before the wait
+  constexpr int RB = 4;
+  float gv[RB], uv[RB];
+  auto load_g = [&](int m0) {
+#pragma unroll
+    for (int q = 0; q < RB; ++q) {
+      gv[q] = 0.f;
+      uv[q] = 0.f;
+      if (col && m0 + q < rows) {
+        gv[q] = __ldcg(G + (size_t)(r0 + m0 + q) * twoI + n);
+        uv[q] = __ldcg(G + (size_t)(r0 + m0 + q) * twoI + I + n);
+      }
+    }
+  };
+  if (early) {
+    load_g(0);
+    if (col && RV > 0 && s_key[0] >= 0) {
+      load_b(s_key[0]);
+      cur = s_key[0];
+    }
+    pdl_wait();
+  }
+  pdl_trigger();
+  if (!early) load_g(0);
+  if (B) {
+    for (int i = threadIdx.x; i < rows * r; i += blockDim.x) {
+      const int m = i / r, c = i - m * r;
+      zs[i] = s_key[m] >= 0 ? __ldcg(Z + (size_t)s_slot[m] * r + c) : 0.f;
+    }
+  }
+  __syncthreads();
+  if (!col) return;
+  for (int m0 = 0; m0 < rows; m0 += RB) {
+    if (m0 > 0) load_g(m0);
+#pragma unroll
+    for (int q = 0; q < RB; ++q) {
+      const int m = m0 + q;
+      if (m >= rows) break;
+      const int key = s_key[m];
+      float g = gv[q], u = uv[q];
+      if (key >= 0) {
+        if (RV > 0) {
+          if (key != cur) {
+            load_b(key);
+            cur = key;
+          }
+#pragma unroll
+          for (int i = 0; i < RV; ++i) {
+            fma8(g, zs + m * r + 8 * i, bg[i]);
+            fma8(u, zs + m * r + 8 * i, bu[i]);
+          }
+        } else {
+          const int e = key >> 16, l = (key & 0xffff) - 1;
+          const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+          g += dot_zb_mem<false>(zs + m * r, bl + (size_t)n * r, r);
+          u += dot_zb_mem<false>(zs + m * r, bl + (size_t)(I + n) * r, r);
+        }
+      }
+      h[(size_t)(r0 + m) * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// epilogue 2: y[t, n] = sum_j w[t, j] * (O[row(t,j), n] + z[t k + j] . B[l, e_j, n, :]),
+// j ascending, one thread per column, `tokens_per_cta` tokens per CTA. O values,
+// B rows, routing weights and align tables are all older than the predecessor
+// (the down shrink) and the first slot's are fetched before the wait; only z
+// waits. The next slot's O value and B rows are fetched while the current slot
+// is reduced.
+// ----------------------------------------------------------------------------
+template <int RV, bool kOutF32>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_combine_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+                          const int* __restrict__ slot_row, const int* __restrict__ row_expert,
+                          const int* __restrict__ row_adapter, const float* __restrict__ w,
+                          int T, int k, int N, int r, int E, const float* __restrict__ O,
+                          void* __restrict__ y, int tokens_per_cta, int early) {
+  extern __shared__ float zs[];  // [tokens_per_cta * k][r]
+  __shared__ int s_row[256], s_key[256];
+  __shared__ float s_w[256];
+  if (!early) pdl_wait();
+  const int t0 = blockIdx.x * tokens_per_cta;
+  const int nt = min(tokens_per_cta, T - t0);
+  const int ns = nt * k;  // slots of this CTA (the host keeps tokens_per_cta * k <= 256)
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const size_t s = (size_t)t0 * k + i;
+    const int row = __ldcg(slot_row + s);
+    int key = -1;
+    if (row >= 0 && B) {
+      const int l = __ldcg(row_adapter + row);
+      if (l >= 0) key = __ldcg(row_expert + row) * 65536 + l + 1;
+    }
+    s_row[i] = row;
+    s_key[i] = key;
+    s_w[i] = __ldcg(w + s);
   }
   __syncthreads();
   const int n = blockIdx.y * kExpandThreads + threadIdx.x;
-  if (n >= N) return;
-  const __nv_bfloat16* brow = B + (((size_t)l * E + e) * N + n) * (size_t)r;
-  float acc[kMaxBmLora];
-  if (kVecB) {
-    // read the B row once, apply it to every row of the block
+  const bool col = n < N;
+  auto brow = [&](int key) {
+    const int e = key >> 16, l = (key & 0xffff) - 1;
+    return B + (((size_t)l * E + e) * N + n) * (size_t)r;
+  };
+  uint4 bcur[RV > 0 ? RV : 1], bnext[RV > 0 ? RV : 1];
+  auto load_slot = [&](int q, float& o, uint4 (&bv)[RV > 0 ? RV : 1]) {
+    if (s_row[q] >= 0) o = __ldcg(O + (size_t)s_row[q] * N + n);
+    if (RV > 0 && s_key[q] >= 0) {
+      const uint4* p = reinterpret_cast<const uint4*>(brow(s_key[q]));
 #pragma unroll
-    for (int m = 0; m < kMaxBmLora; ++m) acc[m] = 0.f;
-    const uint4* b4 = reinterpret_cast<const uint4*>(brow);
-    for (int i = 0; i < r; i += 8) {
-      const uint4 u = __ldg(b4 + (i >> 3));
-      const float bv[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-#pragma unroll
-      for (int m = 0; m < kMaxBmLora; ++m) {
-        if (m < rows) {
-          const float* z = zs + m * r + i;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[m] = fmaf(z[j], bv[j], acc[m]);
-        }
-      }
+      for (int i = 0; i < RV; ++i) bv[i] = __ldg(p + i);
     }
-  } else {
-#pragma unroll
-    for (int m = 0; m < kMaxBmLora; ++m) acc[m] = m < rows ? dot_zb<false>(zs + m * r, brow, r) : 0.f;
-  }
-#pragma unroll
-  for (int m = 0; m < kMaxBmLora; ++m)
-    if (m < rows) base[(size_t)(row0 + m) * N + n] += acc[m];
-}
-
-// epilogue 1: h[row, n] = silu(g) * u over every row of each token tile, with
-// g = G[row, n] + z.B[l, e, n], u = G[row, I + n] + z.B[l, e, I + n].
-template <bool kVecB>
-__global__ void __launch_bounds__(kExpandThreads)
-    expand_swiglu_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
-                         const int* __restrict__ hdr, const int4* __restrict__ tiles,
-                         const int* __restrict__ sorted_slots, const int* __restrict__ row_adapter,
-                         int I, int r, int E, const float* __restrict__ G,
-                         __nv_bfloat16* __restrict__ h) {
-  extern __shared__ float zs[];  // [kSwigluRowChunk][r]
-  __shared__ int s_l[kSwigluRowChunk];
-  pdl_wait();
-  const int nt = hdr[HDR_NTILES];
-  if ((int)blockIdx.x >= nt) return;
+  };
+  float o_cur = 0.f;
+  if (early && col && ns > 0) load_slot(0, o_cur, bcur);
+  if (early) pdl_wait();
   pdl_trigger();
-  const int4 tile = tiles[blockIdx.x];
-  const int e = tile.x, row0 = tile.y, rows = tile.z;
-  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
-  const size_t twoI = 2 * (size_t)I;
-  for (int c0 = 0; c0 < rows; c0 += kSwigluRowChunk) {
-    const int cr = min(kSwigluRowChunk, rows - c0);
-    __syncthreads();
-    if (threadIdx.x < cr) s_l[threadIdx.x] = B ? row_adapter[row0 + c0 + threadIdx.x] : -1;
-    __syncthreads();
-    if (B) {
-      for (int i = threadIdx.x; i < cr * r; i += blockDim.x) {
-        const int m = i / r, c = i - m * r;
-        zs[i] = s_l[m] >= 0 ? Z[(size_t)sorted_slots[row0 + c0 + m] * r + c] : 0.f;
-      }
-    }
-    __syncthreads();
-    if (n < I) {
-      for (int m = 0; m < cr; ++m) {
-        const int row = row0 + c0 + m;
-        float g = G[(size_t)row * twoI + n];
-        float u = G[(size_t)row * twoI + I + n];
-        const int l = s_l[m];
-        if (l >= 0) {
-          const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
-          g += dot_zb<kVecB>(zs + m * r, bl + (size_t)n * r, r);
-          u += dot_zb<kVecB>(zs + m * r, bl + (size_t)(I + n) * r, r);
-        }
-        const float sg = g / (1.f + expf(-g));
-        h[(size_t)row * I + n] = __float2bfloat16_rn(sg * u);
-      }
+  if (B) {
+    for (int i = threadIdx.x; i < ns * r; i += blockDim.x) {
+      const int q = i / r, c = i - q * r;
+      zs[i] = s_key[q] >= 0 ? __ldcg(Z + ((size_t)t0 * k + q) * r + c) : 0.f;
     }
   }
-}
-
-// Weighted top-k combine: y[t, n] = sum_j w[t, j] * O[row(t, j), n], j ascending.
-template <bool kOutF32>
-__global__ void __launch_bounds__(kExpandThreads)
-    combine_kernel(const float* __restrict__ O, const float* __restrict__ w,
-                   const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y) {
-  pdl_wait();
-  pdl_trigger();
-  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
-  if (n >= N) return;
-  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+  __syncthreads();
+  if (!col) return;
+  if (!early && ns > 0) load_slot(0, o_cur, bcur);
+  for (int ti = 0; ti < nt; ++ti) {
     float acc = 0.f;
     for (int j = 0; j < k; ++j) {
-      const int row = slot_row[(size_t)t * k + j];
-      if (row >= 0) acc = fmaf(w[(size_t)t * k + j], O[(size_t)row * N + n], acc);
+      const int q = ti * k + j;
+      float o_next = 0.f;
+      if (q + 1 < ns) load_slot(q + 1, o_next, bnext);
+      if (s_row[q] >= 0) {
+        float o = o_cur;
+        if (s_key[q] >= 0) {
+          if (RV > 0) {
+#pragma unroll
+            for (int i = 0; i < RV; ++i) fma8(o, zs + q * r + 8 * i, bcur[i]);
+          } else {
+            o += dot_zb_mem<false>(zs + q * r, brow(s_key[q]), r);
+          }
+        }
+        acc = fmaf(s_w[q], o, acc);
+      }
+      o_cur = o_next;
+#pragma unroll
+      for (int i = 0; i < (RV > 0 ? RV : 1); ++i) bcur[i] = bnext[i];
     }
-    if (kOutF32) static_cast<float*>(y)[(size_t)t * N + n] = acc;
-    else static_cast<__nv_bfloat16*>(y)[(size_t)t * N + n] = __float2bfloat16_rn(acc);
+    const size_t yi = (size_t)(t0 + ti) * N + n;
+    if (kOutF32) static_cast<float*>(y)[yi] = acc;
+    else static_cast<__nv_bfloat16*>(y)[yi] = __float2bfloat16_rn(acc);
   }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+template <template <int> class K, typename... Args>
+static int launch_rv(int rv, dim3 grid, size_t smem, cudaStream_t stream, bool pdl,
+                     Args... args) {
+  switch (rv) {
+    case 1: return launch_pdl(K<1>::fn, grid, kExpandThreads, smem, stream, pdl, args...);
+    case 2: return launch_pdl(K<2>::fn, grid, kExpandThreads, smem, stream, pdl, args...);
+    case 4: return launch_pdl(K<4>::fn, grid, kExpandThreads, smem, stream, pdl, args...);
+    case 8: return launch_pdl(K<8>::fn, grid, kExpandThreads, smem, stream, pdl, args...);
+    default: return launch_pdl(K<0>::fn, grid, kExpandThreads, smem, stream, pdl, args...);
+  }
+}
+template <int RV> struct AddK { static constexpr auto fn = expand_add_kernel<RV>; };
+template <int RV> struct SwigluK { static constexpr auto fn = expand_swiglu_kernel<RV>; };
+
+// r / 8 when the B rows can sit in registers with 128-bit loads, else 0.
+static int reg_ranks(int r, const void* B) {
+  if (r % 8 != 0 || r > kMaxRegRank || !aligned16(B)) return 0;
+  const int rv = r / 8;
+  return (rv == 1 || rv == 2 || rv == 4 || rv == 8) ? rv : 0;
+}
+
+int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al,
+                       const AlignLayout& a, int N, int r, int epilogue, float* base, void* out,
+                       int out_fp32, const float* topk_w, cudaStream_t stream, bool pdl,
+                       bool early) {
+  if (a.S == 0) return MOE_LORA_OK;
+  AlignView v = align_view(al->buf, a);
+  const auto* Bp = (al->L > 0) ? static_cast<const __nv_bfloat16*>(B) : nullptr;
+  const int rv = Bp ? reg_ranks(r, B) : 1;
+  const int rr = Bp ? r : 0;
+  const int sms = num_sms();
+  const int ea = early ? 1 : 0;
+  if (epilogue == 0) {
+    if (!Bp) return MOE_LORA_OK;
+    const dim3 grid(a.max_blocks, ceil_div(N, 2 * kExpandThreads));
+    const size_t smem = (size_t)kMaxBmLora * r * sizeof(float);
+    return launch_rv<AddK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
+                           (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base,
+                           ea);
+  }
+  if (epilogue == 1) {
+    const int I = N / 2;
+    const int ncol = ceil_div(I, kExpandThreads);
+    // rows per CTA ~ the mean (expert, adapter) segment length, so that a CTA's rows
+    // share B rows; but enough CTAs to cover the SMs a few times over
+    const int64_t segs = (int64_t)al->E * (al->L + 1);
+    int rpc = 1;
+    while (rpc < 64 && (int64_t)rpc * 2 * segs <= a.S) rpc *= 2;
+    while (rpc > 1 && (int64_t)ceil_div(a.S, rpc) * ncol < 4 * sms) rpc /= 2;
+    const dim3 grid(ceil_div(a.S, rpc), ncol);
+    const size_t smem = (size_t)rpc * rr * sizeof(float);
+    auto* hp = static_cast<__nv_bfloat16*>(out);
+    return launch_rv<SwigluK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
+                              (const int*)v.sorted_slots, (const int*)v.row_expert,
+                              (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp,
+                              rpc, ea);
+  }
+  if (epilogue == 2) {
+    const int ncol = ceil_div(N, kExpandThreads);
+    int tpc = 1;
+    while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms &&
+           tpc * 2 * al->k <= 256 && (int64_t)tpc * 2 * al->k * rr * 4 <= 32 * 1024)
+      tpc *= 2;
+    const dim3 grid(ceil_div(al->T, tpc), ncol);
+    const size_t smem = (size_t)tpc * al->k * rr * sizeof(float);
+    auto go = [&](auto kern) {
+      return launch_pdl(kern, grid, kExpandThreads, smem, stream, pdl, Z, Bp,
+                        (const int*)v.slot_row, (const int*)v.row_expert,
+                        (const int*)v.row_adapter, topk_w, al->T, al->k, N, r, al->E,
+                        (const float*)base, out, tpc, ea);
+    };
+    if (out_fp32) {
+      switch (rv) {
+        case 1: return go(expand_combine_kernel<1, true>);
+        case 2: return go(expand_combine_kernel<2, true>);
+        case 4: return go(expand_combine_kernel<4, true>);
+        case 8: return go(expand_combine_kernel<8, true>);
+        default: return go(expand_combine_kernel<0, true>);
+      }
+    }
+    switch (rv) {
+      case 1: return go(expand_combine_kernel<1, false>);
+      case 2: return go(expand_combine_kernel<2, false>);
+      case 4: return go(expand_combine_kernel<4, false>);
+      case 8: return go(expand_combine_kernel<8, false>);
+      default: return go(expand_combine_kernel<0, false>);
+    }
+  }
+  return MOE_LORA_ERR_INVALID_ARG;
 }
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,
                   int N, int r, int epilogue, float* base, void* out, int out_fp32,
                   const float* topk_w, cudaStream_t stream, bool pdl) {
-  if (a.S == 0) return MOE_LORA_OK;
-  AlignView v = align_view(al->buf, a);
-  const auto* Bp = (al->L > 0) ? static_cast<const __nv_bfloat16*>(B) : nullptr;
-  const bool vecB = (r % 8 == 0) && aligned16(B);
-  int st = MOE_LORA_OK;
-  if (epilogue == 0 || epilogue == 2) {
-    if (Bp) {
-      const dim3 grid(a.max_blocks, ceil_div(N, kExpandThreads));
-      const size_t smem = (size_t)kMaxBmLora * r * sizeof(float);
-      st = vecB ? launch_pdl(expand_add_kernel<true>, grid, kExpandThreads, smem, stream, pdl, Z,
-                             Bp, (const int*)v.hdr, (const int4*)v.blocks,
-                             (const int*)v.sorted_slots, N, r, al->E, base)
-                : launch_pdl(expand_add_kernel<false>, grid, kExpandThreads, smem, stream, pdl, Z,
-                             Bp, (const int*)v.hdr, (const int4*)v.blocks,
-                             (const int*)v.sorted_slots, N, r, al->E, base);
-      if (st != MOE_LORA_OK) return st;
-    }
-    if (epilogue == 2) {
-      int bx = al->T < 65535 ? al->T : 65535;
-      const dim3 grid(bx, ceil_div(N, kExpandThreads));
-      st = out_fp32 ? launch_pdl(combine_kernel<true>, grid, kExpandThreads, 0, stream, pdl,
-                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
-                                 N, out)
-                    : launch_pdl(combine_kernel<false>, grid, kExpandThreads, 0, stream, pdl,
-                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
-                                 N, out);
-    }
-    return st;
-  }
-  if (epilogue == 1) {
-    const int I = N / 2;
-    const dim3 grid(a.max_tiles, ceil_div(I, kExpandThreads));
-    const size_t smem = (size_t)kSwigluRowChunk * r * sizeof(float);
-    auto* hp = static_cast<__nv_bfloat16*>(out);
-    return vecB ? launch_pdl(expand_swiglu_kernel<true>, grid, kExpandThreads, smem, stream, pdl,
-                             Z, Bp, (const int*)v.hdr, (const int4*)v.tiles,
-                             (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
-                             (const float*)base, hp)
-                : launch_pdl(expand_swiglu_kernel<false>, grid, kExpandThreads, smem, stream, pdl,
-                             Z, Bp, (const int*)v.hdr, (const int4*)v.tiles,
-                             (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
-                             (const float*)base, hp);
-  }
-  return MOE_LORA_ERR_INVALID_ARG;
+  return launch_expand_impl(Z, B, al, a, N, r, epilogue, base, out, out_fp32, topk_w, stream, pdl,
+                            false);
 }
 
 }  // namespace moe_lora
@@ -220,6 +431,7 @@ extern "C" int lora_expand_add(const float* Z, const void* B, const moe_lora_ali
   if (st != MOE_LORA_OK) return st;
   if (N < 1 || epilogue < 0 || epilogue > 2) return MOE_LORA_ERR_INVALID_ARG;
   if (al->L > 0 && (r < 1 || r > 256)) return r < 1 ? MOE_LORA_ERR_INVALID_ARG : MOE_LORA_ERR_UNSUPPORTED;
+  if (al->L >= 65535 || al->E >= 32768) return MOE_LORA_ERR_UNSUPPORTED;  // packed (e, l) keys
   if (epilogue == 1 && N % 2 != 0) return MOE_LORA_ERR_INVALID_ARG;
   if (a.S > 0) {
     if (!base) return MOE_LORA_ERR_INVALID_ARG;

@@ -21,19 +21,24 @@ namespace moe_lora {
 
 constexpr int kShrinkWarps = 8;
 
-template <bool kVec, bool kEvenK>
+// kCoherent: the row may have been written by an earlier launch (activations), so it
+// is read at L2 (ld.global.cg); weights take the read-only path.
+template <bool kVec, bool kEvenK, bool kCoherent = false>
 __device__ __forceinline__ uint4 load8_bf16(const __nv_bfloat16* p, int kofs, int K) {
   uint4 r = make_uint4(0u, 0u, 0u, 0u);
   if (p == nullptr) return r;
   if (kVec) {
-    if (kEvenK || kofs < K) r = __ldg(reinterpret_cast<const uint4*>(p + kofs));
+    if (kEvenK || kofs < K) {
+      const uint4* q = reinterpret_cast<const uint4*>(p + kofs);
+      r = kCoherent ? __ldcg(q) : __ldg(q);
+    }
   } else {
     const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = (kofs + 2 * i < K) ? q[kofs + 2 * i] : 0u;
-      const uint32_t hi = (kofs + 2 * i + 1 < K) ? q[kofs + 2 * i + 1] : 0u;
+      const uint32_t lo = (kofs + 2 * i < K) ? __ldcg(q + kofs + 2 * i) : 0u;
+      const uint32_t hi = (kofs + 2 * i + 1 < K) ? __ldcg(q + kofs + 2 * i + 1) : 0u;
       w[i] = lo | (hi << 16);
     }
     r = make_uint4(w[0], w[1], w[2], w[3]);
@@ -50,44 +55,47 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT, bool kVec, bool kEvenK>
+template <int NT, int U, bool kVec, bool kEvenK>
 __global__ void __launch_bounds__(kShrinkWarps * 32)
     lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
-                       int K, int r, int E, float* __restrict__ Z, int ngroups) {
+                       int K, int r, int E, float* __restrict__ Z, int ngroups, int early) {
   constexpr int R = 8 * NT;  // ranks per CTA
   __shared__ float red[kShrinkWarps][16][R + 1];
 
-  pdl_wait();
-  const int nb = hdr[HDR_NBLOCKS];
+  // With `early` every input was produced two or more launches back (see
+  // lora_expand.cu on launch ordering): compute first, wait only before publishing.
+  if (!early) pdl_wait();
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
   const int b = blockIdx.x / ngroups;
   const int g = blockIdx.x - b * ngroups;
-  if (b >= nb) return;
-  pdl_trigger();
-  const int4 blk = blocks[b];
+  if (b >= nb) {
+    if (early) pdl_wait();
+    return;
+  }
+  if (!early) pdl_trigger();
+  const int4 blk = __ldcg(blocks + b);
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, q = lane & 3;
 
-  const __nv_bfloat16* x0 = nullptr;
-  const __nv_bfloat16* x1 = nullptr;
-  if (gid < rows) {
-    const int row = row0 + gid;
-    const int in = rows_are_slots ? row : sorted_slots[row] / k;
-    x0 = X + (size_t)in * K;
-  }
-  if (gid + 8 < rows) {
-    const int row = row0 + gid + 8;
-    const int in = rows_are_slots ? row : sorted_slots[row] / k;
-    x1 = X + (size_t)in * K;
-  }
   const __nv_bfloat16* Ab = A + ((size_t)l * E + e) * (size_t)r * K;
   const __nv_bfloat16* ap[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int rank = g * R + nt * 8 + gid;
     ap[nt] = rank < r ? Ab + (size_t)rank * K : nullptr;
+  }
+  const __nv_bfloat16* x0 = nullptr;
+  const __nv_bfloat16* x1 = nullptr;
+  if (gid < rows) {
+    const int row = row0 + gid;
+    x0 = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
+  }
+  if (gid + 8 < rows) {
+    const int row = row0 + gid + 8;
+    x1 = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
   }
 
   float acc[NT][4];
@@ -96,31 +104,30 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
 
   const int nsteps = (K + 31) >> 5;
   int st = warp;
-  // two steps per iteration: all loads first, then the MMAs
-  for (; st + kShrinkWarps < nsteps; st += 2 * kShrinkWarps) {
-    const int k0 = st * 32 + q * 8, k1 = k0 + kShrinkWarps * 32;
-    const uint4 xa0 = load8_bf16<kVec, kEvenK>(x0, k0, K);
-    const uint4 xb0 = load8_bf16<kVec, kEvenK>(x1, k0, K);
-    const uint4 xa1 = load8_bf16<kVec, kEvenK>(x0, k1, K);
-    const uint4 xb1 = load8_bf16<kVec, kEvenK>(x1, k1, K);
-    uint4 av0[NT], av1[NT];
+  // U steps per iteration: every load of the batch is issued before the first MMA
+  for (; st + (U - 1) * kShrinkWarps < nsteps; st += U * kShrinkWarps) {
+    uint4 xa[U], xb[U], av[U][NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      av0[nt] = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
-      av1[nt] = load8_bf16<kVec, kEvenK>(ap[nt], k1, K);
+    for (int u = 0; u < U; ++u) {
+      const int k0 = (st + u * kShrinkWarps) * 32 + q * 8;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) av[u][nt] = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
+      xa[u] = load8_bf16<kVec, kEvenK, true>(x0, k0, K);
+      xb[u] = load8_bf16<kVec, kEvenK, true>(x1, k0, K);
     }
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      mma_16816(acc[nt], xa0.x, xb0.x, xa0.y, xb0.y, av0[nt].x, av0[nt].y);
-      mma_16816(acc[nt], xa0.z, xb0.z, xa0.w, xb0.w, av0[nt].z, av0[nt].w);
-      mma_16816(acc[nt], xa1.x, xb1.x, xa1.y, xb1.y, av1[nt].x, av1[nt].y);
-      mma_16816(acc[nt], xa1.z, xb1.z, xa1.w, xb1.w, av1[nt].z, av1[nt].w);
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_16816(acc[nt], xa[u].x, xb[u].x, xa[u].y, xb[u].y, av[u][nt].x, av[u][nt].y);
+        mma_16816(acc[nt], xa[u].z, xb[u].z, xa[u].w, xb[u].w, av[u][nt].z, av[u][nt].w);
+      }
     }
   }
-  if (st < nsteps) {
+  for (; st < nsteps; st += kShrinkWarps) {
     const int k0 = st * 32 + q * 8;
-    const uint4 xa0 = load8_bf16<kVec, kEvenK>(x0, k0, K);
-    const uint4 xb0 = load8_bf16<kVec, kEvenK>(x1, k0, K);
+    const uint4 xa0 = load8_bf16<kVec, kEvenK, true>(x0, k0, K);
+    const uint4 xb0 = load8_bf16<kVec, kEvenK, true>(x1, k0, K);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const uint4 a = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
@@ -138,6 +145,10 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
     red[warp][gid + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
   }
   __syncthreads();
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   for (int idx = threadIdx.x; idx < rows * R; idx += blockDim.x) {
     const int m = idx / R, c = idx - m * R;
     const int rank = g * R + c;
@@ -145,38 +156,37 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < kShrinkWarps; ++w) s += red[w][m][c];
-    Z[(size_t)sorted_slots[row0 + m] * r + rank] = s;
+    Z[(size_t)__ldcg(sorted_slots + row0 + m) * r + rank] = s;
   }
 }
 
-template <int NT>
+template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
-                            float* Z, bool vec, cudaStream_t stream, bool pdl) {
+                            float* Z, bool vec, cudaStream_t stream, bool pdl, int early) {
   const int ngroups = ceil_div(r, 8 * NT);
   const int64_t grid = (int64_t)max_blocks * ngroups;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
   const dim3 g((unsigned)grid);
-  if (vec && K % 32 == 0)
-    return launch_pdl(lora_shrink_kernel<NT, true, true>, g, kShrinkWarps * 32, 0, stream, pdl, X,
-                      rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
-                      (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
-  if (vec)
-    return launch_pdl(lora_shrink_kernel<NT, true, false>, g, kShrinkWarps * 32, 0, stream, pdl, X,
-                      rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
-                      (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
-  return launch_pdl(lora_shrink_kernel<NT, false, false>, g, kShrinkWarps * 32, 0, stream, pdl, X,
-                    rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
-                    (const int*)v.sorted_slots, k, K, r, E, Z, ngroups);
+  auto args = [&](auto kern) {
+    return launch_pdl(kern, g, kShrinkWarps * 32, 0, stream, pdl, X, rows_are_slots, A,
+                      (const int*)v.hdr, (const int4*)v.blocks, (const int*)v.sorted_slots, k, K,
+                      r, E, Z, ngroups, early);
+  };
+  if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true>);
+  if (vec) return args(lora_shrink_kernel<NT, U, true, false>);
+  return args(lora_shrink_kernel<NT, U, false, false>);
 }
 
-int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
-                  const AlignLayout& a, int K, int r, float* Z, cudaStream_t stream, bool pdl) {
+int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
+                       const moe_lora_align_t* al, const AlignLayout& a, int K, int r, float* Z,
+                       cudaStream_t stream, bool pdl, bool early) {
   if (a.S == 0 || al->L == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   const auto* Xp = static_cast<const __nv_bfloat16*>(X);
   const auto* Ap = static_cast<const __nv_bfloat16*>(A);
   const bool vec = (K % 8 == 0) && aligned16(X) && aligned16(A);
+  const int ea = early ? 1 : 0;
   // Few blocks (decode): one 8-rank group per CTA to spread the A stream over
   // many CTAs. Many blocks (prefill): all ranks in one CTA so that X is read once.
   const int blocks_est = a.max_blocks;
@@ -187,11 +197,16 @@ int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lo
   else if (r <= 32) nt = 4;
   else nt = 8;
   switch (nt) {
-    case 1: return launch_shrink_nt<1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
-    case 2: return launch_shrink_nt<2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
-    case 4: return launch_shrink_nt<4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
-    default: return launch_shrink_nt<8>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl);
+    case 1: return launch_shrink_nt<1, 4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
+    case 2: return launch_shrink_nt<2, 4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
+    case 4: return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
+    default: return launch_shrink_nt<8, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
   }
+}
+
+int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
+                  const AlignLayout& a, int K, int r, float* Z, cudaStream_t stream, bool pdl) {
+  return launch_shrink_impl(X, rows_are_slots, A, al, a, K, r, Z, stream, pdl, false);
 }
 
 }  // namespace moe_lora

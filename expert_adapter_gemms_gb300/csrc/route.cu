@@ -11,6 +11,8 @@ template <int V>  // logits held per lane: experts lane, lane+32, ..., lane+32(V
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T,
                                                            int E, int k, int* __restrict__ ids,
                                                            float* __restrict__ w) {
+  // the next launch (align) waits before reading ids/w, so it may start right away
+  pdl_trigger();
   pdl_wait();
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -22,7 +24,7 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
       const int e = lane + 32 * i;
       float x = -INFINITY;
       if (e < E) {
-        x = logits[(size_t)t * E + e];
+        x = __ldcg(logits + (size_t)t * E + e);
         if (isnan(x)) x = -INFINITY;  // NaN ranks below every number
       } else {
         taken |= 1u << i;
@@ -67,7 +69,6 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
       w[(size_t)t * k + lane] = ex / sum;
     }
   }
-  pdl_trigger();
 }
 
 int launch_topk_softmax(const float* logits, int T, int E, int k, int* ids, float* w,

@@ -192,9 +192,9 @@ MOE_LORA_API int lora_shrink(const void* X, int rows_are_slots, const void* A, c
  *               every valid row (with or without adapter). N must be even.
  *   epilogue 2: out[t, n] = sum_j w[t, j] * (base[row(t,j), n] + delta[row(t,j), n]),
  *               j in increasing order; out [T, N] bf16 (out_fp32 = 0) or fp32.
- *               base is updated in place as in epilogue 0.
+ *               base is only read.
  * Z [S, r] fp32; B [L, E, N, r] bf16 (NULL or L = 0: no adapter term);
- * topk_w [T, k] fp32 (epilogue 2 only). Deterministic.
+ * topk_w [T, k] fp32 (epilogue 2 only). Requires L < 65535. Deterministic.
  * ------------------------------------------------------------------------- */
 MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_align_t* al, int N, int r,
                     int epilogue, float* base, void* out, int out_fp32, const float* topk_w,
@@ -210,7 +210,7 @@ MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_a
  * token_adapter [T] int32 or NULL. LoRA weights may be NULL with L = 0 (base MoE).
  * y [T, H]: bf16 (y_fp32 = 0) or fp32. workspace: moe_lora_workspace_size bytes,
  * 256-byte aligned; its first bytes are the layer's align buffer (error word).
- * Requires H % 8 == 0, I % 8 == 0, 1 <= k <= min(E, 32), E <= 1024.
+ * Requires H % 8 == 0, I % 8 == 0, 1 <= k <= min(E, 32), E <= 1024, L < 65535.
  * ------------------------------------------------------------------------- */
 MOE_LORA_API size_t moe_lora_workspace_size(int T, int k, int E, int L, int H, int I, int r);
 

@@ -188,3 +188,39 @@ def test_expand_combine(out_fp32):
         assert_close(y.t, expect, KERNEL_RTOL, "combine fp32")
     else:
         assert_bf16_close(y.t, expect, "combine bf16")
+
+
+def test_expand_swiglu_many_rows_per_cta():
+    """Long (expert, adapter) segments: 16 sorted rows per CTA sharing B rows in registers,
+    G fetched four rows at a time."""
+    m, inp, ids, w, al, ref = _setup(T=2048, H=64, I=2048, E=2, k=1, L=2, r=16, seed=12,
+                                     bm_base=256)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(4)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, 16))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 4096), dtype=np.float32))
+    h = m.lora_expand_add(dev(Zh), dev(inp.B1), al, 1, dev(G))
+    expect = oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1)
+    assert_bf16_close(h[:n], expect, "expand epilogue 1, long segments")
+
+
+@pytest.mark.parametrize("k", [1, 4])
+def test_expand_combine_many_tokens_per_cta(k):
+    """Several tokens per CTA in the fused down expand + combine."""
+    m, inp, ids, w, al, ref = _setup(T=4096, H=256, I=16, E=8, k=k, L=3, r=16, seed=13)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(5)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, 16))).to(torch.float32)
+    O = torch.from_numpy(rng.standard_normal((al.S, 256), dtype=np.float32))
+    wt = torch.as_tensor(w, dtype=torch.float32)
+    y = m.lora_expand_add(dev(Zh), dev(inp.B2), al, 2, dev(O), out_fp32=True, topk_w=dev(wt))
+    expect = oracle.lora_expand_add(Zh, inp.B2, ref, O[:n], epilogue=2, w=wt)
+    assert_close(y, expect, KERNEL_RTOL, "combine, many tokens per CTA")
+
+
+@pytest.mark.parametrize("r,T", [(16, 4096), (32, 2048), (64, 2048)])
+def test_shrink_many_blocks(r, T):
+    """Enough LoRA blocks that one CTA takes 16-64 ranks (prefill-like)."""
+    m, inp, ids, w, al, ref = _setup(T=T, H=256, I=8, E=8, k=4, L=8, r=r, seed=14)
+    Z = m.lora_shrink(dev(inp.x), False, dev(inp.A1), al)
+    assert_close(Z, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"shrink r={r}")

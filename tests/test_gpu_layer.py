@@ -152,3 +152,17 @@ def test_layer_caller_routing_and_no_pdl():
                      token_adapter=dev(inp.token_adapter), A1=dev(inp.A1), B1=dev(inp.B1),
                      A2=dev(inp.A2), B2=dev(inp.B2), y=y, y_fp32=True, disable_pdl=True)
     assert_close(y.cpu(), oracle_layer(inp), LAYER_RTOL, "caller routing")
+
+
+def test_layer_skewed_decode_multi_chunk():
+    """Few rows per expert on average (the gate_up GEMM runs one CTA per expert and
+    weight block) but Zipf-skewed: the top expert's rows span four chunks and some
+    experts receive no token at all."""
+    m = need_gpu()
+    inp = make_layer_inputs(T=128, H=128, I=96, E=16, k=2, L=3, r=16, seed=95,
+                            routing="zipf2.0", lora_std=None)
+    ids, _ = oracle.route_topk_softmax(inp.logits, inp.k)
+    counts = np.bincount(ids.reshape(-1), minlength=inp.E)
+    assert counts.max() > 96 and (counts == 0).any()  # four chunks of 32; idle experts
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    assert_close(y, oracle_layer(inp), LAYER_RTOL, "skewed decode")
