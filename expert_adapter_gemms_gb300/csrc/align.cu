@@ -6,11 +6,11 @@
 // One CTA (256 threads up to 4096 slots, 1024 beyond). Each slot s gets the
 // packed word (key << slot_bits) | s with key = e * (L + 1) + (l + 1) (dropped
 // slots use the last bucket). A stable least-significant-digit radix sort on the
-// key bits (8-bit digits, per-warp digit histograms, ranks from
-// __match_any_sync) keeps equal keys in slot order, so the result is the unique
-// stable order: deterministic and bit-exact. Bucket counts give the expert and
-// (expert, adapter) segment boundaries, from which the grouped-GEMM token tiles
-// and the LoRA blocks are cut. Working state (bucket counts and starts, the
+// key bits (8-bit digits, per-warp digit histograms, ranks inside a warp from
+// eight ballots) keeps equal keys in slot order, so the result is the unique
+// stable order: deterministic and bit-exact. Bucket starts, read off the sorted
+// keys, give the expert and (expert, adapter) segment boundaries, from which the
+// grouped-GEMM token tiles and the LoRA blocks are cut. Working state (bucket counts and starts, the
 // sort buffers) stays in shared memory whenever it fits; only results go out.
 #include "common.cuh"
 
@@ -48,6 +48,18 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total)
   *total = tmp[NW];
   __syncthreads();
   return r;
+}
+
+// Lanes of `mask` whose 8-bit digit equals this lane's: the AND over the digit's
+// bits of each bit's ballot (or its complement).
+__device__ __forceinline__ unsigned digit_peers(unsigned mask, int d) {
+  unsigned peers = mask;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const unsigned bb = __ballot_sync(mask, (d >> b) & 1);
+    peers &= ((d >> b) & 1) ? bb : ~bb;
+  }
+  return peers;
 }
 
 // Shared-memory plan of one align launch (host and device agree through this).
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(NT, 1)
       const unsigned mask = __ballot_sync(0xffffffffu, act);
       if (act) {
         const int d = (src[i] >> shift) & 255;
-        const unsigned peers = __match_any_sync(mask, d);
+        const unsigned peers = digit_peers(mask, d);
         if (lane == __ffs(peers) - 1) hist[d * NW + warp] += __popc(peers);
       }
       __syncwarp();
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (act) {
         const uint32_t x = src[i];
         d = (x >> shift) & 255;
-        peers = __match_any_sync(mask, d);
+        peers = digit_peers(mask, d);
         dst[hist[d * NW + warp] + __popc(peers & lt)] = x;
       }
       __syncwarp();
@@ -179,15 +191,13 @@ __global__ void __launch_bounds__(NT, 1)
   }
 
   // 3. segment starts: bucket c starts at the first sorted word with key >= c
-  //    (bucket order is expert-major, adapter -1 first); counts are differences.
-  for (int c = tid; c < nbuckets; c += NT) {
-    int lo = 0, hi = S;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (static_cast<int>(src[mid] >> slot_bits) < c) lo = mid + 1;
-      else hi = mid;
-    }
-    bstart[c] = lo;
+  //    (bucket order is expert-major, adapter -1 first); each sorted position
+  //    fills the starts of the buckets between its predecessor's key and its own,
+  //    so every bucket is written once; counts are differences.
+  for (int i = tid; i <= S; i += NT) {
+    const int kp = i == 0 ? -1 : static_cast<int>(src[i - 1] >> slot_bits);
+    const int kc = i == S ? nbuckets - 1 : static_cast<int>(src[i] >> slot_bits);
+    for (int c = kp + 1; c <= kc; ++c) bstart[c] = i;
   }
   __syncthreads();
   for (int c = tid; c < nbuckets; c += NT)

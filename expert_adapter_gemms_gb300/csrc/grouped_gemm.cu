@@ -30,6 +30,7 @@ constexpr int kBM = 128;  // weight rows per CTA (MMA M)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kGemmThreads = 192;
 constexpr int kGroupTiles = 8;
+enum { kModeTile = 0, kModeExpert = 1, kModePersistent = 2 };
 
 template <int BN, int STAGES>
 struct GemmCfg {
@@ -38,8 +39,9 @@ struct GemmCfg {
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-  static_assert((2 * STAGES + 2) * 8 + 16 <= 256, "barrier area");
-  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  static_assert((2 * STAGES + 4) * 8 + 16 <= 256, "barrier area");
+  static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;  // one fp32 accumulator
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;     // two, used alternately
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kABytes % 1024 == 0, "stage alignment");
 };
@@ -98,42 +100,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const __grid_constant__ CUtensorMap tm_a, int* __restrict__ hdr,
                         const int4* __restrict__ tiles, const int* __restrict__ expert_begin,
                         float* __restrict__ out, int N, int K, int n_wblocks, int max_tiles,
-                        int expert_major, int early) {
+                        int mode, int early) {
   using C = GemmCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + STAGES;
-  uint64_t* tmem_full = empty + STAGES;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
+  uint64_t* tmem_full = empty + STAGES;  // [2]: one per accumulator
+  uint64_t* tmem_empty = tmem_full + 2;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // first row and row count of the CTA's work
+  int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // expert-major: first row, row count
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Which weight block and which expert.
-  //  tile-major: CTA -> (token tile, weight block); groups of kGroupTiles tiles
-  //              sweep all weight blocks before the next group starts.
-  //  expert-major: CTA -> (expert, weight block); the CTA takes every token of the
-  //              expert, in chunks of BN rows, so it knows its weights before any
-  //              table of the align step exists.
-  int wb, ti = 0, e;
-  if (expert_major) {
-    e = blockIdx.x / n_wblocks;
-    wb = blockIdx.x - e * n_wblocks;
-  } else {
-    const int lin = blockIdx.x;
+  // Work decomposition (see the mode constants): a job is one token chunk of one
+  // expert against one 128-row weight block.
+  //  kModeTile:       one job, (token tile, weight block) from blockIdx
+  //  kModeExpert:     the expert's rows in chunks of BN against one weight block
+  //  kModePersistent: jobs w = blockIdx.x, + gridDim.x, ... over every
+  //                   (token tile, weight block) in grouped order
+  const bool expert_major = mode == kModeExpert;
+  const bool persistent = mode == kModePersistent;
+  auto tile_job = [&](int w, int n_tiles, int& e, int& wb, int& r0, int& rows) {
     const int per_group = kGroupTiles * n_wblocks;
-    const int grp = lin / per_group;
+    const int grp = w / per_group;
     const int first = grp * kGroupTiles;
-    const int gsz = min(kGroupTiles, max_tiles - first);
-    const int within = lin - grp * per_group;
+    const int gsz = min(kGroupTiles, n_tiles - first);
+    const int within = w - grp * per_group;
     wb = within / gsz;
-    ti = first + within % gsz;
-    e = 0;
-  }
+    const int4 tile = __ldcg(tiles + first + within % gsz);
+    e = tile.x;
+    r0 = tile.y;
+    rows = tile.z;
+  };
 
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -141,8 +142,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 2);  // one arrival for the weight copy, one for the token copy
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);  // one arrival per epilogue warp
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 4);  // one arrival per epilogue warp
+    }
     *s_abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -153,21 +156,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncthreads();
 
-  // Tile-major with `early`: the tile table (from the align launch, two or more
-  // launches back) is read before griddepcontrol.wait. Expert-major: nothing of the
-  // align step is read before the wait.
-  int row0 = 0, rows = 0;
-  if (!expert_major) {
+  // First job's expert and weight block. Tile modes with `early` read the tile table
+  // (from the align launch, two or more launches back) before griddepcontrol.wait;
+  // expert-major reads nothing of the align step before the wait.
+  int njobs, e0, wb0, r00 = 0, rows0 = 0, n_tiles = 0;
+  if (expert_major) {
+    e0 = blockIdx.x / n_wblocks;
+    wb0 = blockIdx.x - e0 * n_wblocks;
+    njobs = -1;  // known after the wait
+  } else {
     if (!early) pdl_wait();
-    const int n_tiles = __ldcg(hdr + HDR_NTILES);
-    if (ti >= n_tiles) {
+    n_tiles = __ldcg(hdr + HDR_NTILES);
+    const int total = n_tiles * n_wblocks;
+    if (persistent) {
+      njobs = blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+      if (njobs > 0) tile_job(blockIdx.x, n_tiles, e0, wb0, r00, rows0);
+    } else {
+      // one job from the grouped mapping over the host's tile bound
+      const int lin = blockIdx.x;
+      const int per_group = kGroupTiles * n_wblocks;
+      const int grp = lin / per_group;
+      const int first = grp * kGroupTiles;
+      const int gsz = min(kGroupTiles, max_tiles - first);
+      const int within = lin - grp * per_group;
+      wb0 = within / gsz;
+      const int ti = first + within % gsz;
+      njobs = ti < n_tiles ? 1 : 0;
+      if (njobs) {
+        const int4 tile = __ldcg(tiles + ti);
+        e0 = tile.x;
+        r00 = tile.y;
+        rows0 = tile.z;
+      }
+    }
+    if (njobs == 0) {
       if (early) pdl_wait();
       return;
     }
-    const int4 tile = __ldcg(tiles + ti);
-    e = tile.x;
-    row0 = tile.y;
-    rows = tile.z;
   }
   const int nk = (K + kBK - 1) / kBK;
   const int pre = nk < STAGES ? nk : STAGES;
@@ -176,32 +201,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  // the first ring of weight stages (a weight never depends on a launch)
+  // the first ring of weight stages of the first job (a weight never depends on a launch)
   if (threadIdx.x == 0) {
     const uint64_t pol_w = l2_policy_evict_first();
     for (int kb = 0; kb < pre; ++kb) {
       mbar_arrive_expect_tx(&full[kb], C::kWBytes);
-      tma_load_3d(smem + kb * C::kStageBytes, &tm_w, &full[kb], kb * kBK, wb * kBM, e, pol_w);
+      tma_load_3d(smem + kb * C::kStageBytes, &tm_w, &full[kb], kb * kBK, wb0 * kBM, e0, pol_w);
     }
   }
   if (expert_major || early) pdl_wait();
   if (threadIdx.x == 0) {
     pdl_trigger();
     if (expert_major) {
-      const int eb = __ldcg(expert_begin + e), ee = __ldcg(expert_begin + e + 1);
+      const int eb = __ldcg(expert_begin + e0), ee = __ldcg(expert_begin + e0 + 1);
       s_job[0] = eb;
       s_job[1] = ee - eb;
-    } else {
-      s_job[0] = row0;
-      s_job[1] = rows;
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int jrow0 = s_job[0], jrows = s_job[1];
-  const int njobs = expert_major ? (jrows + BN - 1) / BN : 1;
+  if (expert_major) njobs = (s_job[1] + BN - 1) / BN;
+
+  // job j -> expert, weight block, first row, rows
+  auto job = [&](int j, int& e, int& wb, int& r0, int& rows) {
+    if (expert_major) {
+      e = e0;
+      wb = wb0;
+      r0 = s_job[0] + j * BN;
+      rows = min(BN, s_job[1] - j * BN);
+    } else if (persistent) {
+      if (j == 0) {
+        e = e0; wb = wb0; r0 = r00; rows = rows0;
+      } else {
+        tile_job(blockIdx.x + j * gridDim.x, n_tiles, e, wb, r0, rows);
+      }
+    } else {
+      e = e0; wb = wb0; r0 = r00; rows = rows0;
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -209,12 +248,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_a = l2_policy_evict_last();
       int issued = 0;
-      if (njobs == 0) {  // no token for this expert: complete the prefetched stages, drain
+      if (njobs == 0) {  // expert-major with no token: complete the prefetched stages, drain
         for (int kb = 0; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
         for (int kb = 0; kb < pre; ++kb) mbar_wait_bounded(&full[kb], 0);
       }
       for (int j = 0; j < njobs && !*s_abort; ++j) {
-        const int r0 = jrow0 + j * BN;
+        int e, wb, r0, rows;
+        job(j, e, wb, r0, rows);
         for (int kb = 0; kb < nk; ++kb) {
           const int g = j * nk + kb;
           const int s = g % STAGES;
@@ -240,12 +280,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issuer
+      // MMA issuer: job j accumulates in buffer j % 2
       for (int j = 0; j < njobs && !*s_abort; ++j) {
-        const int jr = min(BN, jrows - j * BN);
-        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>((jr + 15) & ~15));
-        if (j > 0) {  // the epilogue must have read the previous job's accumulator
-          if (!mbar_wait_bounded(tmem_empty, (j - 1) & 1)) {
+        int e, wb, r0, rows;
+        job(j, e, wb, r0, rows);
+        const int a = j & 1;
+        const uint32_t acc = tmem + static_cast<uint32_t>(a * C::kAccCols);
+        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>((rows + 15) & ~15));
+        if (j >= 2) {  // the epilogue must have read this buffer's previous job
+          if (!mbar_wait_bounded(&tmem_empty[a], ((j >> 1) - 1) & 1)) {
             *s_abort = 1;
             break;
           }
@@ -265,25 +308,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t db = smem_desc_sw128(smem_u32(sw + C::kWBytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
+            tc_mma_bf16(acc, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0);
           tc_commit(&empty[s]);
         }
-        tc_commit(tmem_full);  // fires when every MMA issued above has completed
+        tc_commit(&tmem_full[a]);  // fires when every MMA issued above has completed
       }
     }
   } else {
     // epilogue: warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
     const int quad = warp & 3;
-    const int n = wb * kBM + quad * 32 + lane;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     for (int j = 0; j < njobs; ++j) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(tmem_full, j & 1) ? 1 : 0);
+      int e, wb, r0, rows;
+      job(j, e, wb, r0, rows);
+      const int a = j & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1) ? 1 : 0);
       if (!ok) *s_abort = 1;
       if (!ok || *s_abort) break;
       tc_fence_after();
-      const int r0 = jrow0 + j * BN;
-      const int jr = min(BN, jrows - j * BN);
-      const uint32_t nmma = static_cast<uint32_t>((jr + 15) & ~15);
+      const int n = wb * kBM + quad * 32 + lane;
+      const uint32_t taddr = tmem + static_cast<uint32_t>(a * C::kAccCols) +
+                             (static_cast<uint32_t>(quad * 32) << 16);
+      const uint32_t nmma = static_cast<uint32_t>((rows + 15) & ~15);
       for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
         uint32_t v[16];
         tmem_ld_x16(taddr + c0, v);
@@ -292,13 +337,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int tok = static_cast<int>(c0) + q;
-            if (tok < jr) out[(size_t)(r0 + tok) * N + n] = __uint_as_float(v[q]);
+            if (tok < rows) out[(size_t)(r0 + tok) * N + n] = __uint_as_float(v[q]);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
+      if (lane == 0) mbar_arrive(&tmem_empty[a]);
     }
   }
   tc_fence_before();
@@ -353,7 +398,7 @@ static int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint
 template <int BN, int STAGES>
 static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const AlignView& v,
                          int max_tiles, int E, int N, int K, float* out, cudaStream_t stream,
-                         bool pdl, int expert_major, int early) {
+                         bool pdl, int mode, int early) {
   using C = GemmCfg<BN, STAGES>;
   static int configured[64] = {0};
   int dev = 0;
@@ -364,12 +409,18 @@ static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const Ali
     configured[dev] = 1;
   }
   const int n_wblocks = ceil_div(N, kBM);
-  const int64_t grid = (int64_t)(expert_major ? E : max_tiles) * n_wblocks;
+  int64_t grid = (int64_t)(mode == kModeExpert ? E : max_tiles) * n_wblocks;
+  if (mode == kModePersistent) {  // one resident CTA per SM slot, each looping over jobs
+    int per_sm = 0;
+    ML_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, grouped_gemm_kernel<BN, STAGES>, kGemmThreads, C::kSmemBytes));
+    const int64_t slots = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
+    if (grid > slots) grid = slots;
+  }
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
   return launch_pdl(grouped_gemm_kernel<BN, STAGES>, dim3((unsigned)grid), kGemmThreads,
                     C::kSmemBytes, stream, pdl, tw, ta, v.hdr, (const int4*)v.tiles,
-                    (const int*)v.expert_begin, out, N, K, n_wblocks, max_tiles, expert_major,
-                    early);
+                    (const int*)v.expert_begin, out, N, K, n_wblocks, max_tiles, mode, early);
 }
 
 int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora_align_t* al,
@@ -377,8 +428,10 @@ int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora
                              bool pdl, bool early, int expert_major_bn) {
   if (a.S == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
-  const int em = expert_major_bn > 0 ? 1 : 0;
-  const int bn = em ? expert_major_bn : al->bm_base;
+  // expert-major when asked; else persistent for large token tiles (prefill), whose
+  // epilogue then overlaps the next job's main loop; else one job per CTA
+  const int bn = expert_major_bn > 0 ? expert_major_bn : al->bm_base;
+  const int em = expert_major_bn > 0 ? kModeExpert : bn >= 128 ? kModePersistent : kModeTile;
   const int ea = early ? 1 : 0;
   CUtensorMap tw, ta;
   {

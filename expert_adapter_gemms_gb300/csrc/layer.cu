@@ -58,7 +58,7 @@ int num_sms() {
 // ---------------------------------------------------------------------------
 // tiles and workspace
 // ---------------------------------------------------------------------------
-static void pick_tiles(int T, int k, int E, int32_t* bm_base, int32_t* bm_lora) {
+static void pick_tiles(int T, int k, int E, int L, int32_t* bm_base, int32_t* bm_lora) {
   const int64_t S = (int64_t)T * k;
   const int64_t per_expert = (S + E - 1) / E;
   int64_t b = (2 * per_expert + 15) / 16 * 16;
@@ -69,7 +69,8 @@ static void pick_tiles(int T, int k, int E, int32_t* bm_base, int32_t* bm_lora) 
   for (int i = 0; i < 5; ++i)
     if (allowed[i] >= b) { pick = allowed[i]; break; }
   *bm_base = pick;
-  *bm_lora = 16;
+  // short (expert, adapter) segments (decode): blocks of at most 8 rows
+  *bm_lora = S <= 2 * (int64_t)E * (L > 0 ? L : 1) ? 8 : 16;
 }
 
 struct LayerPlan {
@@ -84,7 +85,7 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r, int
   LayerPlan p = {};
   p.valid = false;
   int32_t hb, hl;
-  pick_tiles(T, k, E, &hb, &hl);
+  pick_tiles(T, k, E, L, &hb, &hl);
   p.bm_base = bm_base > 0 ? bm_base : hb;
   p.bm_lora = bm_lora > 0 ? bm_lora : hl;
   p.al = align_layout(T, k, E, L, p.bm_base, p.bm_lora);
@@ -143,9 +144,9 @@ extern "C" int moe_lora_clear_error(void* buf, moe_lora_stream_t stream) {
 
 extern "C" int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r,
                                     int32_t* bm_base, int32_t* bm_lora) {
-  (void)L; (void)H; (void)I; (void)r;
-  if (!bm_base || !bm_lora || T < 0 || k < 1 || E < 1) return MOE_LORA_ERR_INVALID_ARG;
-  pick_tiles(T, k, E, bm_base, bm_lora);
+  (void)H; (void)I; (void)r;
+  if (!bm_base || !bm_lora || T < 0 || k < 1 || E < 1 || L < 0) return MOE_LORA_ERR_INVALID_ARG;
+  pick_tiles(T, k, E, L, bm_base, bm_lora);
   return MOE_LORA_OK;
 }
 

@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(kExpandThreads)
 }
 
 // ----------------------------------------------------------------------------
-// epilogue 1: h[row, n] = silu(g) * u for every valid sorted row, with
+// epilogue 1, row walk (short (expert, adapter) segments, e.g. decode; and ranks
+// that are not a multiple of 8): h[row, n] = silu(g) * u for every valid row, with
 //   g = G[row, n] + z.B[l, e, n],  u = G[row, I + n] + z.B[l, e, I + n].
 // A CTA owns `rows_per_cta` consecutive sorted rows and 256 columns. With one row
 // per CTA (short (expert, adapter) segments, e.g. decode) every load of a thread
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(kExpandThreads)
 // ----------------------------------------------------------------------------
 template <int RV>
 __global__ void __launch_bounds__(kExpandThreads)
-    expand_swiglu_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+    expand_swiglu_rows_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                          const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
                          const int* __restrict__ row_expert, const int* __restrict__ row_adapter,
                          int I, int r, int E, const float* __restrict__ G,
@@ -320,6 +321,281 @@ __global__ void __launch_bounds__(kExpandThreads)
 }
 
 // ----------------------------------------------------------------------------
+// Tensor-core expand of one LoRA block (at most 16 rows of one (e, l) segment):
+//   D[m, n] = sum_i z[m, i] * B[l, e, n, i]
+// with mma.sync m16n8k16: the block's rows on M (padded to 16), 8 output columns
+// on N, the rank on K, fp32 accumulation. z is held as a bf16 pair (high part and
+// the bf16 rounding of the remainder), so z . B = z_hi . B + z_lo . B keeps the
+// fp32 z to about 2^-16 relative; B is bf16 already. Each lane loads 16 bytes of
+// the B row of column n0 + lane/4 at k = 32c + 8(lane%4); both operands feed
+// those 8 consecutive k to the fragment slots through the same permutation (the
+// shrink's scheme), which leaves the sums unchanged.
+// One CTA takes a whole block: its z fragments stay in registers while the warps
+// sweep the output columns 8 at a time, each tile's B fragments and base values
+// fetched while the previous tile is reduced.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// z rows of a block in shared memory as bf16 high parts [16][r_pad] followed by the
+// bf16 remainders [16][r_pad]; rows >= rows and ranks >= r are zero.
+__device__ __forceinline__ void stage_z_split(__nv_bfloat16* zb, const float* __restrict__ Z,
+                                              const int* __restrict__ sorted_slots, int row0,
+                                              int rows, int r, int r_pad) {
+  for (int i = threadIdx.x; i < 16 * r_pad; i += blockDim.x) {
+    const int m = i / r_pad, c = i - m * r_pad;
+    float v = 0.f;
+    if (m < rows && c < r) v = __ldcg(Z + (size_t)__ldcg(sorted_slots + row0 + m) * r + c);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    zb[i] = hi;
+    zb[16 * r_pad + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+}
+
+// This lane's z fragments, chunk c: [part][c] = {row lane/4, row lane/4 + 8} x 8 k.
+template <int KC>
+struct ZFrag {
+  uint4 a[2][KC], b[2][KC];
+  __device__ __forceinline__ void load(const __nv_bfloat16* zb, int r_pad) {
+    const int lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int c = 0; c < KC; ++c) {
+        const __nv_bfloat16* zp = zb + part * 16 * r_pad + 32 * c + 8 * q;
+        a[part][c] = *reinterpret_cast<const uint4*>(zp + gid * r_pad);
+        b[part][c] = *reinterpret_cast<const uint4*>(zp + (gid + 8) * r_pad);
+      }
+  }
+};
+
+// The B fragment of chunk c for this lane (zeros past the rank or the last column).
+__device__ __forceinline__ uint4 b_frag(const __nv_bfloat16* brow, int c, int r) {
+  const int k0 = 32 * c + 8 * (threadIdx.x & 3);
+  if (!brow || k0 >= r) return make_uint4(0, 0, 0, 0);
+  return __ldg(reinterpret_cast<const uint4*>(brow + k0));
+}
+
+template <int KC>
+__device__ __forceinline__ void block_mma(float (&acc)[4], const ZFrag<KC>& z, const uint4 (&bf)[KC]) {
+  acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+  for (int part = 0; part < 2; ++part)
+#pragma unroll
+    for (int c = 0; c < KC; ++c) {
+      mma_bf16_16816(acc, z.a[part][c].x, z.b[part][c].x, z.a[part][c].y, z.b[part][c].y,
+                     bf[c].x, bf[c].y);
+      mma_bf16_16816(acc, z.a[part][c].z, z.b[part][c].z, z.a[part][c].w, z.b[part][c].w,
+                     bf[c].z, bf[c].w);
+    }
+}
+
+// epilogue 1 with tensor cores. CTAs [0, max_blocks): one LoRA block each, all
+// columns; CTAs beyond: (token tile, 512-column chunk) pairs applying the plain
+// SwiGLU to the tile's rows without adapter.
+template <int KC>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_swiglu_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+                             const int* __restrict__ hdr, const int4* __restrict__ blocks,
+                             const int4* __restrict__ tiles, const int* __restrict__ sorted_slots,
+                             const int* __restrict__ row_adapter, int I, int r, int E,
+                             const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
+                             int max_blocks, int early) {
+  constexpr int kWarps = kExpandThreads / 32;
+  constexpr int kChunk = 2 * kExpandThreads;  // columns per plain-SwiGLU CTA
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  const int r_pad = 32 * KC;
+  const size_t twoI = 2 * (size_t)I;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+  if (!early) pdl_wait();
+  if ((int)blockIdx.x < max_blocks) {
+    const int b = blockIdx.x;
+    if (!B || b >= __ldcg(hdr + HDR_NBLOCKS)) {
+      if (early) pdl_wait();
+      return;
+    }
+    const int4 blk = __ldcg(blocks + b);
+    const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
+    const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+    const int ntiles = (I + 7) / 8;
+    // operands of tile t (B fragments: weights; G: two launches old)
+    uint4 bg[KC], bu[KC];
+    float2 gg[2], gu[2];
+    auto fetch = [&](int t, bool with_g) {
+      const int nl = t * 8 + gid, n = t * 8 + 2 * q;
+#pragma unroll
+      for (int c = 0; c < KC; ++c) {
+        bg[c] = b_frag(nl < I ? bl + (size_t)nl * r : nullptr, c, r);
+        bu[c] = b_frag(nl < I ? bl + (size_t)(I + nl) * r : nullptr, c, r);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int m = gid + 8 * half;
+        gg[half] = gu[half] = make_float2(0.f, 0.f);
+        if (with_g && m < rows && n < I) {
+          const size_t gr = (size_t)(row0 + m) * twoI;
+          gg[half] = __ldcg(reinterpret_cast<const float2*>(G + gr + n));
+          gu[half] = __ldcg(reinterpret_cast<const float2*>(G + gr + I + n));
+        }
+      }
+    };
+    int t = warp;
+    if (t < ntiles) fetch(t, early);
+    if (early) pdl_wait();
+    pdl_trigger();
+    stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
+    __syncthreads();
+    ZFrag<KC> z;
+    z.load(zb, r_pad);
+    if (!early && t < ntiles) fetch(t, true);
+    for (; t < ntiles; t += kWarps) {
+      const uint4 (&cbg)[KC] = bg;
+      uint4 tg[KC], tu[KC];
+      float2 tgg[2] = {gg[0], gg[1]}, tgu[2] = {gu[0], gu[1]};
+#pragma unroll
+      for (int c = 0; c < KC; ++c) {
+        tg[c] = cbg[c];
+        tu[c] = bu[c];
+      }
+      if (t + kWarps < ntiles) fetch(t + kWarps, true);  // next tile in flight
+      float dg[4], du[4];
+      block_mma<KC>(dg, z, tg);
+      block_mma<KC>(du, z, tu);
+      const int n = t * 8 + 2 * q;
+      if (n >= I) continue;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int m = gid + 8 * half;
+        if (m >= rows) continue;
+        const float g0 = tgg[half].x + dg[2 * half], g1 = tgg[half].y + dg[2 * half + 1];
+        const float u0 = tgu[half].x + du[2 * half], u1 = tgu[half].y + du[2 * half + 1];
+        __nv_bfloat162 o;
+        o.x = __float2bfloat16_rn(g0 / (1.f + expf(-g0)) * u0);
+        o.y = __float2bfloat16_rn(g1 / (1.f + expf(-g1)) * u1);
+        *reinterpret_cast<__nv_bfloat162*>(h + (size_t)(row0 + m) * I + n) = o;
+      }
+    }
+  } else {
+    // adapter-free rows of one token tile: plain SwiGLU, two columns per thread
+    const int nch = (I + kChunk - 1) / kChunk;
+    const int idx = blockIdx.x - max_blocks;
+    const int ti = idx / nch, ch = idx - ti * nch;
+    if (ti >= __ldcg(hdr + HDR_NTILES)) {
+      if (early) pdl_wait();
+      return;
+    }
+    const int4 tile = __ldcg(tiles + ti);
+    const int row0 = tile.y, rows = tile.z;
+    if (early) pdl_wait();
+    pdl_trigger();
+    const int n = ch * kChunk + 2 * threadIdx.x;
+    if (n >= I) return;
+    for (int m = 0; m < rows; ++m) {
+      if (B && __ldcg(row_adapter + row0 + m) >= 0) continue;  // a LoRA-block CTA owns it
+      const size_t gr = (size_t)(row0 + m) * twoI;
+      const float2 g = __ldcg(reinterpret_cast<const float2*>(G + gr + n));
+      const float2 u = __ldcg(reinterpret_cast<const float2*>(G + gr + I + n));
+      __nv_bfloat162 o;
+      o.x = __float2bfloat16_rn(g.x / (1.f + expf(-g.x)) * u.x);
+      o.y = __float2bfloat16_rn(g.y / (1.f + expf(-g.y)) * u.y);
+      *reinterpret_cast<__nv_bfloat162*>(h + (size_t)(row0 + m) * I + n) = o;
+    }
+  }
+}
+
+// epilogue 0 (and the block-walk half of epilogue 2) with tensor cores:
+// base[row, n..n+1] += D for the rows of each LoRA block; one CTA per block.
+template <int KC>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_add_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+                          const int* __restrict__ hdr, const int4* __restrict__ blocks,
+                          const int* __restrict__ sorted_slots, int N, int r, int E,
+                          float* __restrict__ base, int early) {
+  constexpr int kWarps = kExpandThreads / 32;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  const int r_pad = 32 * KC;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
+  if (!early) pdl_wait();
+  const int b = blockIdx.x;
+  if (b >= __ldcg(hdr + HDR_NBLOCKS)) {
+    if (early) pdl_wait();
+    return;
+  }
+  const int4 blk = __ldcg(blocks + b);
+  const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
+  const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
+  const int ntiles = (N + 7) / 8;
+  uint4 bf[KC];
+  auto fetch = [&](int t) {
+    const int nl = t * 8 + gid;
+#pragma unroll
+    for (int c = 0; c < KC; ++c) bf[c] = b_frag(nl < N ? bl + (size_t)nl * r : nullptr, c, r);
+  };
+  int t = warp;
+  if (t < ntiles) fetch(t);
+  if (early) pdl_wait();
+  pdl_trigger();
+  stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
+  __syncthreads();
+  ZFrag<KC> z;
+  z.load(zb, r_pad);
+  for (; t < ntiles; t += kWarps) {
+    uint4 cur[KC];
+#pragma unroll
+    for (int c = 0; c < KC; ++c) cur[c] = bf[c];
+    if (t + kWarps < ntiles) fetch(t + kWarps);
+    float d[4];
+    block_mma<KC>(d, z, cur);
+    const int n = t * 8 + 2 * q;
+    if (n >= N) continue;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int m = gid + 8 * half;
+      if (m >= rows) continue;
+      float2* o = reinterpret_cast<float2*>(base + (size_t)(row0 + m) * N + n);
+      float2 v = __ldcg(o);
+      v.x += d[2 * half];
+      v.y += d[2 * half + 1];
+      *o = v;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Weighted top-k combine after an in-place expand over LoRA blocks:
+//   y[t, n] = sum_j w[t, j] * O[row(t, j), n], j ascending.
+// ----------------------------------------------------------------------------
+template <bool kOutF32>
+__global__ void __launch_bounds__(kExpandThreads)
+    combine_kernel(const float* __restrict__ O, const float* __restrict__ w,
+                   const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
+                   int tokens_per_cta) {
+  pdl_wait();
+  pdl_trigger();
+  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
+  if (n >= N) return;
+  const int t0 = blockIdx.x * tokens_per_cta;
+  const int t1 = min(T, t0 + tokens_per_cta);
+  for (int t = t0; t < t1; ++t) {
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __ldcg(slot_row + (size_t)t * k + j);
+      if (row >= 0) acc = fmaf(__ldcg(w + (size_t)t * k + j), __ldcg(O + (size_t)row * N + n), acc);
+    }
+    if (kOutF32) static_cast<float*>(y)[(size_t)t * N + n] = acc;
+    else static_cast<__nv_bfloat16*>(y)[(size_t)t * N + n] = __float2bfloat16_rn(acc);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
 template <template <int> class K, typename... Args>
@@ -334,7 +610,7 @@ static int launch_rv(int rv, dim3 grid, size_t smem, cudaStream_t stream, bool p
   }
 }
 template <int RV> struct AddK { static constexpr auto fn = expand_add_kernel<RV>; };
-template <int RV> struct SwigluK { static constexpr auto fn = expand_swiglu_kernel<RV>; };
+template <int RV> struct SwigluK { static constexpr auto fn = expand_swiglu_rows_kernel<RV>; };
 
 // r / 8 when the B rows can sit in registers with 128-bit loads, else 0.
 static int reg_ranks(int r, const void* B) {
@@ -354,6 +630,43 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   const int rr = Bp ? r : 0;
   const int sms = num_sms();
   const int ea = early ? 1 : 0;
+  // tensor-core block expand: B rows of r % 8 == 0 ranks, 16-byte aligned, column pairs
+  const int kc = (r + 31) / 32;
+  const bool mma_ok = Bp && r % 8 == 0 && aligned16(B) && kc <= 8 &&
+                      (reinterpret_cast<uintptr_t>(base) & 7u) == 0 &&
+                      (epilogue == 1 ? (N / 2) % 2 == 0 : N % 2 == 0);
+  const int kcp = kc <= 1 ? 1 : kc <= 2 ? 2 : kc <= 4 ? 4 : 8;
+  const size_t zsmem = (size_t)2 * 16 * 32 * kcp * sizeof(__nv_bfloat16);  // z high + remainder
+  auto add_mma = [&](dim3 grid) {
+    auto go = [&](auto kern) {
+      return launch_pdl(kern, grid, kExpandThreads, zsmem, stream, pdl, Z, Bp, (const int*)v.hdr,
+                        (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base, ea);
+    };
+    switch (kcp) {
+      case 1: return go(expand_add_mma_kernel<1>);
+      case 2: return go(expand_add_mma_kernel<2>);
+      case 4: return go(expand_add_mma_kernel<4>);
+      default: return go(expand_add_mma_kernel<8>);
+    }
+  };
+  if (epilogue == 0 && mma_ok) return add_mma(dim3(a.max_blocks));
+  const bool short_segments = (int64_t)a.S <= 2 * (int64_t)al->E * (al->L > 0 ? al->L : 1);
+  if (epilogue == 1 && !short_segments && (mma_ok || (!Bp && (N / 2) % 2 == 0))) {
+    const int I = N / 2;
+    const dim3 grid(a.max_blocks + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
+    auto go = [&](auto kern) {
+      return launch_pdl(kern, grid, kExpandThreads, Bp ? zsmem : 0, stream, pdl, Z, Bp,
+                        (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
+                        (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
+                        (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, ea);
+    };
+    switch (Bp ? kcp : 1) {
+      case 1: return go(expand_swiglu_mma_kernel<1>);
+      case 2: return go(expand_swiglu_mma_kernel<2>);
+      case 4: return go(expand_swiglu_mma_kernel<4>);
+      default: return go(expand_swiglu_mma_kernel<8>);
+    }
+  }
   if (epilogue == 0) {
     if (!Bp) return MOE_LORA_OK;
     const dim3 grid(a.max_blocks, ceil_div(N, 2 * kExpandThreads));
@@ -378,6 +691,31 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
                               (const int*)v.sorted_slots, (const int*)v.row_expert,
                               (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp,
                               rpc, ea);
+  }
+  if (epilogue == 2 && Bp && (int64_t)a.S >= 2 * (int64_t)al->E * al->L) {
+    // several rows per (expert, adapter) pair: apply each B row once per LoRA block
+    // (in place on the base output), then combine
+    int st;
+    if (mma_ok) {
+      st = add_mma(dim3(a.max_blocks));
+    } else {
+      const dim3 grid(a.max_blocks, ceil_div(N, 2 * kExpandThreads));
+      const size_t smem = (size_t)kMaxBmLora * r * sizeof(float);
+      st = launch_rv<AddK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
+                           (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base,
+                           ea);
+    }
+    if (st != MOE_LORA_OK) return st;
+    const int ncol = ceil_div(N, kExpandThreads);
+    int tpc = 1;
+    while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms) tpc *= 2;
+    const dim3 g2(ceil_div(al->T, tpc), ncol);
+    return out_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl,
+                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
+                                 N, out, tpc)
+                    : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl,
+                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
+                                 N, out, tpc);
   }
   if (epilogue == 2) {
     const int ncol = ceil_div(N, kExpandThreads);

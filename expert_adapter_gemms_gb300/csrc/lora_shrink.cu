@@ -55,13 +55,14 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT, int U, bool kVec, bool kEvenK>
-__global__ void __launch_bounds__(kShrinkWarps * 32)
+template <int NT, int U, bool kVec, bool kEvenK, bool kSmallM>
+__global__ void __launch_bounds__(kShrinkWarps * 32, NT == 1 && kSmallM ? 5 : 1)  // one wave at decode
     lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
                        int K, int r, int E, float* __restrict__ Z, int ngroups, int early) {
   constexpr int R = 8 * NT;  // ranks per CTA
+  constexpr int XB = kSmallM ? 1 : U;  // kSmallM: blocks of at most 8 rows, no second row set
   __shared__ float red[kShrinkWarps][16][R + 1];
 
   // With `early` every input was produced two or more launches back (see
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
     const int row = row0 + gid;
     x0 = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
   }
-  if (gid + 8 < rows) {
+  if (!kSmallM && gid + 8 < rows) {
     const int row = row0 + gid + 8;
     x1 = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
   }
@@ -102,38 +103,49 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 
+  // Batches of U k-steps per warp; the next batch's loads are in flight while the
+  // current batch is reduced (two register buffers, used alternately).
   const int nsteps = (K + 31) >> 5;
-  int st = warp;
-  // U steps per iteration: every load of the batch is issued before the first MMA
-  for (; st + (U - 1) * kShrinkWarps < nsteps; st += U * kShrinkWarps) {
-    uint4 xa[U], xb[U], av[U][NT];
+  struct Batch {
+    uint4 xa[U], xb[XB], av[U][NT];
+  };
+  auto load = [&](Batch& bt, int st0) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int k0 = (st + u * kShrinkWarps) * 32 + q * 8;
+      const int st = st0 + u * kShrinkWarps;
+      const bool ok = st < nsteps;
+      const int k0 = st * 32 + q * 8;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) av[u][nt] = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
-      xa[u] = load8_bf16<kVec, kEvenK, true>(x0, k0, K);
-      xb[u] = load8_bf16<kVec, kEvenK, true>(x1, k0, K);
+      for (int nt = 0; nt < NT; ++nt)
+        bt.av[u][nt] = ok ? load8_bf16<kVec, kEvenK>(ap[nt], k0, K) : make_uint4(0, 0, 0, 0);
+      bt.xa[u] = ok ? load8_bf16<kVec, kEvenK, true>(x0, k0, K) : make_uint4(0, 0, 0, 0);
+      if (!kSmallM)
+        bt.xb[kSmallM ? 0 : u] = ok ? load8_bf16<kVec, kEvenK, true>(x1, k0, K) : make_uint4(0, 0, 0, 0);
     }
+  };
+  auto reduce = [&](const Batch& bt) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+      const uint4 xb = kSmallM ? make_uint4(0, 0, 0, 0) : bt.xb[kSmallM ? 0 : u];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        mma_16816(acc[nt], xa[u].x, xb[u].x, xa[u].y, xb[u].y, av[u][nt].x, av[u][nt].y);
-        mma_16816(acc[nt], xa[u].z, xb[u].z, xa[u].w, xb[u].w, av[u][nt].z, av[u][nt].w);
+        mma_16816(acc[nt], bt.xa[u].x, xb.x, bt.xa[u].y, xb.y, bt.av[u][nt].x, bt.av[u][nt].y);
+        mma_16816(acc[nt], bt.xa[u].z, xb.z, bt.xa[u].w, xb.w, bt.av[u][nt].z, bt.av[u][nt].w);
       }
     }
-  }
-  for (; st < nsteps; st += kShrinkWarps) {
-    const int k0 = st * 32 + q * 8;
-    const uint4 xa0 = load8_bf16<kVec, kEvenK, true>(x0, k0, K);
-    const uint4 xb0 = load8_bf16<kVec, kEvenK, true>(x1, k0, K);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint4 a = load8_bf16<kVec, kEvenK>(ap[nt], k0, K);
-      mma_16816(acc[nt], xa0.x, xb0.x, xa0.y, xb0.y, a.x, a.y);
-      mma_16816(acc[nt], xa0.z, xb0.z, xa0.w, xb0.w, a.z, a.w);
-    }
+  };
+  constexpr int STRIDE = U * kShrinkWarps;
+  Batch b0, b1;
+  int st = warp;
+  if (st < nsteps) load(b0, st);
+  while (st < nsteps) {
+    if (st + STRIDE < nsteps) load(b1, st + STRIDE);
+    reduce(b0);
+    st += STRIDE;
+    if (st >= nsteps) break;
+    if (st + STRIDE < nsteps) load(b0, st + STRIDE);
+    reduce(b1);
+    st += STRIDE;
   }
 
   // accumulator fragment: c0,c1 -> (row gid, ranks 2q, 2q+1); c2,c3 -> (row gid+8, ...)
@@ -153,17 +165,18 @@ __global__ void __launch_bounds__(kShrinkWarps * 32)
     const int m = idx / R, c = idx - m * R;
     const int rank = g * R + c;
     if (rank >= r) continue;
-    float s = 0.f;
+    float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < kShrinkWarps; ++w) s += red[w][m][c];
-    Z[(size_t)__ldcg(sorted_slots + row0 + m) * r + rank] = s;
+    for (int w = 0; w < kShrinkWarps; ++w) sum += red[w][m][c];
+    Z[(size_t)__ldcg(sorted_slots + row0 + m) * r + rank] = sum;
   }
 }
 
 template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
-                            float* Z, bool vec, cudaStream_t stream, bool pdl, int early) {
+                            float* Z, bool vec, cudaStream_t stream, bool pdl, int early,
+                            bool small_m) {
   const int ngroups = ceil_div(r, 8 * NT);
   const int64_t grid = (int64_t)max_blocks * ngroups;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
@@ -173,9 +186,14 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
                       (const int*)v.hdr, (const int4*)v.blocks, (const int*)v.sorted_slots, k, K,
                       r, E, Z, ngroups, early);
   };
-  if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true>);
-  if (vec) return args(lora_shrink_kernel<NT, U, true, false>);
-  return args(lora_shrink_kernel<NT, U, false, false>);
+  if (small_m) {
+    if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true, true>);
+    if (vec) return args(lora_shrink_kernel<NT, U, true, false, true>);
+    return args(lora_shrink_kernel<NT, U, false, false, true>);
+  }
+  if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true, false>);
+  if (vec) return args(lora_shrink_kernel<NT, U, true, false, false>);
+  return args(lora_shrink_kernel<NT, U, false, false, false>);
 }
 
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
@@ -197,10 +215,10 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   else if (r <= 32) nt = 4;
   else nt = 8;
   switch (nt) {
-    case 1: return launch_shrink_nt<1, 4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
-    case 2: return launch_shrink_nt<2, 4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
-    case 4: return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
-    default: return launch_shrink_nt<8, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea);
+    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+    case 4: return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
   }
 }
 

@@ -151,7 +151,7 @@ def test_expand_add_inplace(r, bm_lora):
 
 
 @pytest.mark.parametrize("bm_base", [16, 64])
-@pytest.mark.parametrize("r", [8, 32, 0])
+@pytest.mark.parametrize("r", [8, 32, 5, 0])
 def test_expand_swiglu(bm_base, r):
     L = 3 if r else 0
     m, inp, ids, w, al, ref = _setup(T=80, H=40, I=72, E=4, k=2, L=L, r=max(r, 1), seed=9,
@@ -224,3 +224,23 @@ def test_shrink_many_blocks(r, T):
     m, inp, ids, w, al, ref = _setup(T=T, H=256, I=8, E=8, k=4, L=8, r=r, seed=14)
     Z = m.lora_shrink(dev(inp.x), False, dev(inp.A1), al)
     assert_close(Z, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"shrink r={r}")
+
+
+@pytest.mark.parametrize("r", [32, 5])
+def test_expand_short_segments(r):
+    """Decode-like routing: about one row per (expert, adapter) pair; the SwiGLU expand walks
+    rows and the down expand walks tokens (fused with the combine)."""
+    m, inp, ids, w, al, ref = _setup(T=64, H=96, I=80, E=32, k=4, L=8, r=r, seed=15,
+                                     adapters="round_robin_shuffled")
+    n = ref["n_valid"]
+    rng = np.random.default_rng(6)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, r))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 160), dtype=np.float32))
+    h = m.lora_expand_add(dev(Zh), dev(inp.B1), al, 1, dev(G))
+    assert_bf16_close(h[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1),
+                      "expand epilogue 1, short segments")
+    O = torch.from_numpy(rng.standard_normal((al.S, 96), dtype=np.float32))
+    wt = torch.as_tensor(w, dtype=torch.float32)
+    y = m.lora_expand_add(dev(Zh), dev(inp.B2), al, 2, dev(O), out_fp32=True, topk_w=dev(wt))
+    assert_close(y, oracle.lora_expand_add(Zh, inp.B2, ref, O[:n], epilogue=2, w=wt),
+                 KERNEL_RTOL, "expand epilogue 2, short segments")
