@@ -406,17 +406,19 @@ __global__ void __launch_bounds__(kExpandThreads)
                              const int4* __restrict__ tiles, const int* __restrict__ sorted_slots,
                              const int* __restrict__ row_adapter, int I, int r, int E,
                              const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
-                             int max_blocks, int early) {
+                             int max_blocks, int col_chunks, int early) {
   constexpr int kWarps = kExpandThreads / 32;
   constexpr int kChunk = 2 * kExpandThreads;  // columns per plain-SwiGLU CTA
+  __shared__ int s_flag[256];
+  __shared__ int s_any;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   const int r_pad = 32 * KC;
   const size_t twoI = 2 * (size_t)I;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
   if (!early) pdl_wait();
-  if ((int)blockIdx.x < max_blocks) {
-    const int b = blockIdx.x;
+  if ((int)blockIdx.x < max_blocks * col_chunks) {
+    const int b = blockIdx.x / col_chunks, chunk = blockIdx.x - b * col_chunks;
     if (!B || b >= __ldcg(hdr + HDR_NBLOCKS)) {
       if (early) pdl_wait();
       return;
@@ -424,7 +426,11 @@ __global__ void __launch_bounds__(kExpandThreads)
     const int4 blk = __ldcg(blocks + b);
     const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
     const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
-    const int ntiles = (I + 7) / 8;
+    // this CTA's 8-column tiles: [t_begin, t_end)
+    const int all_tiles = (I + 7) / 8;
+    const int per = (all_tiles + col_chunks - 1) / col_chunks;
+    const int t_begin = chunk * per;
+    const int ntiles = min(all_tiles, t_begin + per);
     // operands of tile t (B fragments: weights; G: two launches old)
     uint4 bg[KC], bu[KC];
     float2 gg[2], gu[2];
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(kExpandThreads)
         }
       }
     };
-    int t = warp;
+    int t = t_begin + warp;
     if (t < ntiles) fetch(t, early);
     if (early) pdl_wait();
     pdl_trigger();
@@ -485,20 +491,28 @@ __global__ void __launch_bounds__(kExpandThreads)
   } else {
     // adapter-free rows of one token tile: plain SwiGLU, two columns per thread
     const int nch = (I + kChunk - 1) / kChunk;
-    const int idx = blockIdx.x - max_blocks;
+    const int idx = blockIdx.x - max_blocks * col_chunks;
     const int ti = idx / nch, ch = idx - ti * nch;
     if (ti >= __ldcg(hdr + HDR_NTILES)) {
       if (early) pdl_wait();
       return;
     }
     const int4 tile = __ldcg(tiles + ti);
-    const int row0 = tile.y, rows = tile.z;
+    const int row0 = tile.y, rows = tile.z;  // rows <= 256
+    if (threadIdx.x == 0) s_any = 0;
+    __syncthreads();
+    if ((int)threadIdx.x < rows) {  // which rows need the plain SwiGLU (no adapter)
+      const int f = B ? (__ldcg(row_adapter + row0 + threadIdx.x) < 0) : 1;
+      s_flag[threadIdx.x] = f;
+      if (f) s_any = 1;
+    }
+    __syncthreads();
     if (early) pdl_wait();
     pdl_trigger();
     const int n = ch * kChunk + 2 * threadIdx.x;
-    if (n >= I) return;
+    if (!s_any || n >= I) return;
     for (int m = 0; m < rows; ++m) {
-      if (B && __ldcg(row_adapter + row0 + m) >= 0) continue;  // a LoRA-block CTA owns it
+      if (!s_flag[m]) continue;  // a LoRA-block CTA owns it
       const size_t gr = (size_t)(row0 + m) * twoI;
       const float2 g = __ldcg(reinterpret_cast<const float2*>(G + gr + n));
       const float2 u = __ldcg(reinterpret_cast<const float2*>(G + gr + I + n));
@@ -517,14 +531,14 @@ __global__ void __launch_bounds__(kExpandThreads)
     expand_add_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                           const int* __restrict__ hdr, const int4* __restrict__ blocks,
                           const int* __restrict__ sorted_slots, int N, int r, int E,
-                          float* __restrict__ base, int early) {
+                          float* __restrict__ base, int col_chunks, int early) {
   constexpr int kWarps = kExpandThreads / 32;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   const int r_pad = 32 * KC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
   if (!early) pdl_wait();
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / col_chunks, chunk = blockIdx.x - b * col_chunks;
   if (b >= __ldcg(hdr + HDR_NBLOCKS)) {
     if (early) pdl_wait();
     return;
@@ -532,14 +546,17 @@ __global__ void __launch_bounds__(kExpandThreads)
   const int4 blk = __ldcg(blocks + b);
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
-  const int ntiles = (N + 7) / 8;
+  const int all_tiles = (N + 7) / 8;
+  const int per = (all_tiles + col_chunks - 1) / col_chunks;
+  const int t_begin = chunk * per;
+  const int ntiles = min(all_tiles, t_begin + per);
   uint4 bf[KC];
   auto fetch = [&](int t) {
     const int nl = t * 8 + gid;
 #pragma unroll
     for (int c = 0; c < KC; ++c) bf[c] = b_frag(nl < N ? bl + (size_t)nl * r : nullptr, c, r);
   };
-  int t = warp;
+  int t = t_begin + warp;
   if (t < ntiles) fetch(t);
   if (early) pdl_wait();
   pdl_trigger();
@@ -637,10 +654,22 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
                       (epilogue == 1 ? (N / 2) % 2 == 0 : N % 2 == 0);
   const int kcp = kc <= 1 ? 1 : kc <= 2 ? 2 : kc <= 4 ? 4 : 8;
   const size_t zsmem = (size_t)2 * 16 * 32 * kcp * sizeof(__nv_bfloat16);  // z high + remainder
-  auto add_mma = [&](dim3 grid) {
+  // column chunks per LoRA block: enough CTAs to cover the SMs a few times over when
+  // blocks are few (the device count is at most max_blocks; assume about half)
+  auto chunks_for = [&](int cols) {
+    const int tiles8 = ceil_div(cols, 8);
+    const int est = a.max_blocks / 2 > 0 ? a.max_blocks / 2 : 1;
+    int c = ceil_div(4 * sms, est);
+    const int cap = tiles8 / (2 * (kExpandThreads / 32)) > 0 ? tiles8 / (2 * (kExpandThreads / 32)) : 1;
+    return c < 1 ? 1 : c > cap ? cap : c;
+  };
+  auto add_mma = [&](dim3) {
+    const int cc = chunks_for(N);
+    const dim3 grid(a.max_blocks * cc);
     auto go = [&](auto kern) {
       return launch_pdl(kern, grid, kExpandThreads, zsmem, stream, pdl, Z, Bp, (const int*)v.hdr,
-                        (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base, ea);
+                        (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base, cc,
+                        ea);
     };
     switch (kcp) {
       case 1: return go(expand_add_mma_kernel<1>);
@@ -653,12 +682,14 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   const bool short_segments = (int64_t)a.S <= 2 * (int64_t)al->E * (al->L > 0 ? al->L : 1);
   if (epilogue == 1 && !short_segments && (mma_ok || (!Bp && (N / 2) % 2 == 0))) {
     const int I = N / 2;
-    const dim3 grid(a.max_blocks + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
+    const int cc = chunks_for(I);
+    const dim3 grid(a.max_blocks * cc + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
     auto go = [&](auto kern) {
       return launch_pdl(kern, grid, kExpandThreads, Bp ? zsmem : 0, stream, pdl, Z, Bp,
                         (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
                         (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
-                        (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, ea);
+                        (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, cc,
+                        ea);
     };
     switch (Bp ? kcp : 1) {
       case 1: return go(expand_swiglu_mma_kernel<1>);
