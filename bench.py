@@ -317,6 +317,73 @@ def run_reference(args):
     return 0
 
 
+def launches_per_layer(inp) -> int:
+    """Kernels one layer call launches: route, align, gather, two grouped GEMMs, the
+    SwiGLU expand and the down expand (+ combine), plus the two shrinks with adapters;
+    with several rows per (expert, adapter) pair the down expand adds in place and a
+    separate combine kernel follows."""
+    if not inp.L:
+        return 7
+    return 9 + (1 if inp.S >= 2 * inp.E * inp.L else 0)
+
+
+def multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, n_layers, steps, warmup):
+    """N layers chained on one stream, layer i + 1 reading layer i's y, timed eagerly and
+    replayed from one CUDA graph. Layer i's weights, adapters and router logits are layer
+    0's rolled by i along the expert axis: the same statistics in distinct memory, so every
+    layer streams its own weights from HBM. Programmatic dependent launch chains the
+    kernels across layer boundaries as within a layer."""
+    import torch
+    layers = []
+    for i in range(n_layers):
+        if i == 0:
+            layers.append((W1, W2, lora, lg_d))
+        else:
+            layers.append((torch.roll(W1, i, 0), torch.roll(W2, i, 0),
+                           {kk: torch.roll(v, i, 1) for kk, v in lora.items()},
+                           torch.roll(lg_d, i, 1)))
+    ys = [torch.empty_like(x_d) for _ in range(n_layers)]
+
+    def run():
+        xin = x_d
+        for (w1, w2, lo, lg), y in zip(layers, ys):
+            m.moe_lora_layer(xin, w1, w2, logits=lg, k=inp.k, token_adapter=ta_d, y=y,
+                             workspace=ws, **lo)
+            xin = y
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / steps  # us per pass over all layers
+
+    eager_us = timed(run)
+    y_eager = ys[-1].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    graph_us = timed(g.replay)
+    same = bool(torch.equal(ys[-1], y_eager))
+    err = m.get_error(ws)
+    del g, layers, ys
+    return {"layers": n_layers, "steps": steps,
+            "eager_us_per_layer": round(eager_us / n_layers, 2),
+            "graph_us_per_layer": round(graph_us / n_layers, 2),
+            "graph_tokens_s": inp.T * n_layers / (graph_us * 1e-6),
+            "graph_matches_eager": same, "device_error": err}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -442,8 +509,11 @@ def run_ours(args):
                     (sb["gate_up_gemm"] + sb["down_gemm"]) / 1e9)}),
             "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * (10 if inp.L else 8),
+            "gpu_launches": args.steps * launches_per_layer(inp),
             "clocks": clk, "roofline": roof, "kernels": kernels}
+    if args.layers > 1:
+        line["multi_layer"] = multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, args.layers,
+                                          max(10, args.steps // 4), max(3, args.warmup // 4))
     if rank == 0 and nw == 1 and not args.no_cpu_baseline:
         rate, reps, el = cpu_oracle_rate(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_cores(),
@@ -468,6 +538,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=4,
+                    help="also chain this many layers (eager and one CUDA graph); < 2 skips it")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

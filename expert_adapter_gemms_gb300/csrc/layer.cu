@@ -242,7 +242,14 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(mark(3));
   ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, pdl, em_bn));
   ML_STEP(mark(4));
-  if (L > 0) ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
+  // Short LoRA blocks (decode-like) read the gathered rows: addressed by sorted row, they
+  // need no slot lookup before the load (and are recent in L2).
+  if (L > 0) {
+    if (p.bm_lora <= 8)
+      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
+    else
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
+  }
   ML_STEP(mark(5));
   ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, 1, G, h, 0,
                              nullptr, stream, pdl, pdl && L > 0));

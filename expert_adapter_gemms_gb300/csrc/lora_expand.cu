@@ -321,6 +321,69 @@ __global__ void __launch_bounds__(kExpandThreads)
 }
 
 // ----------------------------------------------------------------------------
+// epilogue 1, one sorted row per CTA (short (expert, adapter) segments: decode, or
+// many adapters): the same arithmetic as the row walk above, but a thread's loads
+// do not wait on one another. The row's align tables, the G pair and then the B
+// rows are all issued before anything is consumed, and no thread waits at a
+// barrier for another thread's table reads; the one barrier stages z (r floats)
+// after the B rows are in flight.
+// ----------------------------------------------------------------------------
+template <int RV>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_swiglu_row1_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
+                              const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
+                              const int* __restrict__ row_expert,
+                              const int* __restrict__ row_adapter, int I, int r, int E,
+                              const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
+                              int early) {
+  __shared__ __align__(16) float zs[8 * RV];
+  if (!early) pdl_wait();
+  const int row = blockIdx.x;
+  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
+  const bool col = n < I;
+  const size_t twoI = 2 * (size_t)I;
+  // rows past n_valid exist (the tables and G have S rows); their values are unused
+  const int n_valid = __ldcg(hdr + HDR_NVALID);
+  const int l = B ? __ldcg(row_adapter + row) : -1;
+  const int e = __ldcg(row_expert + row);
+  const int slot = __ldcg(sorted_slots + row);
+  float g = 0.f, u = 0.f;
+  if (col) {
+    g = __ldcg(G + (size_t)row * twoI + n);
+    u = __ldcg(G + (size_t)row * twoI + I + n);
+  }
+  const bool active = row < n_valid;
+  const bool lora = active && l >= 0;  // uniform over the CTA
+  uint4 bg[RV], bu[RV];
+  if (lora && col) {
+    const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+    const uint4* pg = reinterpret_cast<const uint4*>(bl + (size_t)n * r);
+    const uint4* pu = reinterpret_cast<const uint4*>(bl + (size_t)(I + n) * r);
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+      bg[i] = __ldg(pg + i);
+      bu[i] = __ldg(pu + i);
+    }
+  }
+  if (early) pdl_wait();
+  pdl_trigger();
+  if (!active) return;
+  if (lora) {
+    if (threadIdx.x < 2 * RV)
+      reinterpret_cast<float4*>(zs)[threadIdx.x] =
+          __ldcg(reinterpret_cast<const float4*>(Z + (size_t)slot * r) + threadIdx.x);
+    __syncthreads();
+    if (!col) return;
+#pragma unroll
+    for (int i = 0; i < RV; ++i) {
+      fma8(g, zs + 8 * i, bg[i]);
+      fma8(u, zs + 8 * i, bu[i]);
+    }
+  }
+  if (col) h[(size_t)row * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+}
+
+// ----------------------------------------------------------------------------
 // Tensor-core expand of one LoRA block (at most 16 rows of one (e, l) segment):
 //   D[m, n] = sum_i z[m, i] * B[l, e, n, i]
 // with mma.sync m16n8k16: the block's rows on M (padded to 16), 8 output columns
@@ -715,9 +778,23 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     int rpc = 1;
     while (rpc < 64 && (int64_t)rpc * 2 * segs <= a.S) rpc *= 2;
     while (rpc > 1 && (int64_t)ceil_div(a.S, rpc) * ncol < 4 * sms) rpc /= 2;
+    auto* hp = static_cast<__nv_bfloat16*>(out);
+    if (rpc == 1 && Bp && rv >= 1 && aligned16(Z)) {
+      const dim3 g1(a.S, ncol);
+      auto go = [&](auto kern) {
+        return launch_pdl(kern, g1, kExpandThreads, 0, stream, pdl, Z, Bp, (const int*)v.hdr,
+                          (const int*)v.sorted_slots, (const int*)v.row_expert,
+                          (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp, ea);
+      };
+      switch (rv) {
+        case 1: return go(expand_swiglu_row1_kernel<1>);
+        case 2: return go(expand_swiglu_row1_kernel<2>);
+        case 4: return go(expand_swiglu_row1_kernel<4>);
+        default: return go(expand_swiglu_row1_kernel<8>);
+      }
+    }
     const dim3 grid(ceil_div(a.S, rpc), ncol);
     const size_t smem = (size_t)rpc * rr * sizeof(float);
-    auto* hp = static_cast<__nv_bfloat16*>(out);
     return launch_rv<SwigluK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
                               (const int*)v.sorted_slots, (const int*)v.row_expert,
                               (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp,

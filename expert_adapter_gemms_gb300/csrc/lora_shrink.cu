@@ -56,7 +56,7 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
 }
 
 template <int NT, int U, bool kVec, bool kEvenK, bool kSmallM>
-__global__ void __launch_bounds__(kShrinkWarps * 32, NT == 1 && kSmallM ? 5 : 1)  // one wave at decode
+__global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 : NT == 4 ? 2 : 1)
     lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
@@ -68,15 +68,17 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, NT == 1 && kSmallM ? 5 : 1)
   // With `early` every input was produced two or more launches back (see
   // lora_expand.cu on launch ordering): compute first, wait only before publishing.
   if (!early) pdl_wait();
-  const int nb = __ldcg(hdr + HDR_NBLOCKS);
+  // The block count and this CTA's descriptor are read together: the grid covers the
+  // host's bound on the block count, so blocks + b is in bounds either way.
   const int b = blockIdx.x / ngroups;
   const int g = blockIdx.x - b * ngroups;
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
+  const int4 blk = __ldcg(blocks + b);
   if (b >= nb) {
     if (early) pdl_wait();
     return;
   }
   if (!early) pdl_trigger();
-  const int4 blk = __ldcg(blocks + b);
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, q = lane & 3;
@@ -217,7 +219,10 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   switch (nt) {
     case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
     case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
-    case 4: return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+    case 4:  // short blocks: two k-steps per batch, still two CTAs per SM
+      if (al->bm_lora <= 8)
+        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true);
+      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false);
     default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
   }
 }

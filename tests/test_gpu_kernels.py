@@ -244,3 +244,39 @@ def test_expand_short_segments(r):
     y = m.lora_expand_add(dev(Zh), dev(inp.B2), al, 2, dev(O), out_fp32=True, topk_w=dev(wt))
     assert_close(y, oracle.lora_expand_add(Zh, inp.B2, ref, O[:n], epilogue=2, w=wt),
                  KERNEL_RTOL, "expand epilogue 2, short segments")
+
+
+@pytest.mark.parametrize("r", [8, 16, 64])
+@pytest.mark.parametrize("k", [1, 3, 4])
+def test_expand_short_segment_forms(r, k):
+    """About one row per (expert, adapter) pair: the SwiGLU expand takes one sorted row per
+    CTA (all of a thread's loads issued before any is consumed) and the down expand walks
+    tokens; ranks 8..64, k = 1..4 slots per token, ragged column tails (I = 300, H = 520)."""
+    m, inp, ids, w, al, ref = _setup(T=48, H=520, I=300, E=32, k=k, L=8, r=r, seed=17,
+                                     adapters="round_robin_shuffled")
+    n = ref["n_valid"]
+    rng = np.random.default_rng(7)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, r))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 600), dtype=np.float32))
+    h = Guarded((al.S, 300), torch.bfloat16)
+    m.lora_expand_add(dev(Zh), dev(inp.B1), al, 1, dev(G), out=h.t)
+    h.check()
+    assert_bf16_close(h.t[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1),
+                      "expand epilogue 1, one row per CTA")
+    O = torch.from_numpy(rng.standard_normal((al.S, 520), dtype=np.float32))
+    wt = torch.as_tensor(w, dtype=torch.float32)
+    y = m.lora_expand_add(dev(Zh), dev(inp.B2), al, 2, dev(O), out_fp32=True, topk_w=dev(wt))
+    assert_close(y, oracle.lora_expand_add(Zh, inp.B2, ref, O[:n], epilogue=2, w=wt),
+                 KERNEL_RTOL, "expand epilogue 2, token walk")
+
+
+@pytest.mark.parametrize("K", [768, 2048])
+def test_shrink_short_blocks_all_ranks(K):
+    """Many short blocks (the many-adapter stress shape): one CTA takes all 32 ranks of a
+    block with two k-steps per load batch."""
+    m, inp, ids, w, al, ref = _setup(T=256, H=K, I=8, E=128, k=8, L=16, r=32, seed=18,
+                                     bm_lora=8, adapters="zipf1.1")
+    Z = Guarded((al.S, 32), torch.float32, fill=0.0)
+    m.lora_shrink(dev(inp.x), False, dev(inp.A1), al, out=Z.t)
+    Z.check()
+    assert_close(Z.t, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"K={K}")

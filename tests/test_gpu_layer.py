@@ -166,3 +166,52 @@ def test_layer_skewed_decode_multi_chunk():
     assert counts.max() > 96 and (counts == 0).any()  # four chunks of 32; idle experts
     y = run_layer(m, inp, y_fp32=True).cpu()
     assert_close(y, oracle_layer(inp), LAYER_RTOL, "skewed decode")
+
+
+def test_layers_chained_in_cuda_graph():
+    """Three layers chained on one stream (layer i + 1 reads layer i's y, one shared
+    workspace), captured in a CUDA graph with programmatic dependent launch across the
+    layer boundaries: the replay reproduces the eager chain bit for bit, and the first
+    layer matches the oracle."""
+    m = need_gpu()
+    inp = make_layer_inputs(T=24, H=256, I=192, E=8, k=2, L=3, r=16, seed=21,
+                            adapters="uniform_with_none", lora_std=None)
+    n = 3
+    Ws = [(dev(torch.roll(inp.W1, i, 0)), dev(torch.roll(inp.W2, i, 0)),
+           {nm: dev(torch.roll(getattr(inp, nm), i, 1)) for nm in ("A1", "B1", "A2", "B2")},
+           dev(torch.roll(inp.logits, i, 1))) for i in range(n)]
+    x = dev(inp.x)
+    ta = dev(inp.token_adapter)
+    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    ys = [torch.empty_like(x) for _ in range(n)]
+
+    def chain():
+        xin = x
+        for (w1, w2, lo, lg), y in zip(Ws, ys):
+            m.moe_lora_layer(xin, w1, w2, logits=lg, k=inp.k, token_adapter=ta, y=y,
+                             workspace=ws, **lo)
+            xin = y
+
+    chain()
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    for y in ys:
+        y.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        chain()
+    torch.cuda.current_stream().wait_stream(side)
+    for y in ys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(n):
+        assert torch.equal(ys[i], eager[i]), f"layer {i}: graph replay differs from eager"
+    assert m.get_error(ws) == 0
+    ref = oracle_layer(inp)
+    assert_close(eager[0].cpu(), ref, LAYER_RTOL, "first chained layer")
