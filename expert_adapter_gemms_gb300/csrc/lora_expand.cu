@@ -588,7 +588,11 @@ __global__ void __launch_bounds__(kExpandThreads)
 }
 
 // epilogue 0 (and the block-walk half of epilogue 2) with tensor cores:
-// base[row, n..n+1] += D for the rows of each LoRA block; one CTA per block.
+// base[row, n..n+1] += D for the rows of each LoRA block. A warp takes its column
+// tiles TB at a time: the B fragments and base values of all TB tiles are loaded
+// before any is reduced, so each warp keeps several KB of the read-modify-write
+// in flight (base is two or more launches old: with `early` the first batch goes
+// out before the wait).
 template <int KC>
 __global__ void __launch_bounds__(kExpandThreads)
     expand_add_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
@@ -596,79 +600,119 @@ __global__ void __launch_bounds__(kExpandThreads)
                           const int* __restrict__ sorted_slots, int N, int r, int E,
                           float* __restrict__ base, int col_chunks, int early) {
   constexpr int kWarps = kExpandThreads / 32;
+  constexpr int TB = 8 / KC > 1 ? 8 / KC : 1;  // tiles per batch
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   const int r_pad = 32 * KC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, q = lane & 3;
   if (!early) pdl_wait();
   const int b = blockIdx.x / col_chunks, chunk = blockIdx.x - b * col_chunks;
-  if (b >= __ldcg(hdr + HDR_NBLOCKS)) {
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
+  const int4 blk = __ldcg(blocks + b);  // in bounds: the grid covers the host's block bound
+  if (b >= nb) {
     if (early) pdl_wait();
     return;
   }
-  const int4 blk = __ldcg(blocks + b);
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
   const int all_tiles = (N + 7) / 8;
   const int per = (all_tiles + col_chunks - 1) / col_chunks;
   const int t_begin = chunk * per;
   const int ntiles = min(all_tiles, t_begin + per);
-  uint4 bf[KC];
-  auto fetch = [&](int t) {
-    const int nl = t * 8 + gid;
+  uint4 bf[TB][KC];
+  float2 ov[TB][2];
+  auto fetch = [&](int t0) {
 #pragma unroll
-    for (int c = 0; c < KC; ++c) bf[c] = b_frag(nl < N ? bl + (size_t)nl * r : nullptr, c, r);
+    for (int j = 0; j < TB; ++j) {
+      const int t = t0 + j * kWarps;
+      const int nl = t * 8 + gid, n = t * 8 + 2 * q;
+      const bool tv = t < ntiles;
+#pragma unroll
+      for (int c = 0; c < KC; ++c)
+        bf[j][c] = b_frag(tv && nl < N ? bl + (size_t)nl * r : nullptr, c, r);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int m = gid + 8 * half;
+        ov[j][half] = make_float2(0.f, 0.f);
+        if (tv && n < N && m < rows)
+          ov[j][half] = __ldcg(reinterpret_cast<const float2*>(base + (size_t)(row0 + m) * N + n));
+      }
+    }
   };
-  int t = t_begin + warp;
-  if (t < ntiles) fetch(t);
+  int t0 = t_begin + warp;
+  if (early && t0 < ntiles) fetch(t0);
   if (early) pdl_wait();
   pdl_trigger();
   stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
   __syncthreads();
   ZFrag<KC> z;
   z.load(zb, r_pad);
-  for (; t < ntiles; t += kWarps) {
-    uint4 cur[KC];
+  if (!early && t0 < ntiles) fetch(t0);
+  for (; t0 < ntiles; t0 += TB * kWarps) {
 #pragma unroll
-    for (int c = 0; c < KC; ++c) cur[c] = bf[c];
-    if (t + kWarps < ntiles) fetch(t + kWarps);
-    float d[4];
-    block_mma<KC>(d, z, cur);
-    const int n = t * 8 + 2 * q;
-    if (n >= N) continue;
+    for (int j = 0; j < TB; ++j) {
+      const int t = t0 + j * kWarps;
+      const int n = t * 8 + 2 * q;
+      if (t >= ntiles || n >= N) continue;
+      float d[4];
+      block_mma<KC>(d, z, bf[j]);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int m = gid + 8 * half;
-      if (m >= rows) continue;
-      float2* o = reinterpret_cast<float2*>(base + (size_t)(row0 + m) * N + n);
-      float2 v = __ldcg(o);
-      v.x += d[2 * half];
-      v.y += d[2 * half + 1];
-      *o = v;
+      for (int half = 0; half < 2; ++half) {
+        const int m = gid + 8 * half;
+        if (m >= rows) continue;
+        float2 v = ov[j][half];
+        v.x += d[2 * half];
+        v.y += d[2 * half + 1];
+        *reinterpret_cast<float2*>(base + (size_t)(row0 + m) * N + n) = v;
+      }
     }
+    if (t0 + TB * kWarps < ntiles) fetch(t0 + TB * kWarps);
   }
 }
 
 // ----------------------------------------------------------------------------
 // Weighted top-k combine after an in-place expand over LoRA blocks:
 //   y[t, n] = sum_j w[t, j] * O[row(t, j), n], j ascending.
+// The CTA's slot rows and weights are staged in shared memory first; then each
+// thread issues the O values of all of a token's slots (eight at a time) before
+// it sums them, in j order.
 // ----------------------------------------------------------------------------
 template <bool kOutF32>
 __global__ void __launch_bounds__(kExpandThreads)
     combine_kernel(const float* __restrict__ O, const float* __restrict__ w,
                    const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
                    int tokens_per_cta) {
+  constexpr int KM = 8;
+  __shared__ int s_row[kExpandThreads];
+  __shared__ float s_w[kExpandThreads];
   pdl_wait();
   pdl_trigger();
-  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
-  if (n >= N) return;
   const int t0 = blockIdx.x * tokens_per_cta;
   const int t1 = min(T, t0 + tokens_per_cta);
+  const int ns = (t1 - t0) * k;  // the host keeps tokens_per_cta * k <= 256
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    s_row[i] = __ldcg(slot_row + (size_t)t0 * k + i);
+    s_w[i] = __ldcg(w + (size_t)t0 * k + i);
+  }
+  __syncthreads();
+  const int n = blockIdx.y * kExpandThreads + threadIdx.x;
+  if (n >= N) return;
   for (int t = t0; t < t1; ++t) {
+    const int q0 = (t - t0) * k;
     float acc = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int row = __ldcg(slot_row + (size_t)t * k + j);
-      if (row >= 0) acc = fmaf(__ldcg(w + (size_t)t * k + j), __ldcg(O + (size_t)row * N + n), acc);
+    for (int j0 = 0; j0 < k; j0 += KM) {
+      float o[KM];
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        o[j] = 0.f;
+        if (j0 + j < k) {
+          const int row = s_row[q0 + j0 + j];
+          if (row >= 0) o[j] = __ldcg(O + (size_t)row * N + n);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        if (j0 + j < k && s_row[q0 + j0 + j] >= 0) acc = fmaf(s_w[q0 + j0 + j], o[j], acc);
     }
     if (kOutF32) static_cast<float*>(y)[(size_t)t * N + n] = acc;
     else static_cast<__nv_bfloat16*>(y)[(size_t)t * N + n] = __float2bfloat16_rn(acc);
@@ -816,7 +860,9 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     if (st != MOE_LORA_OK) return st;
     const int ncol = ceil_div(N, kExpandThreads);
     int tpc = 1;
-    while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms) tpc *= 2;
+    while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms &&
+           tpc * 2 * al->k <= kExpandThreads)
+      tpc *= 2;
     const dim3 g2(ceil_div(al->T, tpc), ncol);
     return out_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl,
                                  (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
