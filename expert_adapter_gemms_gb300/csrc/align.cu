@@ -73,7 +73,7 @@ __host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nt
   AlignSmem p;
   const int nw = nthreads / 32;
   p.hist_off = 0;
-  p.tmp_off = 256 * nw;
+  p.tmp_off = 256 * (nw + 1);
   int o = p.tmp_off + 64;
   const size_t sort_b = (size_t)2 * S * 4;
   const size_t bucket_b = (size_t)2 * nbuckets * 4;
@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(NT, 1)
   constexpr int NW = NT / 32;
   extern __shared__ __align__(16) int smem[];
   const AlignSmem plan = align_smem_plan(S, nbuckets, NT);
-  int* hist = smem + plan.hist_off;  // [256 digits][NW warps]
+  // [256 digits][NW warps + 1]: the pad puts a warp's different digits in different banks
+  constexpr int HS = NW + 1;
+  int* hist = smem + plan.hist_off;
   int* tmp = smem + plan.tmp_off;
   int* bcount = plan.smem_buckets ? smem + plan.bcount_off : v.bucket_count;
   int* bstart = plan.smem_buckets ? smem + plan.bstart_off : v.bucket_start;
@@ -114,18 +116,32 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) s_err = 0u;
   __syncthreads();
 
-  // 1. keys
-  for (int s = tid; s < S; s += NT) {
-    const int t = s / k;
-    const int e = __ldcg(ids + s);
-    const int l = token_adapter ? __ldcg(token_adapter + t) : -1;
-    unsigned int bad = 0;
-    if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
-    if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
-    int key = drop;
-    if (bad) atomicOr(&s_err, bad);
-    else key = e * (L + 1) + (l + 1);
-    bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
+  // 1. keys (the loads of four slots go out together)
+  for (int s0 = tid; s0 < S; s0 += 4 * NT) {
+    int ev[4], lv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * NT;
+      ev[u] = 0;
+      lv[u] = -1;
+      if (s < S) {
+        ev[u] = __ldcg(ids + s);
+        if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * NT;
+      if (s >= S) break;
+      const int e = ev[u], l = lv[u];
+      unsigned int bad = 0;
+      if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
+      if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
+      int key = drop;
+      if (bad) atomicOr(&s_err, bad);
+      else key = e * (L + 1) + (l + 1);
+      bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
+    }
   }
   __syncthreads();
 
@@ -136,7 +152,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int wb = min(S, warp * chunk), we = min(S, wb + chunk);
   const unsigned lt = (1u << lane) - 1u;
   for (int shift = slot_bits; shift < slot_bits + key_bits; shift += 8) {
-    for (int d = lane; d < 256; d += 32) hist[d * NW + warp] = 0;
+    for (int d = lane; d < 256; d += 32) hist[d * HS + warp] = 0;
     __syncwarp();
     for (int base = wb; base < we; base += 32) {
       const int i = base + lane;
@@ -145,7 +161,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (act) {
         const int d = (src[i] >> shift) & 255;
         const unsigned peers = digit_peers(mask, d);
-        if (lane == __ffs(peers) - 1) hist[d * NW + warp] += __popc(peers);
+        if (lane == __ffs(peers) - 1) hist[d * HS + warp] += __popc(peers);
       }
       __syncwarp();
     }
@@ -156,14 +172,16 @@ __global__ void __launch_bounds__(NT, 1)
       int s = 0;
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
-        loc[q] = hist[tid * PER + q];
+        const int pidx = tid * PER + q;  // (digit, warp) in digit-major order
+        loc[q] = hist[(pidx / NW) * HS + pidx % NW];
         s += loc[q];
       }
       int total;
       int run = block_exclusive_scan<NW>(s, tmp, &total);
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
-        hist[tid * PER + q] = run;
+        const int pidx = tid * PER + q;
+        hist[(pidx / NW) * HS + pidx % NW] = run;
         run += loc[q];
       }
     }
@@ -178,10 +196,10 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t x = src[i];
         d = (x >> shift) & 255;
         peers = digit_peers(mask, d);
-        dst[hist[d * NW + warp] + __popc(peers & lt)] = x;
+        dst[hist[d * HS + warp] + __popc(peers & lt)] = x;
       }
       __syncwarp();
-      if (act && lane == __ffs(peers) - 1) hist[d * NW + warp] += __popc(peers);
+      if (act && lane == __ffs(peers) - 1) hist[d * HS + warp] += __popc(peers);
       __syncwarp();
     }
     __syncthreads();
@@ -205,52 +223,76 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
   const int n_valid = bstart[drop];
 
-  // 4. sorted rows, expert starts
+  // 4. sorted rows, expert starts. slot_row is the inverse permutation: with the sort in
+  //    shared memory it is built in the free sort buffer and then written out coalesced.
+  int* inv = plan.smem_sort ? reinterpret_cast<int*>(dst) : nullptr;
   for (int i = tid; i < S; i += NT) {
     const uint32_t x = src[i];
     const int s = static_cast<int>(x & smask);
     const int key = static_cast<int>(x >> slot_bits);
     if (key == drop) {
       v.sorted_slots[i] = -1;
-      v.slot_row[s] = -1;
+      if (inv) inv[s] = -1;
+      else v.slot_row[s] = -1;
     } else {
       const int e = key / (L + 1), l = key % (L + 1) - 1;
       v.sorted_slots[i] = s;
-      v.slot_row[s] = i;
+      if (inv) inv[s] = i;
+      else v.slot_row[s] = i;
       v.row_expert[i] = e;
       v.row_adapter[i] = l;
     }
   }
   for (int e = tid; e <= E; e += NT) v.expert_begin[e] = bstart[e * (L + 1)];
-  if (!plan.smem_buckets) __syncthreads();  // global bucket arrays: make the scan visible
+  __syncthreads();  // the inverse permutation (and global bucket arrays) complete
+  if (inv)
+    for (int s = tid; s < S; s += NT) v.slot_row[s] = inv[s];
 
-  // 5. token tiles (per expert, bm_base rows) and LoRA blocks (per (e, l>=0), bm_lora rows)
-  const int c = (n_valid + NT - 1) / NT;
-  const int b = tid * c, en = min(n_valid, b + c);
-  int nt = 0, nb = 0, nl = 0;
-  for (int i = b; i < en; ++i) {
-    const int key = static_cast<int>(src[i] >> slot_bits);
-    const int e = key / (L + 1), l = key % (L + 1) - 1;
-    if ((i - bstart[e * (L + 1)]) % bm_base == 0) ++nt;
+  // 5. token tiles (per expert, bm_base rows) and LoRA blocks (per (e, l>=0), bm_lora rows),
+  //    numbered in sorted-row order. Each warp takes a contiguous range of rows and its lanes
+  //    consecutive rows; ballots order the starts inside the warp, a block scan across warps.
+  const int per_w = ((n_valid + NW - 1) / NW + 31) & ~31;
+  const int wb5 = min(n_valid, warp * per_w), we5 = min(n_valid, wb5 + per_w);
+  auto starts = [&](int i, int& e, int& l, int& key, bool& ft, bool& fb, bool& fl) {
+    ft = fb = fl = false;
+    e = l = key = 0;
+    if (i >= we5) return;
+    key = static_cast<int>(src[i] >> slot_bits);
+    e = key / (L + 1);
+    l = key % (L + 1) - 1;
+    ft = (i - bstart[e * (L + 1)]) % bm_base == 0;
     if (l >= 0) {
-      ++nl;
-      if ((i - bstart[key]) % bm_lora == 0) ++nb;
+      fl = true;
+      fb = (i - bstart[key]) % bm_lora == 0;
     }
+  };
+  int nt = 0, nb = 0, nl = 0;
+  for (int base = wb5; base < we5; base += 32) {
+    int e, l, key;
+    bool ft, fb, fl;
+    starts(base + lane, e, l, key, ft, fb, fl);
+    nt += __popc(__ballot_sync(0xffffffffu, ft));
+    nb += __popc(__ballot_sync(0xffffffffu, fb));
+    nl += __popc(__ballot_sync(0xffffffffu, fl));
   }
   int tot_t, tot_b, tot_l;
-  int ti = block_exclusive_scan<NW>(nt, tmp, &tot_t);
-  int bi = block_exclusive_scan<NW>(nb, tmp, &tot_b);
-  block_exclusive_scan<NW>(nl, tmp, &tot_l);
-  for (int i = b; i < en; ++i) {
-    const int key = static_cast<int>(src[i] >> slot_bits);
-    const int e = key / (L + 1), l = key % (L + 1) - 1;
-    const int eb = bstart[e * (L + 1)];
-    if ((i - eb) % bm_base == 0)
-      v.tiles[ti++] = make_int4(e, i, min(bm_base, bstart[(e + 1) * (L + 1)] - i), 0);
-    if (l >= 0) {
+  int ti = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nt : 0, tmp, &tot_t), 0);
+  int bi = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nb : 0, tmp, &tot_b), 0);
+  block_exclusive_scan<NW>(lane == 0 ? nl : 0, tmp, &tot_l);
+  for (int base = wb5; base < we5; base += 32) {
+    const int i = base + lane;
+    int e, l, key;
+    bool ft, fb, fl;
+    starts(i, e, l, key, ft, fb, fl);
+    const unsigned bt = __ballot_sync(0xffffffffu, ft), bb = __ballot_sync(0xffffffffu, fb);
+    if (ft)
+      v.tiles[ti + __popc(bt & lt)] = make_int4(e, i, min(bm_base, bstart[(e + 1) * (L + 1)] - i), 0);
+    if (fb) {
       const int sb = bstart[key];
-      if ((i - sb) % bm_lora == 0) v.blocks[bi++] = make_int4(i, min(bm_lora, sb + bcount[key] - i), e, l);
+      v.blocks[bi + __popc(bb & lt)] = make_int4(i, min(bm_lora, sb + bcount[key] - i), e, l);
     }
+    ti += __popc(bt);
+    bi += __popc(bb);
   }
   if (tid == 0) {
     if (s_err) atomicOr(reinterpret_cast<unsigned int*>(v.hdr + HDR_ERR), s_err);

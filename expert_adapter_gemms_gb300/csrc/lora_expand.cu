@@ -25,6 +25,9 @@ namespace moe_lora {
 constexpr int kExpandThreads = 256;
 constexpr int kMaxBmLora = 16;
 constexpr int kMaxRegRank = 64;  // ranks held in registers; larger r reads B from L1
+constexpr int kGStages = 6;     // tiles of G in flight per warp in the tensor-core SwiGLU expand
+// bytes of the z staging area (bf16 high parts and remainders, 16 rows) for KC rank chunks
+__host__ __device__ constexpr size_t zsmem_bytes(int KC) { return (size_t)2 * 16 * 32 * KC * 2; }
 
 __device__ __forceinline__ void fma8(float& acc, const float* z, uint4 u) {
   acc = fmaf(z[0], bf16_lo(u.x), acc);
@@ -35,6 +38,19 @@ __device__ __forceinline__ void fma8(float& acc, const float* z, uint4 u) {
   acc = fmaf(z[5], bf16_hi(u.z), acc);
   acc = fmaf(z[6], bf16_lo(u.w), acc);
   acc = fmaf(z[7], bf16_hi(u.w), acc);
+}
+
+// 16-byte asynchronous copy global -> shared at L2 (coherent with earlier launches);
+// `valid` false zero-fills the destination without reading the source.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // dot(z[0..r), B row) reading the B row from memory (any r, any alignment when !kVec).
@@ -494,63 +510,78 @@ __global__ void __launch_bounds__(kExpandThreads)
     const int per = (all_tiles + col_chunks - 1) / col_chunks;
     const int t_begin = chunk * per;
     const int ntiles = min(all_tiles, t_begin + per);
-    // operands of tile t (B fragments: weights; G: two launches old)
+    // B fragments of a tile go to registers one tile ahead; the G values of the block's
+    // rows (the largest stream: fp32 rows of the gate_up GEMM) go through a per-warp
+    // ring of kGStages tiles in shared memory with asynchronous copies, so each warp
+    // keeps several KB of G in flight without spending registers on it. A tile's G
+    // part is [16 rows][8 columns] fp32 for gate and for up: lane -> (row lane / 2,
+    // columns 4 (lane % 2) .. +3), one 16-byte copy per part.
     uint4 bg[KC], bu[KC];
-    float2 gg[2], gu[2];
-    auto fetch = [&](int t, bool with_g) {
-      const int nl = t * 8 + gid, n = t * 8 + 2 * q;
+    auto fetch_b = [&](int t) {
+      const int nl = t * 8 + gid;
 #pragma unroll
       for (int c = 0; c < KC; ++c) {
         bg[c] = b_frag(nl < I ? bl + (size_t)nl * r : nullptr, c, r);
         bu[c] = b_frag(nl < I ? bl + (size_t)(I + nl) * r : nullptr, c, r);
       }
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int m = gid + 8 * half;
-        gg[half] = gu[half] = make_float2(0.f, 0.f);
-        if (with_g && m < rows && n < I) {
-          const size_t gr = (size_t)(row0 + m) * twoI;
-          gg[half] = __ldcg(reinterpret_cast<const float2*>(G + gr + n));
-          gu[half] = __ldcg(reinterpret_cast<const float2*>(G + gr + I + n));
-        }
+    };
+    float* gring = reinterpret_cast<float*>(smem_raw + zsmem_bytes(KC)) + warp * (kGStages * 256);
+    auto fetch_g = [&](int t, int stage) {
+      if (t < ntiles) {
+        const int m = lane >> 1, c4 = (lane & 1) * 4;
+        const int n = t * 8 + c4;
+        const bool ok = m < rows && n < I;
+        const float* src = ok ? G + (size_t)(row0 + m) * twoI + n : G;
+        float* dst = gring + stage * 256 + m * 8 + c4;
+        cp_async16(dst, src, ok);
+        cp_async16(dst + 128, ok ? src + I : G, ok);
       }
+      cp_async_commit();  // one group per stage, empty or not
     };
     int t = t_begin + warp;
-    if (t < ntiles) fetch(t, early);
+#pragma unroll
+    for (int d = 0; d < kGStages - 1; ++d) fetch_g(t + d * kWarps, d);
+    if (t < ntiles) fetch_b(t);
     if (early) pdl_wait();
     pdl_trigger();
     stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
     __syncthreads();
     ZFrag<KC> z;
     z.load(zb, r_pad);
-    if (!early && t < ntiles) fetch(t, true);
-    for (; t < ntiles; t += kWarps) {
-      const uint4 (&cbg)[KC] = bg;
+    for (int j = 0; t < ntiles; t += kWarps, ++j) {
+      fetch_g(t + (kGStages - 1) * kWarps, (j + kGStages - 1) % kGStages);
+      cp_async_wait<kGStages - 1>();  // this tile's copies have landed
+      __syncwarp();                   // ... every lane's
       uint4 tg[KC], tu[KC];
-      float2 tgg[2] = {gg[0], gg[1]}, tgu[2] = {gu[0], gu[1]};
 #pragma unroll
       for (int c = 0; c < KC; ++c) {
-        tg[c] = cbg[c];
+        tg[c] = bg[c];
         tu[c] = bu[c];
       }
-      if (t + kWarps < ntiles) fetch(t + kWarps, true);  // next tile in flight
+      if (t + kWarps < ntiles) fetch_b(t + kWarps);  // next tile's B in flight
       float dg[4], du[4];
       block_mma<KC>(dg, z, tg);
       block_mma<KC>(du, z, tu);
       const int n = t * 8 + 2 * q;
-      if (n >= I) continue;
+      const float* gs = gring + (j % kGStages) * 256;
+      if (n < I) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int m = gid + 8 * half;
-        if (m >= rows) continue;
-        const float g0 = tgg[half].x + dg[2 * half], g1 = tgg[half].y + dg[2 * half + 1];
-        const float u0 = tgu[half].x + du[2 * half], u1 = tgu[half].y + du[2 * half + 1];
-        __nv_bfloat162 o;
-        o.x = __float2bfloat16_rn(g0 / (1.f + expf(-g0)) * u0);
-        o.y = __float2bfloat16_rn(g1 / (1.f + expf(-g1)) * u1);
-        *reinterpret_cast<__nv_bfloat162*>(h + (size_t)(row0 + m) * I + n) = o;
+        for (int half = 0; half < 2; ++half) {
+          const int m = gid + 8 * half;
+          if (m >= rows) continue;
+          const float2 gv = *reinterpret_cast<const float2*>(gs + m * 8 + 2 * q);
+          const float2 uv = *reinterpret_cast<const float2*>(gs + 128 + m * 8 + 2 * q);
+          const float g0 = gv.x + dg[2 * half], g1 = gv.y + dg[2 * half + 1];
+          const float u0 = uv.x + du[2 * half], u1 = uv.y + du[2 * half + 1];
+          __nv_bfloat162 o;
+          o.x = __float2bfloat16_rn(g0 / (1.f + expf(-g0)) * u0);
+          o.y = __float2bfloat16_rn(g1 / (1.f + expf(-g1)) * u1);
+          *reinterpret_cast<__nv_bfloat162*>(h + (size_t)(row0 + m) * I + n) = o;
+        }
       }
+      __syncwarp();  // the stage is read by every lane before it is refilled
     }
+    cp_async_wait<0>();
   } else {
     // adapter-free rows of one token tile: plain SwiGLU, two columns per thread
     const int nch = (I + kChunk - 1) / kChunk;
@@ -787,12 +818,26 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   };
   if (epilogue == 0 && mma_ok) return add_mma(dim3(a.max_blocks));
   const bool short_segments = (int64_t)a.S <= 2 * (int64_t)al->E * (al->L > 0 ? al->L : 1);
-  if (epilogue == 1 && !short_segments && (mma_ok || (!Bp && (N / 2) % 2 == 0))) {
+  // epilogue 1 with tensor cores also streams G through 16-byte asynchronous copies:
+  // G 16-byte aligned and I % 4 == 0
+  const bool g_ok = aligned16(base) && (N / 2) % 4 == 0;
+  if (epilogue == 1 && !short_segments && ((mma_ok && g_ok) || (!Bp && (N / 2) % 2 == 0))) {
     const int I = N / 2;
     const int cc = chunks_for(I);
     const dim3 grid(a.max_blocks * cc + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
-    auto go = [&](auto kern) {
-      return launch_pdl(kern, grid, kExpandThreads, Bp ? zsmem : 0, stream, pdl, Z, Bp,
+    const size_t smem1 = Bp ? zsmem + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float) : 0;
+    auto go = [&](auto kern) -> int {
+      static int configured[64][4] = {};
+      int dev = 0;
+      ML_CHECK_CUDA(cudaGetDevice(&dev));
+      const int slot = kcp == 1 ? 0 : kcp == 2 ? 1 : kcp == 4 ? 2 : 3;
+      if (dev < 64 && !configured[dev][slot]) {
+        ML_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)(zsmem_bytes(8) + (size_t)(kExpandThreads / 32) *
+                                                 kGStages * 256 * sizeof(float))));
+        configured[dev][slot] = 1;
+      }
+      return launch_pdl(kern, grid, kExpandThreads, smem1, stream, pdl, Z, Bp,
                         (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
                         (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
                         (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, cc,

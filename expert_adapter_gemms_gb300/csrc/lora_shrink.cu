@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, q = lane & 3;
+  // the slot of the first z element this thread stores, fetched with the operands
+  const int slot0 = (int)threadIdx.x < rows * R ? __ldcg(sorted_slots + row0 + threadIdx.x / R) : 0;
 
   const __nv_bfloat16* Ab = A + ((size_t)l * E + e) * (size_t)r * K;
   const __nv_bfloat16* ap[NT];
@@ -170,7 +172,8 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < kShrinkWarps; ++w) sum += red[w][m][c];
-    Z[(size_t)__ldcg(sorted_slots + row0 + m) * r + rank] = sum;
+    const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
+    Z[(size_t)slot * r + rank] = sum;
   }
 }
 

@@ -280,3 +280,21 @@ def test_shrink_short_blocks_all_ranks(K):
     m.lora_shrink(dev(inp.x), False, dev(inp.A1), al, out=Z.t)
     Z.check()
     assert_close(Z.t, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"K={K}")
+
+
+@pytest.mark.parametrize("I", [300, 302, 1024])
+@pytest.mark.parametrize("r", [16, 64])
+def test_expand_swiglu_long_segments_ragged(I, r):
+    """Long (expert, adapter) segments take the tensor-core SwiGLU expand, whose G rows
+    stream through a ring of asynchronous copies: a ragged last column tile (I = 300),
+    I % 4 != 0 (302, the CUDA-core fallback) and two rank chunks (r = 64)."""
+    m, inp, ids, w, al, ref = _setup(T=512, H=64, I=I, E=4, k=2, L=2, r=r, seed=19)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(8)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, r))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 2 * I), dtype=np.float32))
+    h = Guarded((al.S, I), torch.bfloat16)
+    m.lora_expand_add(dev(Zh), dev(inp.B1), al, 1, dev(G), out=h.t)
+    h.check()
+    assert_bf16_close(h.t[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1),
+                      f"expand epilogue 1, long segments, I={I} r={r}")
