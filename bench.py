@@ -318,13 +318,17 @@ def run_reference(args):
 
 
 def launches_per_layer(inp) -> int:
-    """Kernels one layer call launches: route, align, gather, two grouped GEMMs, the
-    SwiGLU expand and the down expand (+ combine), plus the two shrinks with adapters;
-    with several rows per (expert, adapter) pair the down expand adds in place and a
-    separate combine kernel follows."""
+    """Kernels one layer call launches: route, align (three kernels with many slots),
+    gather, two grouped GEMMs, the SwiGLU expand and the down expand (+ combine), plus
+    the two shrinks with adapters; with several rows per (expert, adapter) pair the down
+    expand adds in place and a separate combine kernel follows."""
+    nb = inp.E * (inp.L + 1) + 1
+    ctas = (inp.S + 511) // 512
+    multi = inp.S >= 2048 and 2 * nb <= inp.S and nb * ctas <= (1 << 22)
+    align = 3 if multi else 1  # the multi-CTA align is three kernels
     if not inp.L:
-        return 7
-    return 9 + (1 if inp.S >= 2 * inp.E * inp.L else 0)
+        return 6 + align
+    return 8 + align + (1 if inp.S >= 2 * inp.E * inp.L else 0)
 
 
 def multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, n_layers, steps, warmup):

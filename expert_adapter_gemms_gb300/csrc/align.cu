@@ -62,96 +62,23 @@ __device__ __forceinline__ unsigned digit_peers(unsigned mask, int d) {
   return peers;
 }
 
-// Shared-memory plan of one align launch (host and device agree through this).
-struct AlignSmem {
-  int hist_off, tmp_off, bcount_off, bstart_off, sort_off;  // in ints
-  size_t bytes;
-  bool smem_buckets, smem_sort;
-};
-
-__host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nthreads) {
-  AlignSmem p;
-  const int nw = nthreads / 32;
-  p.hist_off = 0;
-  p.tmp_off = 256 * (nw + 1);
-  int o = p.tmp_off + 64;
-  const size_t sort_b = (size_t)2 * S * 4;
-  const size_t bucket_b = (size_t)2 * nbuckets * 4;
-  p.smem_sort = S <= kSmemSortMaxSlots;
-  const size_t base = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
-  p.smem_buckets = base + bucket_b <= kAlignSmemBudget;
-  p.bcount_off = o;
-  p.bstart_off = o + (p.smem_buckets ? nbuckets : 0);
-  o = p.bstart_off + (p.smem_buckets ? nbuckets : 0);
-  p.sort_off = o;
-  p.bytes = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
-  return p;
-}
-
+// Stable least-significant-digit radix sort of the n words in a (n fits a and b) on
+// bits [lo, lo + nbits), 8-bit digits; returns the buffer that holds the result. Each
+// warp owns a contiguous range of words; per-warp digit histograms (padded rows, so a
+// warp's different digits fall in different banks) give every (digit, warp) its
+// output offset, and a lane's rank among same-digit lanes of its warp comes from eight
+// ballots. All NT threads call it; hist holds 256 * (NT / 32 + 1) ints, tmp NT / 32 + 1.
 template <int NT>
-__global__ void __launch_bounds__(NT, 1)
-    align_kernel(const int* __restrict__ ids, const int* __restrict__ token_adapter, AlignView v,
-                 int T, int k, int E, int L, int bm_base, int bm_lora, int S, int nbuckets,
-                 int key_bits, int slot_bits) {
-  constexpr int NW = NT / 32;
-  extern __shared__ __align__(16) int smem[];
-  const AlignSmem plan = align_smem_plan(S, nbuckets, NT);
-  // [256 digits][NW warps + 1]: the pad puts a warp's different digits in different banks
-  constexpr int HS = NW + 1;
-  int* hist = smem + plan.hist_off;
-  int* tmp = smem + plan.tmp_off;
-  int* bcount = plan.smem_buckets ? smem + plan.bcount_off : v.bucket_count;
-  int* bstart = plan.smem_buckets ? smem + plan.bstart_off : v.bucket_start;
-  uint32_t* bufA = plan.smem_sort ? reinterpret_cast<uint32_t*>(smem + plan.sort_off) : v.sort0;
-  uint32_t* bufB = plan.smem_sort ? bufA + S : v.sort1;
-  __shared__ unsigned int s_err;
-
+__device__ uint32_t* block_radix_sort(uint32_t* a, uint32_t* b, int n, int lo, int nbits, int* hist,
+                                      int* tmp) {
+  constexpr int NW = NT / 32, HS = NW + 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int drop = nbuckets - 1;
-  const uint32_t smask = (slot_bits >= 32) ? 0xffffffffu : ((1u << slot_bits) - 1u);
-
-  // the next launch waits before reading any of this launch's results
-  pdl_trigger();
-  pdl_wait();
-  if (tid == 0) s_err = 0u;
-  __syncthreads();
-
-  // 1. keys (the loads of four slots go out together)
-  for (int s0 = tid; s0 < S; s0 += 4 * NT) {
-    int ev[4], lv[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int s = s0 + u * NT;
-      ev[u] = 0;
-      lv[u] = -1;
-      if (s < S) {
-        ev[u] = __ldcg(ids + s);
-        if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int s = s0 + u * NT;
-      if (s >= S) break;
-      const int e = ev[u], l = lv[u];
-      unsigned int bad = 0;
-      if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
-      if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
-      int key = drop;
-      if (bad) atomicOr(&s_err, bad);
-      else key = e * (L + 1) + (l + 1);
-      bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
-    }
-  }
-  __syncthreads();
-
-  // 2. stable LSD radix sort on the key bits (8-bit digits)
-  uint32_t* src = bufA;
-  uint32_t* dst = bufB;
-  const int chunk = (S + NW - 1) / NW;
-  const int wb = min(S, warp * chunk), we = min(S, wb + chunk);
+  uint32_t* src = a;
+  uint32_t* dst = b;
+  const int chunk = (n + NW - 1) / NW;
+  const int wb = min(n, warp * chunk), we = min(n, wb + chunk);
   const unsigned lt = (1u << lane) - 1u;
-  for (int shift = slot_bits; shift < slot_bits + key_bits; shift += 8) {
+  for (int shift = lo; shift < lo + nbits; shift += 8) {
     for (int d = lane; d < 256; d += 32) hist[d * HS + warp] = 0;
     __syncwarp();
     for (int base = wb; base < we; base += 32) {
@@ -207,6 +134,94 @@ __global__ void __launch_bounds__(NT, 1)
     src = dst;
     dst = sw;
   }
+  return src;
+}
+
+// Shared-memory plan of one align launch (host and device agree through this).
+struct AlignSmem {
+  int hist_off, tmp_off, bcount_off, bstart_off, sort_off;  // in ints
+  size_t bytes;
+  bool smem_buckets, smem_sort;
+};
+
+__host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nthreads) {
+  AlignSmem p;
+  const int nw = nthreads / 32;
+  p.hist_off = 0;
+  p.tmp_off = 256 * (nw + 1);
+  int o = p.tmp_off + 64;
+  const size_t sort_b = (size_t)2 * S * 4;
+  const size_t bucket_b = (size_t)2 * nbuckets * 4;
+  p.smem_sort = S <= kSmemSortMaxSlots;
+  const size_t base = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
+  p.smem_buckets = base + bucket_b <= kAlignSmemBudget;
+  p.bcount_off = o;
+  p.bstart_off = o + (p.smem_buckets ? nbuckets : 0);
+  o = p.bstart_off + (p.smem_buckets ? nbuckets : 0);
+  p.sort_off = o;
+  p.bytes = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
+  return p;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT, 1)
+    align_kernel(const int* __restrict__ ids, const int* __restrict__ token_adapter, AlignView v,
+                 int T, int k, int E, int L, int bm_base, int bm_lora, int S, int nbuckets,
+                 int key_bits, int slot_bits) {
+  constexpr int NW = NT / 32;
+  extern __shared__ __align__(16) int smem[];
+  const AlignSmem plan = align_smem_plan(S, nbuckets, NT);
+  int* hist = smem + plan.hist_off;  // [256 digits][NW warps + 1]
+  int* tmp = smem + plan.tmp_off;
+  int* bcount = plan.smem_buckets ? smem + plan.bcount_off : v.bucket_count;
+  int* bstart = plan.smem_buckets ? smem + plan.bstart_off : v.bucket_start;
+  uint32_t* bufA = plan.smem_sort ? reinterpret_cast<uint32_t*>(smem + plan.sort_off) : v.sort0;
+  uint32_t* bufB = plan.smem_sort ? bufA + S : v.sort1;
+  __shared__ unsigned int s_err;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int drop = nbuckets - 1;
+  const uint32_t smask = (slot_bits >= 32) ? 0xffffffffu : ((1u << slot_bits) - 1u);
+
+  // the next launch waits before reading any of this launch's results
+  pdl_trigger();
+  pdl_wait();
+  if (tid == 0) s_err = 0u;
+  __syncthreads();
+
+  // 1. keys (the loads of four slots go out together)
+  for (int s0 = tid; s0 < S; s0 += 4 * NT) {
+    int ev[4], lv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * NT;
+      ev[u] = 0;
+      lv[u] = -1;
+      if (s < S) {
+        ev[u] = __ldcg(ids + s);
+        if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u * NT;
+      if (s >= S) break;
+      const int e = ev[u], l = lv[u];
+      unsigned int bad = 0;
+      if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
+      if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
+      int key = drop;
+      if (bad) atomicOr(&s_err, bad);
+      else key = e * (L + 1) + (l + 1);
+      bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
+    }
+  }
+  __syncthreads();
+
+  // 2. stable LSD radix sort on the key bits (8-bit digits)
+  uint32_t* src = block_radix_sort<NT>(bufA, bufB, S, slot_bits, key_bits, hist, tmp);
+  uint32_t* dst = src == bufA ? bufB : bufA;
+  const unsigned lt = (1u << lane) - 1u;
 
   // 3. segment starts: bucket c starts at the first sorted word with key >= c
   //    (bucket order is expert-major, adapter -1 first); each sorted position
@@ -309,6 +324,213 @@ __global__ void __launch_bounds__(NT, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Multi-CTA align (many slots): the one-CTA kernel above runs its sort on one SM;
+// here the same unique stable order comes from three launches.
+//  local: CTA c takes slots [c C, (c + 1) C) (C = kAlignChunk), computes their keys,
+//         sorts them stably with the block radix sort, and records for each word its
+//         rank among the CTA's words of the same key and, per key, the CTA's count
+//         in counts[c][key].
+//  scan:  one CTA turns the count table, read in (key, CTA) order, into exclusive
+//         offsets: the first sorted position of CTA c's words of each key. Bucket
+//         starts, expert starts, token tiles, LoRA blocks and the header follow
+//         from the per-key totals.
+//  place: word i of CTA c goes to offsets[c][key] + its rank.
+// Keys ordered by (key, CTA, rank within the CTA) are ordered by (key, slot), since the
+// CTAs hold increasing slot ranges and each CTA's sort is stable.
+// ----------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(NT)
+    align_local_kernel(const int* __restrict__ ids, const int* __restrict__ token_adapter,
+                       AlignView v, int k, int E, int L, int S, int nbuckets, int key_bits,
+                       int slot_bits, int ctas) {
+  constexpr int NW = NT / 32, C = kAlignChunk, PT = C / NT;
+  __shared__ uint32_t bufA[C], bufB[C];
+  __shared__ int hist[256 * (NW + 1)];
+  __shared__ int tmp[NW + 1];
+  __shared__ int head[C];
+  __shared__ unsigned int s_err;
+  // the next launch waits before reading any of this launch's results
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x, tid = threadIdx.x;
+  const int s0 = c * C, n = min(C, S - s0);
+  const int drop = nbuckets - 1;
+  if (tid == 0) s_err = 0u;
+  int* cnt_c = v.counts + (size_t)c * nbuckets;  // this CTA's row of the count table
+  for (int b = tid; b < nbuckets; b += NT) cnt_c[b] = 0;
+  int ev[PT], lv[PT];
+#pragma unroll
+  for (int u = 0; u < PT; ++u) {
+    const int i = tid + u * NT;
+    ev[u] = 0;
+    lv[u] = -1;
+    if (i < n) {
+      ev[u] = __ldcg(ids + s0 + i);
+      if (token_adapter) lv[u] = __ldcg(token_adapter + (s0 + i) / k);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < PT; ++u) {
+    const int i = tid + u * NT;
+    if (i >= n) break;
+    const int e = ev[u], l = lv[u];
+    unsigned int bad = 0;
+    if (e < 0 || e >= E) bad |= MOE_LORA_DEVERR_EXPERT_RANGE;
+    if (l < -1 || l >= L) bad |= MOE_LORA_DEVERR_ADAPTER_RANGE;
+    int key = drop;
+    if (bad) atomicOr(&s_err, bad);
+    else key = e * (L + 1) + (l + 1);
+    bufA[i] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s0 + i);
+  }
+  __syncthreads();
+  const uint32_t* srt = block_radix_sort<NT>(bufA, bufB, n, slot_bits, key_bits, hist, tmp);
+  // rank within the key run: the run's first index by an inclusive max-scan of run heads
+  for (int i = tid; i < C; i += NT)
+    head[i] = (i < n && (i == 0 || (srt[i] >> slot_bits) != (srt[i - 1] >> slot_bits))) ? i : 0;
+  __syncthreads();
+  for (int off = 1; off < C; off <<= 1) {
+    int hv[PT];
+#pragma unroll
+    for (int u = 0; u < PT; ++u) {
+      const int i = tid + u * NT;
+      hv[u] = i >= off ? max(head[i], head[i - off]) : head[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < PT; ++u) head[tid + u * NT] = hv[u];
+    __syncthreads();
+  }
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t w = srt[i];
+    const int key = static_cast<int>(w >> slot_bits);
+    const int rank = i - head[i];
+    v.sort0[s0 + i] = w;
+    v.sort1[s0 + i] = static_cast<uint32_t>(rank);
+    if (i == n - 1 || (srt[i + 1] >> slot_bits) != static_cast<uint32_t>(key))
+      cnt_c[key] = rank + 1;  // the run's last word holds its length
+  }
+  if (tid == 0 && s_err) atomicOr(reinterpret_cast<unsigned int*>(v.hdr + HDR_ERR), s_err);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT)
+    align_scan_kernel(AlignView v, int T, int k, int E, int L, int bm_base, int bm_lora, int S,
+                      int nbuckets, int ctas) {
+  constexpr int NW = NT / 32;
+  __shared__ int tmp[NW + 1];
+  pdl_trigger();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  // 1. exclusive scan of the count table in (key, CTA) order, in place. The table is
+  //    stored CTA-major ([ctas][nbuckets]); a tile of NT keys is read one key per thread
+  //    (coalesced across threads for each CTA row), totalled per key, scanned across
+  //    the tile with the carry of the tiles before, and written back as offsets.
+  int carry = 0;
+  for (int b0 = 0; b0 < nbuckets; b0 += NT) {
+    const int b = b0 + tid;
+    int tot = 0;
+    if (b < nbuckets) {
+#pragma unroll 8
+      for (int c = 0; c < ctas; ++c) tot += __ldcg(v.counts + (size_t)c * nbuckets + b);
+    }
+    int tile_total;
+    int run = carry + block_exclusive_scan<NW>(tot, tmp, &tile_total);
+    if (b < nbuckets) {
+      v.bucket_start[b] = run;
+      v.bucket_count[b] = tot;
+      for (int c = 0; c < ctas; ++c) {
+        int* p = v.counts + (size_t)c * nbuckets + b;
+        const int cnt = __ldcg(p);
+        *p = run;
+        run += cnt;
+      }
+    }
+    carry += tile_total;
+  }
+  __syncthreads();
+  // 2. expert starts
+  for (int e = tid; e <= E; e += NT) v.expert_begin[e] = __ldcg(v.bucket_start + (size_t)e * (L + 1));
+  __syncthreads();
+  const int n_valid = __ldcg(v.bucket_start + nbuckets - 1);
+  // 3. token tiles: each expert's rows in chunks of bm_base, experts in order
+  const int pe = (E + NT - 1) / NT;
+  const int e0 = min(E, tid * pe), e1 = min(E, e0 + pe);
+  int nt = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int rows = __ldcg(v.expert_begin + e + 1) - __ldcg(v.expert_begin + e);
+    nt += (rows + bm_base - 1) / bm_base;
+  }
+  int tot_t;
+  int ti = block_exclusive_scan<NW>(nt, tmp, &tot_t);
+  for (int e = e0; e < e1; ++e) {
+    const int rb = __ldcg(v.expert_begin + e), rows = __ldcg(v.expert_begin + e + 1) - rb;
+    for (int j = 0; j * bm_base < rows; ++j)
+      v.tiles[ti++] = make_int4(e, rb + j * bm_base, min(bm_base, rows - j * bm_base), 0);
+  }
+  // 4. LoRA blocks: each (e, l >= 0) bucket's rows in chunks of bm_lora, buckets in order
+  const int pb = (nbuckets + NT - 1) / NT;
+  const int q0 = min(nbuckets, tid * pb), q1 = min(nbuckets, q0 + pb);
+  int nb = 0, nl = 0;
+  for (int b = q0; b < q1; ++b) {
+    if (b % (L + 1) == 0) continue;  // adapter -1 (and the dropped-slot bucket)
+    const int cnt = __ldcg(v.bucket_count + b);
+    nb += (cnt + bm_lora - 1) / bm_lora;
+    nl += cnt;
+  }
+  int tot_b, tot_l;
+  int bi = block_exclusive_scan<NW>(nb, tmp, &tot_b);
+  block_exclusive_scan<NW>(nl, tmp, &tot_l);
+  for (int b = q0; b < q1; ++b) {
+    if (b % (L + 1) == 0) continue;
+    const int e = b / (L + 1), l = b % (L + 1) - 1;
+    const int rb = __ldcg(v.bucket_start + b), cnt = __ldcg(v.bucket_count + b);
+    for (int j = 0; j * bm_lora < cnt; ++j)
+      v.blocks[bi++] = make_int4(rb + j * bm_lora, min(bm_lora, cnt - j * bm_lora), e, l);
+  }
+  if (tid == 0) {
+    v.hdr[HDR_NVALID] = n_valid;
+    v.hdr[HDR_NTILES] = tot_t;
+    v.hdr[HDR_NBLOCKS] = tot_b;
+    v.hdr[HDR_NLORAROWS] = tot_l;
+    v.hdr[HDR_T] = T;
+    v.hdr[HDR_K] = k;
+    v.hdr[HDR_E] = E;
+    v.hdr[HDR_L] = L;
+    v.hdr[HDR_BMB] = bm_base;
+    v.hdr[HDR_BML] = bm_lora;
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT)
+    align_place_kernel(AlignView v, int L, int S, int nbuckets, int slot_bits, int ctas) {
+  constexpr int C = kAlignChunk;
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x;
+  const int s0 = c * C, n = min(C, S - s0);
+  const int drop = nbuckets - 1;
+  const uint32_t smask = (slot_bits >= 32) ? 0xffffffffu : ((1u << slot_bits) - 1u);
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t w = __ldcg(v.sort0 + s0 + i);
+    const int rank = static_cast<int>(__ldcg(v.sort1 + s0 + i));
+    const int key = static_cast<int>(w >> slot_bits);
+    const int s = static_cast<int>(w & smask);
+    const int pos = __ldcg(v.counts + (size_t)c * nbuckets + key) + rank;
+    if (key == drop) {
+      v.sorted_slots[pos] = -1;
+      v.slot_row[s] = -1;
+    } else {
+      v.sorted_slots[pos] = s;
+      v.slot_row[s] = pos;
+      v.row_expert[pos] = key / (L + 1);
+      v.row_adapter[pos] = key % (L + 1) - 1;
+    }
+  }
+}
+
 template <int NT>
 static int launch_align_t(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
                           const AlignLayout& a, cudaStream_t stream, bool pdl) {
@@ -329,6 +551,17 @@ static int launch_align_t(const int* ids, const int* token_adapter, const moe_lo
 
 int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
                  const AlignLayout& a, cudaStream_t stream, bool pdl) {
+  if (a.ctas > 0) {  // many slots: spread the sort over a.ctas CTAs
+    AlignView v = align_view(al->buf, a);
+    int st = launch_pdl(align_local_kernel<256>, a.ctas, 256, 0, stream, pdl, ids, token_adapter,
+                        v, al->k, al->E, al->L, a.S, a.nbuckets, a.key_bits, a.slot_bits, a.ctas);
+    if (st != MOE_LORA_OK) return st;
+    st = launch_pdl(align_scan_kernel<1024>, 1, 1024, 0, stream, pdl, v, al->T, al->k, al->E,
+                    al->L, al->bm_base, al->bm_lora, a.S, a.nbuckets, a.ctas);
+    if (st != MOE_LORA_OK) return st;
+    return launch_pdl(align_place_kernel<256>, a.ctas, 256, 0, stream, pdl, v, al->L, a.S,
+                      a.nbuckets, a.slot_bits, a.ctas);
+  }
   // few slots: a small CTA keeps the many barriers of the sort cheap
   if (a.S <= 4096) return launch_align_t<256>(ids, token_adapter, al, a, stream, pdl);
   return launch_align_t<1024>(ids, token_adapter, al, a, stream, pdl);

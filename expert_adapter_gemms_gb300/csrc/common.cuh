@@ -58,9 +58,17 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 struct AlignLayout {
   int64_t off[MOE_LORA_ALIGN_NFIELDS];
   int S, max_tiles, max_blocks, nbuckets, key_bits, slot_bits;
-  int64_t off_bucket_count, off_bucket_start, off_sort0, off_sort1;
+  int64_t off_bucket_count, off_bucket_start, off_sort0, off_sort1, off_counts;
+  int ctas;  // CTAs of the multi-CTA align (kAlignChunk slots each); 0: one-CTA align
   bool valid;
 };
+
+// Multi-CTA align: from kAlignMultiMin slots on, with at most half as many buckets as
+// slots (else the (bucket, CTA) count table, not the sort, is the work) and the table
+// within kAlignMaxCounts entries.
+constexpr int kAlignChunk = 512;
+constexpr int kAlignMultiMin = 2048;
+constexpr int64_t kAlignMaxCounts = 1 << 22;
 
 // header word indices
 enum { HDR_ERR = 0, HDR_NVALID = 1, HDR_NTILES = 2, HDR_NBLOCKS = 3, HDR_NLORAROWS = 4,
@@ -110,6 +118,9 @@ inline AlignLayout align_layout(int T, int k, int E, int L, int bm_base, int bm_
   a.off_bucket_start = take(nb * 4);
   a.off_sort0 = take((int64_t)S * 4);
   a.off_sort1 = take((int64_t)S * 4);
+  const int64_t ctas = ((int64_t)S + kAlignChunk - 1) / kAlignChunk;
+  a.ctas = (S >= kAlignMultiMin && 2 * nb <= S && nb * ctas <= kAlignMaxCounts) ? (int)ctas : 0;
+  a.off_counts = take(a.ctas ? nb * ctas * 4 : 0);
   a.off[MOE_LORA_AF_TOTAL_BYTES] = o;
   a.valid = true;
   return a;
@@ -129,6 +140,7 @@ struct AlignView {
   int* bucket_start;
   uint32_t* sort0;
   uint32_t* sort1;
+  int* counts;  // [ctas][nbuckets] of the multi-CTA align
 };
 
 inline AlignView align_view(void* buf, const AlignLayout& a) {
@@ -146,6 +158,7 @@ inline AlignView align_view(void* buf, const AlignLayout& a) {
   v.bucket_start = reinterpret_cast<int*>(b + a.off_bucket_start);
   v.sort0 = reinterpret_cast<uint32_t*>(b + a.off_sort0);
   v.sort1 = reinterpret_cast<uint32_t*>(b + a.off_sort1);
+  v.counts = reinterpret_cast<int*>(b + a.off_counts);
   return v;
 }
 

@@ -140,3 +140,34 @@ def test_align_is_deterministic():
     torch.cuda.synchronize()
     n = a1.header()["n_valid"]
     assert torch.equal(a1.sorted_slots()[:n], a2.sorted_slots()[:n])
+
+
+def test_align_multi_cta_cases():
+    """From 2048 slots on, with at most half as many keys as slots, the align runs on many
+    CTAs (local stable sorts of 512 slots, a scan of the (key, CTA) count table,
+    placement): bit-exact with the oracle on a partial last CTA, keys needing two radix
+    digits, out-of-range ids and adapters, one pair holding every slot, and bm_lora that
+    does not divide the segments. Many keys over few slots stay on the one-CTA kernel."""
+    m = need_gpu()
+    rng = np.random.default_rng(11)
+    # partial last CTA (S = 2050), adapters -1..3
+    ids = np.stack([rng.permutation(8)[:2] for _ in range(1025)])
+    _check_align(m, ids, rng.integers(-1, 4, size=1025), 8, 4, 16, 5)
+    # two radix digits: E * (L + 1) + 1 = 1025 keys, S = 3000
+    ids = rng.integers(0, 64, size=(1500, 2))
+    _check_align(m, ids, rng.integers(-1, 15, size=1500), 64, 15, 32, 3)
+    # many keys over few slots (65537 keys, S = 3000): the one-CTA kernel
+    ids = rng.integers(0, 256, size=(1500, 2))
+    _check_align(m, ids, rng.integers(-1, 255, size=1500), 256, 255, 32, 3)
+    # out-of-range expert ids and adapters: slots dropped, bits set
+    ids = rng.integers(0, 12, size=(700, 4))
+    ids[rng.random(ids.shape) < 0.05] = 99
+    ids[3, 1] = -2
+    ad = rng.integers(-1, 6, size=700)
+    ad[[5, 77]] = [6, -3]
+    al = _check_align(m, ids, ad, 12, 6, 64, 16)
+    assert m.get_error(al.buf) == 3
+    # every slot in one (expert, adapter) pair: one long run across all CTAs
+    _check_align(m, np.full((2048, 2), 1), np.full(2048, 0), 4, 2, 256, 16)
+    # exactly four full CTAs, no adapters
+    _check_align(m, rng.integers(0, 32, size=(512, 4)), None, 32, 0, 128, 16)
