@@ -34,6 +34,10 @@ Readings where the pages are silent (each also listed in the design notes):
 * A slot whose expert id or whose token's adapter id is out of range is
   dropped (contributes nothing) and flagged in an error word.
 * Intermediates are kept in fp64 with no rounding.
+* Separate gate and up adapters (the pages describe one LoRA per projection and
+  are silent on a gate_up projection split in two): A1 [L, E, 2r, H] stacks the
+  gate and the up A, B1 [L, E, 2I, r] keeps gate rows first, and each half of
+  the gate_up output takes its own z.
 """
 from __future__ import annotations
 
@@ -235,19 +239,30 @@ def lora_shrink(X, A, al: dict, rows_are_slots: bool) -> np.ndarray:
     return Z
 
 
-def lora_delta_rows(Z, B, al: dict) -> np.ndarray:
-    """Expand z B for each sorted row with an adapter; [n_valid, N], zero elsewhere."""
+def lora_delta_rows(Z, B, al: dict, slices: int = 1) -> np.ndarray:
+    """Expand z B for each sorted row with an adapter; [n_valid, N], zero elsewhere.
+
+    slices = 2 (separate gate and up adapters): z rows hold 2r values; output
+    columns [0, N/2) take the first r with B rows [0, N/2), columns [N/2, N) the
+    last r with B rows [N/2, N).
+    """
     Zf = as_f64(Z)
     Bf = as_f64(B)
     n = al["n_valid"]
-    D = np.zeros((n, Bf.shape[2]))
+    N = Bf.shape[2]
+    r = Bf.shape[3]
+    D = np.zeros((n, N))
     for row in range(n):
         l = int(al["row_adapter"][row])
         if l < 0:
             continue
         e = int(al["row_expert"][row])
         s = int(al["sorted_slots"][row])
-        D[row] = Bf[l, e] @ Zf[s]
+        if slices == 1:
+            D[row] = Bf[l, e] @ Zf[s]
+        else:
+            D[row, : N // 2] = Bf[l, e, : N // 2] @ Zf[s, :r]
+            D[row, N // 2:] = Bf[l, e, N // 2:] @ Zf[s, r: 2 * r]
     return D
 
 
@@ -271,15 +286,17 @@ def lora_expand_add(Z, B, al: dict, base_rows, epilogue: int, w=None) -> np.ndar
     epilogue 0: base + zB                      [n_valid, N]
     epilogue 1: swiglu(base + zB)              [n_valid, N/2]
     epilogue 2: combine(base + zB, w)          [T, N]
+    epilogue 3: as 1 with separate gate and up adapters (two z slices; see
+                lora_delta_rows)              [n_valid, N/2]
     """
-    G = as_f64(base_rows) + lora_delta_rows(Z, B, al)
+    G = as_f64(base_rows) + lora_delta_rows(Z, B, al, slices=2 if epilogue == 3 else 1)
     if epilogue == 0:
         return G
-    if epilogue == 1:
+    if epilogue in (1, 3):
         return swiglu(G)
     if epilogue == 2:
         return combine(G, w, al)
-    raise ValueError("epilogue must be 0, 1 or 2")
+    raise ValueError("epilogue must be 0, 1, 2 or 3")
 
 
 # ----------------------------------------------------------------------------
@@ -292,13 +309,16 @@ def _slots_ok(ids, ad, E, L):
 
 
 def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=None,
-                   B2=None) -> np.ndarray:
+                   B2=None, gate_up_slices: int = 1) -> np.ndarray:
     """y[t] = sum_j w[t,j] * expert_{ids[t,j]}(x[t]) with the token's adapter.
 
     expert_e with adapter l (l = -1: none):
       g = x W1_e^T + (x A1_{l,e}^T) B1_{l,e}^T        gate_up with LoRA
       h = silu(g[:I]) * g[I:]                          SwiGLU
       o = h W2_e^T + (h A2_{l,e}^T) B2_{l,e}^T         down with LoRA
+    gate_up_slices = 2: the gate and up projections carry separate adapters,
+    A1 [L, E, 2r, H] (rows [0, r) gate, [r, 2r) up), B1 [L, E, 2I, r]:
+      g[:I] += (x A1_{l,e}[:r]^T) B1_{l,e}[:I]^T,  g[I:] += (x A1_{l,e}[r:]^T) B1_{l,e}[I:]^T
     Slots that share (e, l) are stacked into one matrix product per group; the
     arithmetic per slot is unchanged. Weights may be torch tensors or fp64
     numpy arrays (the latter skip the per-call conversion).
@@ -330,8 +350,13 @@ def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=N
         ts, js = tt[sel], jj[sel]
         Xg = X[ts]
         g = Xg @ W1e.T
-        if l >= 0:
+        if l >= 0 and gate_up_slices == 1:
             g = g + (Xg @ as_f64(A1[l, e]).T) @ as_f64(B1[l, e]).T
+        elif l >= 0:
+            A1le, B1le = as_f64(A1[l, e]), as_f64(B1[l, e])
+            r1, I1 = A1le.shape[0] // 2, B1le.shape[0] // 2
+            g[:, :I1] += (Xg @ A1le[:r1].T) @ B1le[:I1].T
+            g[:, I1:] += (Xg @ A1le[r1:].T) @ B1le[I1:].T
         h = swiglu(g)
         o = h @ W2e.T
         if l >= 0:

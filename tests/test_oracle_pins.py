@@ -29,6 +29,22 @@ def _rel(a, b):
 # ----------------------------------------------------------------------------
 # pin functions (raise AssertionError when the oracle is wrong)
 # ----------------------------------------------------------------------------
+def _two_slice_weights(inp, seed):
+    """Separate gate and up adapters for a workload, and the same map written as one
+    adapter of rank 2r: A stacked, B block-diagonal (gate rows [B_g | 0], up rows
+    [0 | B_u])."""
+    rng = np.random.default_rng(seed)
+    L, E, r, H = inp.A1.shape
+    I2 = inp.B1.shape[2]
+    A1s = torch.from_numpy(rng.standard_normal((L, E, 2 * r, H)) * 0.1)
+    B1 = torch.from_numpy(rng.standard_normal((L, E, I2, r)) * 0.1)
+    B1bd = torch.zeros((L, E, I2, 2 * r), dtype=torch.float64)
+    B1bd[:, :, : I2 // 2, :r] = B1[:, :, : I2 // 2]
+    B1bd[:, :, I2 // 2:, r:] = B1[:, :, I2 // 2:]
+    return A1s, B1, B1bd
+
+
+
 def pin_route_golden(golden_dir):
     with open(os.path.join(golden_dir, "route_cases.json")) as f:
         cases = json.load(f)["cases"]
@@ -313,6 +329,55 @@ def test_layer_scalar_vs_vectorised_random(seed):
                             L=int(rng.integers(0, 3)), r=int(rng.integers(1, 5)),
                             seed=200 + seed, lora_std=None)
     pin_layer_scalar_vs_vectorised(inp)
+
+
+def pin_two_slice_gate_up(inp, seed):
+    """Separate gate and up adapters equal one adapter of twice the rank with a stacked A
+    and a block-diagonal B: the layer and the epilogue-3 expand against the (pinned)
+    one-slice forms."""
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    A1s, B1, B1bd = _two_slice_weights(inp, seed)
+    y2 = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, A1s, B1,
+                               inp.A2, inp.B2, gate_up_slices=2)
+    y1 = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, A1s, B1bd,
+                               inp.A2, inp.B2)
+    assert _rel(y2, y1) < 1e-12, _rel(y2, y1)
+    al = oracle.align(torch.as_tensor(ids, dtype=torch.int32), inp.token_adapter, inp.E, inp.L, 16, 4)
+    Z = oracle.lora_shrink(inp.x, A1s, al, rows_are_slots=False)
+    G = np.random.default_rng(seed + 1).standard_normal((al["n_valid"], B1.shape[2]))
+    h3 = oracle.lora_expand_add(Z, B1, al, G, epilogue=3)
+    h1 = oracle.lora_expand_add(Z, B1bd, al, G, epilogue=1)
+    assert _rel(h3, h1) < 1e-12, _rel(h3, h1)
+    # a zero up adapter leaves the up half to the base output
+    B1g = B1.clone()
+    B1g[:, :, B1.shape[2] // 2:] = 0
+    D = om.lora_delta_rows(Z, B1g, al, slices=2)
+    assert np.all(D[:, B1.shape[2] // 2:] == 0)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_two_slice_gate_up(seed):
+    pin_two_slice_gate_up(make_layer_inputs(T=13, H=24, I=10, E=3, k=2, L=3, r=3,
+                                            seed=400 + seed, adapters="uniform_with_none"), 500 + seed)
+
+
+def test_planted_two_slice_swap(monkeypatch):
+    """Feeding the up z to the gate columns (and the gate z to the up columns) trips the pin."""
+    real = om.lora_delta_rows
+
+    def swapped(Z, B, al, slices=1):
+        if slices == 1:
+            return real(Z, B, al, 1)
+        Zf = np.array(om.as_f64(Z))
+        r = om.as_f64(B).shape[3]
+        Zs = Zf.copy()
+        Zs[:, :r], Zs[:, r: 2 * r] = Zf[:, r: 2 * r], Zf[:, :r]
+        return real(Zs, B, al, 2)
+
+    monkeypatch.setattr(om, "lora_delta_rows", swapped)
+    with pytest.raises(AssertionError):
+        pin_two_slice_gate_up(make_layer_inputs(T=13, H=24, I=10, E=3, k=2, L=3, r=3, seed=400,
+                                                adapters="uniform_with_none"), 500)
 
 
 def test_dense_swiglu_mlp():
