@@ -45,7 +45,7 @@ class AlignDesc(ctypes.Structure):
 class LayerOpts(ctypes.Structure):
     _fields_ = [("bm_base", ctypes.c_int32), ("bm_lora", ctypes.c_int32),
                 ("disable_pdl", ctypes.c_int32), ("num_events", ctypes.c_int32),
-                ("events", ctypes.POINTER(ctypes.c_void_p))]
+                ("events", ctypes.POINTER(ctypes.c_void_p)), ("gate_up_slices", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p

@@ -188,7 +188,8 @@ def lora_shrink(X: torch.Tensor, rows_are_slots: bool, A: torch.Tensor, al: Alig
 def lora_expand_add(Z: torch.Tensor, B: Optional[torch.Tensor], al: Align, epilogue: int,
                     base: torch.Tensor, out: Optional[torch.Tensor] = None, out_fp32: bool = False,
                     topk_w: Optional[torch.Tensor] = None, N: Optional[int] = None):
-    """Expand with the base add fused; epilogue 0 (in place), 1 (SwiGLU), 2 (combine)."""
+    """Expand with the base add fused; epilogue 0 (in place), 1 (SwiGLU), 2 (combine),
+    3 (SwiGLU with separate gate and up adapters: Z rows hold 2r values)."""
     _need(base, "base", torch.float32, 2)
     Nb = base.shape[1]
     r = 0
@@ -197,9 +198,9 @@ def lora_expand_add(Z: torch.Tensor, B: Optional[torch.Tensor], al: Align, epilo
         r = B.shape[3]
         if B.shape[2] != Nb or B.shape[1] != al.E or B.shape[0] != al.L:
             raise ValueError("shape mismatch between B, base and the align buffer")
-        _need(Z, "Z", torch.float32, 2, (al.S, r))
+        _need(Z, "Z", torch.float32, 2, (al.S, 2 * r if epilogue == 3 else r))
     dev = base.device
-    if epilogue == 1 and out is None:
+    if epilogue in (1, 3) and out is None:
         out = torch.zeros((al.S, Nb // 2), dtype=torch.bfloat16, device=dev)
     if epilogue == 2 and out is None:
         out = torch.zeros((al.T, Nb), dtype=torch.float32 if out_fp32 else torch.bfloat16,
@@ -241,8 +242,9 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
                    A1=None, B1=None, A2=None, B2=None, y: Optional[torch.Tensor] = None,
                    y_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
                    bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
-                   events: Optional[Sequence] = None) -> torch.Tensor:
-    """The whole fused MoE-LoRA layer; returns y [T, H]."""
+                   events: Optional[Sequence] = None, gate_up_slices: int = 1) -> torch.Tensor:
+    """The whole fused MoE-LoRA layer; returns y [T, H]. gate_up_slices=2: separate gate
+    and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r]."""
     _need(x, "x", torch.bfloat16, 2)
     _need(W1, "W1", torch.bfloat16, 3)
     _need(W2, "W2", torch.bfloat16, 3)
@@ -260,9 +262,14 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
         k = topk_ids.shape[1]
         _need(topk_w, "topk_w", torch.float32, 2, (T, k))
     Ln, r = 0, 0
+    if gate_up_slices not in (1, 2):
+        raise ValueError("gate_up_slices must be 1 or 2")
     if A1 is not None:
         _need(A1, "A1", torch.bfloat16, 4)
         Ln, _, r, _ = A1.shape
+        if r % gate_up_slices:
+            raise ValueError("A1 rows must hold gate_up_slices adapters of equal rank")
+        r //= gate_up_slices
         _need(B1, "B1", torch.bfloat16, 4, (Ln, E, twoI, r))
         _need(A2, "A2", torch.bfloat16, 4, (Ln, E, r, I))
         _need(B2, "B2", torch.bfloat16, 4, (Ln, E, H, r))
@@ -276,6 +283,7 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
         workspace = new_workspace(T, k, E, Ln, H, I, r, x.device)
     opts = LayerOpts()
     opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
+    opts.gate_up_slices = gate_up_slices
     ev_arr = None
     if events:
         ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])

@@ -101,7 +101,7 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r, int
   p.off_w = take(S * 4);
   p.off_xs = take(S * H * 2);
   p.off_G = take(S * 2 * (int64_t)I * 4);
-  p.off_Z1 = take(S * rr * 4);
+  p.off_Z1 = take(S * 2 * rr * 4);  // two z slices with separate gate and up adapters
   p.off_h = take(S * (int64_t)I * 2);
   p.off_Z2 = take(S * rr * 4);
   p.off_O = take(S * (int64_t)H * 4);
@@ -184,6 +184,8 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   moe_lora_layer_opts o = {};
   if (opts) o = *opts;
   if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return MOE_LORA_ERR_INVALID_ARG;
+  const int slices = o.gate_up_slices == 0 ? 1 : o.gate_up_slices;
+  if (slices != 1 && slices != 2) return MOE_LORA_ERR_INVALID_ARG;
   LayerPlan p = plan_layer(T, k, E, L, H, I, r, o.bm_base, o.bm_lora);
   if (!p.valid) return MOE_LORA_ERR_UNSUPPORTED;
   if (T == 0) return MOE_LORA_OK;
@@ -245,13 +247,14 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   // Short LoRA blocks (decode-like) read the gathered rows: addressed by sorted row, they
   // need no slot lookup before the load (and are recent in L2).
   if (L > 0) {
+    // with separate gate and up adapters the gate_up shrink is one of rank 2r
     if (p.bm_lora <= 8)
-      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, Z1, stream, pdl, pdl));
     else
-      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, Z1, stream, pdl, pdl));
   }
   ML_STEP(mark(5));
-  ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, 1, G, h, 0,
+  ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, L > 0 && slices == 2 ? 3 : 1, G, h, 0,
                              nullptr, stream, pdl, pdl && L > 0));
   ML_STEP(mark(6));
   ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, 0));

@@ -148,8 +148,11 @@ __global__ void __launch_bounds__(kExpandThreads)
                          const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
                          const int* __restrict__ row_expert, const int* __restrict__ row_adapter,
                          int I, int r, int E, const float* __restrict__ G,
-                         __nv_bfloat16* __restrict__ h, int rows_per_cta, int early) {
-  extern __shared__ float zs[];  // [rows_per_cta][r]
+                         __nv_bfloat16* __restrict__ h, int rows_per_cta, int early,
+                         int zstride, int zu_off) {
+  // z rows: zstride floats (r, or 2r with separate gate and up adapters); the gate
+  // columns take z[0, r), the up columns z[zu_off, zu_off + r)
+  extern __shared__ float zs[];  // [rows_per_cta][zstride]
   __shared__ int s_key[64];      // e * 65536 + (l + 1), or -1 without adapter
   __shared__ int s_slot[64];
   if (!early) pdl_wait();
@@ -207,9 +210,9 @@ __global__ void __launch_bounds__(kExpandThreads)
   pdl_trigger();
   if (!early) load_g(0);
   if (B) {
-    for (int i = threadIdx.x; i < rows * r; i += blockDim.x) {
-      const int m = i / r, c = i - m * r;
-      zs[i] = s_key[m] >= 0 ? __ldcg(Z + (size_t)s_slot[m] * r + c) : 0.f;
+    for (int i = threadIdx.x; i < rows * zstride; i += blockDim.x) {
+      const int m = i / zstride, c = i - m * zstride;
+      zs[i] = s_key[m] >= 0 ? __ldcg(Z + (size_t)s_slot[m] * zstride + c) : 0.f;
     }
   }
   __syncthreads();
@@ -230,14 +233,14 @@ __global__ void __launch_bounds__(kExpandThreads)
           }
 #pragma unroll
           for (int i = 0; i < RV; ++i) {
-            fma8(g, zs + m * r + 8 * i, bg[i]);
-            fma8(u, zs + m * r + 8 * i, bu[i]);
+            fma8(g, zs + m * zstride + 8 * i, bg[i]);
+            fma8(u, zs + m * zstride + zu_off + 8 * i, bu[i]);
           }
         } else {
           const int e = key >> 16, l = (key & 0xffff) - 1;
           const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
-          g += dot_zb_mem<false>(zs + m * r, bl + (size_t)n * r, r);
-          u += dot_zb_mem<false>(zs + m * r, bl + (size_t)(I + n) * r, r);
+          g += dot_zb_mem<false>(zs + m * zstride, bl + (size_t)n * r, r);
+          u += dot_zb_mem<false>(zs + m * zstride + zu_off, bl + (size_t)(I + n) * r, r);
         }
       }
       h[(size_t)(r0 + m) * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
@@ -344,18 +347,18 @@ __global__ void __launch_bounds__(kExpandThreads)
 // barrier for another thread's table reads; the one barrier stages z (r floats)
 // after the B rows are in flight.
 // ----------------------------------------------------------------------------
-template <int RV>
+template <int RV, bool kTwo>  // kTwo: separate gate and up adapters (two z slices)
 __global__ void __launch_bounds__(kExpandThreads)
     expand_swiglu_row1_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                               const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
                               const int* __restrict__ row_expert,
                               const int* __restrict__ row_adapter, int I, int r, int E,
                               const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
-                              int early) {
-  __shared__ __align__(16) float zs[8 * RV];
+                              int early, int zstride, int zu_off) {
   if (!early) pdl_wait();
   const int row = blockIdx.x;
   const int n = blockIdx.y * kExpandThreads + threadIdx.x;
+  const int lane = threadIdx.x & 31;
   const bool col = n < I;
   const size_t twoI = 2 * (size_t)I;
   // rows past n_valid exist (the tables and G have S rows); their values are unused
@@ -371,6 +374,8 @@ __global__ void __launch_bounds__(kExpandThreads)
   const bool active = row < n_valid;
   const bool lora = active && l >= 0;  // uniform over the CTA
   uint4 bg[RV], bu[RV];
+#pragma unroll
+  for (int i = 0; i < RV; ++i) bg[i] = bu[i] = make_uint4(0, 0, 0, 0);
   if (lora && col) {
     const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
     const uint4* pg = reinterpret_cast<const uint4*>(bl + (size_t)n * r);
@@ -385,15 +390,29 @@ __global__ void __launch_bounds__(kExpandThreads)
   pdl_trigger();
   if (!active) return;
   if (lora) {
-    if (threadIdx.x < 2 * RV)
-      reinterpret_cast<float4*>(zs)[threadIdx.x] =
-          __ldcg(reinterpret_cast<const float4*>(Z + (size_t)slot * r) + threadIdx.x);
-    __syncthreads();
-    if (!col) return;
+    // z (r = 8 RV floats) is read once per warp, one or two values per lane, and
+    // broadcast with shuffles: no shared-memory staging, no barrier
+    // (the up columns' z sits zu_off floats further when gate and up have separate adapters)
+    constexpr int ZL = RV > 4 ? 2 : 1;
+    float zl[ZL], zul[ZL];
+    const float* zrow = Z + (size_t)slot * zstride;
+#pragma unroll
+    for (int j = 0; j < ZL; ++j) {
+      const int i = lane + 32 * j;
+      zl[j] = i < 8 * RV ? __ldcg(zrow + i) : 0.f;
+      zul[j] = kTwo && i < 8 * RV ? __ldcg(zrow + zu_off + i) : 0.f;
+    }
+    // every lane takes part in the shuffles (lanes past the last column included)
 #pragma unroll
     for (int i = 0; i < RV; ++i) {
-      fma8(g, zs + 8 * i, bg[i]);
-      fma8(u, zs + 8 * i, bu[i]);
+      float zv[8], zw[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        zv[c] = __shfl_sync(0xffffffffu, zl[(8 * i + c) >> 5], (8 * i + c) & 31);
+        zw[c] = kTwo ? __shfl_sync(0xffffffffu, zul[(8 * i + c) >> 5], (8 * i + c) & 31) : zv[c];
+      }
+      fma8(g, zv, bg[i]);
+      fma8(u, zw, bu[i]);
     }
   }
   if (col) h[(size_t)row * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
@@ -426,11 +445,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 // bf16 remainders [16][r_pad]; rows >= rows and ranks >= r are zero.
 __device__ __forceinline__ void stage_z_split(__nv_bfloat16* zb, const float* __restrict__ Z,
                                               const int* __restrict__ sorted_slots, int row0,
-                                              int rows, int r, int r_pad) {
+                                              int rows, int r, int r_pad, int zstride = -1,
+                                              int zoff = 0) {
+  if (zstride < 0) zstride = r;  // z rows of zstride floats; this slice starts at zoff
   for (int i = threadIdx.x; i < 16 * r_pad; i += blockDim.x) {
     const int m = i / r_pad, c = i - m * r_pad;
     float v = 0.f;
-    if (m < rows && c < r) v = __ldcg(Z + (size_t)__ldcg(sorted_slots + row0 + m) * r + c);
+    if (m < rows && c < r) v = __ldcg(Z + (size_t)__ldcg(sorted_slots + row0 + m) * zstride + zoff + c);
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
     zb[i] = hi;
     zb[16 * r_pad + i] = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -478,14 +499,14 @@ __device__ __forceinline__ void block_mma(float (&acc)[4], const ZFrag<KC>& z, c
 // epilogue 1 with tensor cores. CTAs [0, max_blocks): one LoRA block each, all
 // columns; CTAs beyond: (token tile, 512-column chunk) pairs applying the plain
 // SwiGLU to the tile's rows without adapter.
-template <int KC>
+template <int KC, bool kTwo>  // kTwo: separate gate and up adapters (two z slices)
 __global__ void __launch_bounds__(kExpandThreads)
     expand_swiglu_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                              const int* __restrict__ hdr, const int4* __restrict__ blocks,
                              const int4* __restrict__ tiles, const int* __restrict__ sorted_slots,
                              const int* __restrict__ row_adapter, int I, int r, int E,
                              const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
-                             int max_blocks, int col_chunks, int early) {
+                             int max_blocks, int col_chunks, int early, int zstride, int zu_off) {
   constexpr int kWarps = kExpandThreads / 32;
   constexpr int kChunk = 2 * kExpandThreads;  // columns per plain-SwiGLU CTA
   __shared__ int s_flag[256];
@@ -525,7 +546,8 @@ __global__ void __launch_bounds__(kExpandThreads)
         bu[c] = b_frag(nl < I ? bl + (size_t)(I + nl) * r : nullptr, c, r);
       }
     };
-    float* gring = reinterpret_cast<float*>(smem_raw + zsmem_bytes(KC)) + warp * (kGStages * 256);
+    // shared memory: z of the gate columns, z of the up columns, then the G ring
+    float* gring = reinterpret_cast<float*>(smem_raw + 2 * zsmem_bytes(KC)) + warp * (kGStages * 256);
     auto fetch_g = [&](int t, int stage) {
       if (t < ntiles) {
         const int m = lane >> 1, c4 = (lane & 1) * 4;
@@ -544,10 +566,14 @@ __global__ void __launch_bounds__(kExpandThreads)
     if (t < ntiles) fetch_b(t);
     if (early) pdl_wait();
     pdl_trigger();
-    stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
+    __nv_bfloat16* zbu = zb + zsmem_bytes(KC) / sizeof(__nv_bfloat16);
+    stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad, zstride, 0);
+    if (kTwo) stage_z_split(zbu, Z, sorted_slots, row0, rows, r, r_pad, zstride, zu_off);
     __syncthreads();
-    ZFrag<KC> z;
+    ZFrag<KC> z, z2;
     z.load(zb, r_pad);
+    if (kTwo) z2.load(zbu, r_pad);
+    const ZFrag<KC>& zu = kTwo ? z2 : z;
     for (int j = 0; t < ntiles; t += kWarps, ++j) {
       fetch_g(t + (kGStages - 1) * kWarps, (j + kGStages - 1) % kGStages);
       cp_async_wait<kGStages - 1>();  // this tile's copies have landed
@@ -561,7 +587,7 @@ __global__ void __launch_bounds__(kExpandThreads)
       if (t + kWarps < ntiles) fetch_b(t + kWarps);  // next tile's B in flight
       float dg[4], du[4];
       block_mma<KC>(dg, z, tg);
-      block_mma<KC>(du, z, tu);
+      block_mma<KC>(du, zu, tu);
       const int n = t * 8 + 2 * q;
       const float* gs = gring + (j % kGStages) * 256;
       if (n < I) {
@@ -775,10 +801,14 @@ static int reg_ranks(int r, const void* B) {
 }
 
 int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al,
-                       const AlignLayout& a, int N, int r, int epilogue, float* base, void* out,
+                       const AlignLayout& a, int N, int r, int epilogue_in, float* base, void* out,
                        int out_fp32, const float* topk_w, cudaStream_t stream, bool pdl,
                        bool early) {
   if (a.S == 0) return MOE_LORA_OK;
+  // epilogue 3 is epilogue 1 with separate gate and up adapters: z rows of 2r floats,
+  // the up columns taking the second r
+  const int epilogue = epilogue_in == 3 ? 1 : epilogue_in;
+  const int zstride = epilogue_in == 3 ? 2 * r : r, zu_off = epilogue_in == 3 ? r : 0;
   AlignView v = align_view(al->buf, a);
   const auto* Bp = (al->L > 0) ? static_cast<const __nv_bfloat16*>(B) : nullptr;
   const int rv = Bp ? reg_ranks(r, B) : 1;
@@ -825,29 +855,40 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     const int I = N / 2;
     const int cc = chunks_for(I);
     const dim3 grid(a.max_blocks * cc + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
-    const size_t smem1 = Bp ? zsmem + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float) : 0;
+    const size_t smem1 = Bp ? 2 * zsmem + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float) : 0;
+    static int configured[64] = {0};  // every instance at once, once per device
+    int dev = 0;
+    ML_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 64 && !configured[dev]) {
+      const int lim = (int)(2 * zsmem_bytes(8) + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float));
+      const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<1, false>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<2, false>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<4, false>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<8, false>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<1, true>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<2, true>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<4, true>, attr, lim));
+      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<8, true>, attr, lim));
+      configured[dev] = 1;
+    }
     auto go = [&](auto kern) -> int {
-      static int configured[64][4] = {};
-      int dev = 0;
-      ML_CHECK_CUDA(cudaGetDevice(&dev));
-      const int slot = kcp == 1 ? 0 : kcp == 2 ? 1 : kcp == 4 ? 2 : 3;
-      if (dev < 64 && !configured[dev][slot]) {
-        ML_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(zsmem_bytes(8) + (size_t)(kExpandThreads / 32) *
-                                                 kGStages * 256 * sizeof(float))));
-        configured[dev][slot] = 1;
-      }
       return launch_pdl(kern, grid, kExpandThreads, smem1, stream, pdl, Z, Bp,
                         (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
                         (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
                         (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, cc,
-                        ea);
+                        ea, Bp ? zstride : 0, Bp ? zu_off : 0);
     };
-    switch (Bp ? kcp : 1) {
-      case 1: return go(expand_swiglu_mma_kernel<1>);
-      case 2: return go(expand_swiglu_mma_kernel<2>);
-      case 4: return go(expand_swiglu_mma_kernel<4>);
-      default: return go(expand_swiglu_mma_kernel<8>);
+    const bool two = Bp && zu_off != 0;
+    switch ((Bp ? kcp : 1) * 2 + (two ? 1 : 0)) {
+      case 2: return go(expand_swiglu_mma_kernel<1, false>);
+      case 3: return go(expand_swiglu_mma_kernel<1, true>);
+      case 4: return go(expand_swiglu_mma_kernel<2, false>);
+      case 5: return go(expand_swiglu_mma_kernel<2, true>);
+      case 8: return go(expand_swiglu_mma_kernel<4, false>);
+      case 9: return go(expand_swiglu_mma_kernel<4, true>);
+      case 16: return go(expand_swiglu_mma_kernel<8, false>);
+      default: return go(expand_swiglu_mma_kernel<8, true>);
     }
   }
   if (epilogue == 0) {
@@ -873,21 +914,27 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
       auto go = [&](auto kern) {
         return launch_pdl(kern, g1, kExpandThreads, 0, stream, pdl, Z, Bp, (const int*)v.hdr,
                           (const int*)v.sorted_slots, (const int*)v.row_expert,
-                          (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp, ea);
+                          (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp, ea,
+                          zstride, zu_off);
       };
-      switch (rv) {
-        case 1: return go(expand_swiglu_row1_kernel<1>);
-        case 2: return go(expand_swiglu_row1_kernel<2>);
-        case 4: return go(expand_swiglu_row1_kernel<4>);
-        default: return go(expand_swiglu_row1_kernel<8>);
+      switch (rv * 2 + (zu_off != 0 ? 1 : 0)) {
+        case 2: return go(expand_swiglu_row1_kernel<1, false>);
+        case 3: return go(expand_swiglu_row1_kernel<1, true>);
+        case 4: return go(expand_swiglu_row1_kernel<2, false>);
+        case 5: return go(expand_swiglu_row1_kernel<2, true>);
+        case 8: return go(expand_swiglu_row1_kernel<4, false>);
+        case 9: return go(expand_swiglu_row1_kernel<4, true>);
+        case 16: return go(expand_swiglu_row1_kernel<8, false>);
+        default: return go(expand_swiglu_row1_kernel<8, true>);
       }
     }
     const dim3 grid(ceil_div(a.S, rpc), ncol);
-    const size_t smem = (size_t)rpc * rr * sizeof(float);
+    const int zs_rows = Bp ? zstride : 0;
+    const size_t smem = (size_t)rpc * zs_rows * sizeof(float);
     return launch_rv<SwigluK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
                               (const int*)v.sorted_slots, (const int*)v.row_expert,
                               (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp,
-                              rpc, ea);
+                              rpc, ea, zs_rows, Bp ? zu_off : 0);
   }
   if (epilogue == 2 && Bp && (int64_t)a.S >= 2 * (int64_t)al->E * al->L) {
     // several rows per (expert, adapter) pair: apply each B row once per LoRA block
@@ -966,10 +1013,10 @@ extern "C" int lora_expand_add(const float* Z, const void* B, const moe_lora_ali
   AlignLayout a;
   int st = check_align(al, &a);
   if (st != MOE_LORA_OK) return st;
-  if (N < 1 || epilogue < 0 || epilogue > 2) return MOE_LORA_ERR_INVALID_ARG;
+  if (N < 1 || epilogue < 0 || epilogue > 3) return MOE_LORA_ERR_INVALID_ARG;
   if (al->L > 0 && (r < 1 || r > 256)) return r < 1 ? MOE_LORA_ERR_INVALID_ARG : MOE_LORA_ERR_UNSUPPORTED;
   if (al->L >= 65535 || al->E >= 32768) return MOE_LORA_ERR_UNSUPPORTED;  // packed (e, l) keys
-  if (epilogue == 1 && N % 2 != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if ((epilogue == 1 || epilogue == 3) && N % 2 != 0) return MOE_LORA_ERR_INVALID_ARG;
   if (a.S > 0) {
     if (!base) return MOE_LORA_ERR_INVALID_ARG;
     if (al->L > 0 && (!Z || !B)) return MOE_LORA_ERR_INVALID_ARG;

@@ -15,6 +15,8 @@
 // keeping every load 16 bytes wide. Masks on K are compiled out when
 // K % 32 == 0 (the EVEN_K specialisation); K % 8 != 0 or unaligned bases fall
 // back to element loads.
+#include <algorithm>
+
 #include "internal.h"
 
 namespace moe_lora {
@@ -177,6 +179,119 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
   }
 }
 
+// ----------------------------------------------------------------------------
+// Short K, short blocks, all ranks of a block in one CTA (the many-adapter shape's
+// down shrink: K = 768, r = 32, thousands of blocks of one or two rows). Register
+// loads cap the bytes a CTA keeps in flight and, at 124 registers, the CTAs per SM;
+// here the block's A slab (8 NT rows x K) lands in shared memory through 16-byte
+// asynchronous copies, only the activation fragments sit in registers, and four
+// CTAs fit an SM. The same mma.sync products and fixed-order warp reduction (done in
+// the slab's space once the products are formed) as the kernel above.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void shrink_cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+constexpr int kShortUMax = 4;  // k-steps per warp: K <= 8 warps x 4 x 32 = 1024
+
+// bytes per shared-memory row of A: at least K bf16, == 64 (mod 128) so that the rows
+// of a fragment load fall in alternate bank halves
+inline int short_astride(int K) { return (K * 2 + 127) / 128 * 128 + 64; }
+
+template <int NT, bool kEvenK>
+__global__ void __launch_bounds__(kShrinkWarps * 32, 4)
+    lora_shrink_smem_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
+                            const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
+                            const int4* __restrict__ blocks, const int* __restrict__ sorted_slots,
+                            int k, int K, int r, int E, float* __restrict__ Z, int ngroups,
+                            int early, int astride) {
+  constexpr int R = 8 * NT;
+  extern __shared__ __align__(16) uint8_t sA[];  // [R][astride] bytes; reused for the reduction
+  if (!early) pdl_wait();
+  const int b = blockIdx.x / ngroups;
+  const int g = blockIdx.x - b * ngroups;
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
+  const int4 blk = __ldcg(blocks + b);  // in bounds: the grid covers the host's block bound
+  if (b >= nb) {
+    if (early) pdl_wait();
+    return;
+  }
+  if (!early) pdl_trigger();
+  const int row0 = blk.x, rows = min(blk.y, 8), e = blk.z, l = blk.w;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, q = lane & 3;
+  const int slot0 = (int)threadIdx.x < rows * R ? __ldcg(sorted_slots + row0 + threadIdx.x / R) : 0;
+  // the slab: rank rows g R .. g R + nr - 1, 16 bytes per copy
+  const int nr = min(R, r - g * R);
+  const __nv_bfloat16* Ab = A + (((size_t)l * E + e) * r + (size_t)g * R) * K;
+  const int cpr = K / 8;
+  for (int i = threadIdx.x; i < nr * cpr; i += blockDim.x) {
+    const int rho = i / cpr, c = i - rho * cpr;
+    shrink_cp_async16(sA + (size_t)rho * astride + c * 16, Ab + (size_t)rho * K + c * 8);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  // activation fragments of this warp's k-steps (rows gid < rows)
+  const int nsteps = (K + 31) >> 5;
+  const __nv_bfloat16* x0 = nullptr;
+  if (gid < rows) {
+    const int row = row0 + gid;
+    x0 = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
+  }
+  uint4 xa[kShortUMax];
+#pragma unroll
+  for (int u = 0; u < kShortUMax; ++u) {
+    const int st = warp + kShrinkWarps * u;
+    const int k0 = st * 32 + q * 8;
+    xa[u] = make_uint4(0, 0, 0, 0);
+    if (x0 && st < nsteps && (kEvenK || k0 < K)) xa[u] = __ldcg(reinterpret_cast<const uint4*>(x0 + k0));
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+  for (int u = 0; u < kShortUMax; ++u) {
+    const int st = warp + kShrinkWarps * u;
+    if (st >= nsteps) break;
+    const int k0 = st * 32 + q * 8;
+    const bool kin = kEvenK || k0 < K;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int rho = nt * 8 + gid;
+      uint4 av = make_uint4(0, 0, 0, 0);
+      if (rho < nr && kin) av = *reinterpret_cast<const uint4*>(sA + (size_t)rho * astride + k0 * 2);
+      mma_16816(acc[nt], xa[u].x, 0u, xa[u].y, 0u, av.x, av.y);
+      mma_16816(acc[nt], xa[u].z, 0u, xa[u].w, 0u, av.z, av.w);
+    }
+  }
+  __syncthreads();  // every warp is done with the slab
+  float (*red)[8][R + 1] = reinterpret_cast<float (*)[8][R + 1]>(sA);  // [warp][row][rank]
+  // accumulator fragment: c0, c1 -> (row gid, ranks 2q, 2q+1); rows 8..15 are empty
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][gid][nt * 8 + 2 * q] = acc[nt][0];
+    red[warp][gid][nt * 8 + 2 * q + 1] = acc[nt][1];
+  }
+  __syncthreads();
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  for (int idx = threadIdx.x; idx < rows * R; idx += blockDim.x) {
+    const int m = idx / R, c = idx - m * R;
+    const int rank = g * R + c;
+    if (rank >= r) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kShrinkWarps; ++w) sum += red[w][m][c];
+    const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
+    Z[(size_t)slot * r + rank] = sum;
+  }
+}
+
 template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
@@ -223,6 +338,31 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
     case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
     case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
     case 4:  // short blocks: two k-steps per batch, still two CTAs per SM
+      if (al->bm_lora <= 8 && vec && K <= 32 * kShrinkWarps * kShortUMax &&
+          32 * short_astride(K) <= 56 * 1024) {  // short K: the slab in shared memory
+        const int astride = short_astride(K);
+        // the reduction reuses the slab: [8 warps][8 rows][33] floats at least
+        const size_t smem = std::max((size_t)32 * astride, (size_t)kShrinkWarps * 8 * 33 * sizeof(float));
+        const int ngroups = ceil_div(r, 32);
+        const int64_t grid = (int64_t)a.max_blocks * ngroups;
+        if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
+        static int configured[64] = {0};  // both instances at once, once per device
+        int dev = 0;
+        ML_CHECK_CUDA(cudaGetDevice(&dev));
+        if (dev < 64 && !configured[dev]) {
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 56 * 1024));
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 56 * 1024));
+          configured[dev] = 1;
+        }
+        auto go = [&](auto kern) -> int {
+          return launch_pdl(kern, dim3((unsigned)grid), kShrinkWarps * 32, smem, stream, pdl, Xp,
+                            rows_are_slots, Ap, (const int*)v.hdr, (const int4*)v.blocks,
+                            (const int*)v.sorted_slots, al->k, K, r, al->E, Z, ngroups, ea, astride);
+        };
+        return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true>) : go(lora_shrink_smem_kernel<4, false>);
+      }
       if (al->bm_lora <= 8)
         return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true);
       return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false);

@@ -194,6 +194,9 @@ MOE_LORA_API int lora_shrink(const void* X, int rows_are_slots, const void* A, c
  *               j in increasing order; out [T, N] bf16 (out_fp32 = 0) or fp32.
  *               base is only read.
  * Z [S, r] fp32; B [L, E, N, r] bf16 (NULL or L = 0: no adapter term);
+ *   epilogue 3: as epilogue 1 with separate gate and up adapters: Z rows hold 2r
+ *               values, columns [0, N/2) take z[0, r) and B rows [0, N/2), columns
+ *               [N/2, N) take z[r, 2r) and B rows [N/2, N); B stays [L, E, N, r].
  * topk_w [T, k] fp32 (epilogue 2 only). Requires L < 65535. Deterministic.
  * ------------------------------------------------------------------------- */
 MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_align_t* al, int N, int r,
@@ -230,6 +233,12 @@ typedef struct moe_lora_layer_opts {
                            after the last: [0] route, [1] align, [2] gather, [3] gate_up GEMM,
                            [4] gate_up shrink, [5] gate_up expand+SwiGLU, [6] down GEMM,
                            [7] down shrink, [8] down expand+combine, [9] end */
+  int32_t gate_up_slices; /* 0 or 1: one adapter over the fused gate_up output (A1
+                           [L,E,r,H]); 2: separate gate and up adapters, A1 [L,E,2r,H]
+                           with the gate A in rows [0,r) and the up A in [r,2r), B1
+                           [L,E,2I,r] unchanged: gate columns take the gate z, up columns
+                           the up z (lora_expand_add epilogue 3). The pages describe one
+                           adapter per projection and are silent on a split gate_up. */
 } moe_lora_layer_opts;
 
 #define MOE_LORA_LAYER_NUM_STAGES 9

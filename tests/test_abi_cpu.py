@@ -136,8 +136,10 @@ def test_host_validation_before_any_cuda_call(L):
     assert L.moe_grouped_gemm(P(0x1008), fake, ctypes.byref(ok), 64, 64, fake, None) == 1
     assert L.lora_shrink(fake, 2, fake, ctypes.byref(ok), 64, 8, fake, None) == 1
     assert L.lora_shrink(fake, 0, fake, ctypes.byref(ok), 64, 300, fake, None) == 2
-    assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 64, 8, 3, fake, fake, 0, fake,
-                             None) == 1
+    assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 64, 8, 4, fake, fake, 0, fake,
+                             None) == 1  # epilogues are 0..3
+    assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 63, 8, 3, fake, fake, 0, fake,
+                             None) == 1  # SwiGLU epilogues need an even N
     assert L.lora_expand_add(fake, fake, ctypes.byref(ok), 63, 8, 1, fake, fake, 0, fake,
                              None) == 1                                     # SwiGLU needs even N
     args = [fake, fake, None, None, None, 8, 256, 512, 4, 2, fake, fake, fake, fake, fake, fake,

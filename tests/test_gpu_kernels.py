@@ -270,16 +270,25 @@ def test_expand_short_segment_forms(r, k):
                  KERNEL_RTOL, "expand epilogue 2, token walk")
 
 
-@pytest.mark.parametrize("K", [768, 2048])
-def test_shrink_short_blocks_all_ranks(K):
-    """Many short blocks (the many-adapter stress shape): one CTA takes all 32 ranks of a
-    block with two k-steps per load batch."""
-    m, inp, ids, w, al, ref = _setup(T=256, H=K, I=8, E=128, k=8, L=16, r=32, seed=18,
+@pytest.mark.parametrize("K", [136, 768, 2048])
+@pytest.mark.parametrize("r", [32, 24])
+def test_shrink_short_blocks_all_ranks(K, r):
+    """Many short blocks (the many-adapter stress shape): one CTA takes all ranks of a block;
+    K <= 832 stages the A slab in shared memory through asynchronous copies (K = 136: a
+    partial last k-step), longer K loads two k-steps per batch into registers; r = 24 leaves
+    the last rank tile partial."""
+    m, inp, ids, w, al, ref = _setup(T=256, H=K, I=8, E=128, k=8, L=16, r=r, seed=18,
                                      bm_lora=8, adapters="zipf1.1")
-    Z = Guarded((al.S, 32), torch.float32, fill=0.0)
+    Z = Guarded((al.S, r), torch.float32, fill=0.0)
     m.lora_shrink(dev(inp.x), False, dev(inp.A1), al, out=Z.t)
     Z.check()
-    assert_close(Z.t, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"K={K}")
+    assert_close(Z.t, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"K={K} r={r}")
+    # the down shrink's form: rows addressed by sorted row
+    n = ref["n_valid"]
+    h = torch.from_numpy(np.random.default_rng(9).standard_normal((al.S, K), dtype=np.float32)).to(torch.bfloat16)
+    Z2 = m.lora_shrink(dev(h), True, dev(inp.A1), al)
+    assert_close(Z2, oracle.lora_shrink(h[:n], inp.A1, ref, rows_are_slots=True), KERNEL_RTOL,
+                 f"sorted rows K={K} r={r}")
 
 
 @pytest.mark.parametrize("I", [300, 302, 1024])
@@ -298,3 +307,29 @@ def test_expand_swiglu_long_segments_ragged(I, r):
     h.check()
     assert_bf16_close(h.t[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=1),
                       f"expand epilogue 1, long segments, I={I} r={r}")
+
+
+@pytest.mark.parametrize("shape", ["short", "long", "long_ragged"])
+@pytest.mark.parametrize("r", [5, 8, 32, 64])
+def test_expand_two_slices(shape, r):
+    """Epilogue 3: SwiGLU with separate gate and up adapters (z rows of 2r values, the up
+    columns taking the second r), on each form of the expand: one row per CTA (short
+    segments), the tensor-core block walk (long segments) and the CUDA-core row walk
+    (I % 4 != 0, or r not a multiple of 8)."""
+    if shape == "short":
+        T, I, E, k, L = 48, 300, 32, 4, 8
+        adapters = "round_robin_shuffled"
+    else:
+        T, I, E, k, L = 512, (300 if shape == "long" else 302), 4, 2, 2
+        adapters = "uniform_with_none"
+    m, inp, ids, w, al, ref = _setup(T=T, H=64, I=I, E=E, k=k, L=L, r=r, seed=20,
+                                     adapters=adapters)
+    n = ref["n_valid"]
+    rng = np.random.default_rng(10)
+    Zh = torch.from_numpy(rng.standard_normal((al.S, 2 * r))).to(torch.float32)
+    G = torch.from_numpy(rng.standard_normal((al.S, 2 * I), dtype=np.float32))
+    h = Guarded((al.S, I), torch.bfloat16)
+    m.lora_expand_add(dev(Zh), dev(inp.B1), al, 3, dev(G), out=h.t)
+    h.check()
+    assert_bf16_close(h.t[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=3),
+                      f"epilogue 3, {shape} segments, r={r}")

@@ -215,3 +215,29 @@ def test_layers_chained_in_cuda_graph():
     assert m.get_error(ws) == 0
     ref = oracle_layer(inp)
     assert_close(eager[0].cpu(), ref, LAYER_RTOL, "first chained layer")
+
+
+@pytest.mark.parametrize("shape", ["tiny", "decode", "prefill_like"])
+def test_layer_two_slice_gate_up(shape):
+    """Separate gate and up adapters (A1 [L, E, 2r, H]) through the whole layer: the gate_up
+    shrink runs at rank 2r and the SwiGLU expand gives each half its own z."""
+    m = need_gpu()
+    if shape == "tiny":
+        kw = dict(T=8, H=256, I=512, E=4, k=2, L=2, r=8, adapters="tiny")
+    elif shape == "decode":
+        kw = dict(T=64, H=512, I=384, E=32, k=4, L=8, r=32, adapters="round_robin_shuffled")
+    else:
+        kw = dict(T=1024, H=256, I=256, E=8, k=2, L=16, r=16, adapters="one_per_request16")
+    inp = make_layer_inputs(seed=31, lora_std=None, **kw)
+    rng = np.random.default_rng(32)
+    A1s = torch.from_numpy(rng.standard_normal((inp.L, inp.E, 2 * inp.r, inp.H)).astype(np.float32)
+                           * 0.05).to(torch.bfloat16)
+    lora = dict(A1=dev(A1s), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
+    y = Guarded((inp.T, inp.H), torch.bfloat16)
+    m.moe_lora_layer(dev(inp.x), dev(inp.W1), dev(inp.W2), logits=dev(inp.logits), k=inp.k,
+                     token_adapter=dev(inp.token_adapter), y=y.t, gate_up_slices=2, **lora)
+    y.check()
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    ref = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, A1s, inp.B1,
+                                inp.A2, inp.B2, gate_up_slices=2)
+    assert_close(y.t.cpu(), ref, LAYER_RTOL, f"two-slice gate_up, {shape}")
