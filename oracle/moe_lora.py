@@ -34,6 +34,9 @@ Readings where the pages are silent (each also listed in the design notes):
 * A slot whose expert id or whose token's adapter id is out of range is
   dropped (contributes nothing) and flagged in an error word.
 * Intermediates are kept in fp64 with no rounding.
+* Adapters of different ranks (the pages give ranks "typically 16-64" but one r
+  per serving instance): adapter l of rank r_l <= r is stored padded to r and uses
+  the first r_l rows of A (of each slice) and the first r_l columns of B.
 * Separate gate and up adapters (the pages describe one LoRA per projection and
   are silent on a gate_up projection split in two): A1 [L, E, 2r, H] stacks the
   gate and the up A, B1 [L, E, 2I, r] keeps gate rows first, and each half of
@@ -217,14 +220,43 @@ def grouped_gemm(a_sorted, W, al: dict) -> np.ndarray:
     return out
 
 
-def lora_shrink(X, A, al: dict, rows_are_slots: bool) -> np.ndarray:
+def rank_mask_A(A, adapter_ranks, rank: int):
+    """A of adapters with their own ranks: adapter l keeps rows [0, r_l) of each slice of
+    `rank` rows (r_l clamped to [0, rank]); the rows past r_l are zero."""
+    Af = as_f64(A)
+    if adapter_ranks is None:
+        return Af
+    Af = Af.copy()
+    for l, rl in enumerate(as_i64(adapter_ranks)):
+        rl = min(max(int(rl), 0), rank)
+        for sl in range(Af.shape[2] // rank):
+            Af[l, :, sl * rank + rl: (sl + 1) * rank] = 0.0
+    return Af
+
+
+def rank_mask_B(B, adapter_ranks):
+    """B of adapters with their own ranks: adapter l keeps columns [0, r_l)."""
+    Bf = as_f64(B)
+    if adapter_ranks is None:
+        return Bf
+    Bf = Bf.copy()
+    rank = Bf.shape[3]
+    for l, rl in enumerate(as_i64(adapter_ranks)):
+        Bf[l, :, :, min(max(int(rl), 0), rank):] = 0.0
+    return Bf
+
+
+def lora_shrink(X, A, al: dict, rows_are_slots: bool, adapter_ranks=None,
+                rank: int = None) -> np.ndarray:
     """Shrink z = x A for every slot with an adapter; Z [S, r], zero elsewhere.
 
     rows_are_slots=False: the input row of slot s is token s // k of X [T, K].
     rows_are_slots=True:  the input row of slot s is its sorted row of X [n, K].
+    adapter_ranks [L]: adapter l uses rows [0, r_l) of each slice of `rank` rows of A
+    (default: all rows, one slice); z entries past r_l are zero.
     """
     Xf = as_f64(X)
-    Af = as_f64(A)
+    Af = rank_mask_A(A, adapter_ranks, as_f64(A).shape[2] if rank is None else rank)
     r = Af.shape[2]
     Z = np.zeros((al["S"], r))
     n = al["n_valid"]
@@ -239,15 +271,15 @@ def lora_shrink(X, A, al: dict, rows_are_slots: bool) -> np.ndarray:
     return Z
 
 
-def lora_delta_rows(Z, B, al: dict, slices: int = 1) -> np.ndarray:
+def lora_delta_rows(Z, B, al: dict, slices: int = 1, adapter_ranks=None) -> np.ndarray:
     """Expand z B for each sorted row with an adapter; [n_valid, N], zero elsewhere.
 
     slices = 2 (separate gate and up adapters): z rows hold 2r values; output
     columns [0, N/2) take the first r with B rows [0, N/2), columns [N/2, N) the
-    last r with B rows [N/2, N).
+    last r with B rows [N/2, N). adapter_ranks [L]: adapter l uses columns [0, r_l) of B.
     """
     Zf = as_f64(Z)
-    Bf = as_f64(B)
+    Bf = rank_mask_B(B, adapter_ranks)
     n = al["n_valid"]
     N = Bf.shape[2]
     r = Bf.shape[3]
@@ -280,7 +312,8 @@ def combine(O_rows, w, al: dict) -> np.ndarray:
     return y
 
 
-def lora_expand_add(Z, B, al: dict, base_rows, epilogue: int, w=None) -> np.ndarray:
+def lora_expand_add(Z, B, al: dict, base_rows, epilogue: int, w=None,
+                    adapter_ranks=None) -> np.ndarray:
     """Expand with the base add fused (vllm.com.cn, "Kernel optimizations").
 
     epilogue 0: base + zB                      [n_valid, N]
@@ -289,7 +322,8 @@ def lora_expand_add(Z, B, al: dict, base_rows, epilogue: int, w=None) -> np.ndar
     epilogue 3: as 1 with separate gate and up adapters (two z slices; see
                 lora_delta_rows)              [n_valid, N/2]
     """
-    G = as_f64(base_rows) + lora_delta_rows(Z, B, al, slices=2 if epilogue == 3 else 1)
+    G = as_f64(base_rows) + lora_delta_rows(Z, B, al, slices=2 if epilogue == 3 else 1,
+                                            adapter_ranks=adapter_ranks)
     if epilogue == 0:
         return G
     if epilogue in (1, 3):
@@ -309,7 +343,7 @@ def _slots_ok(ids, ad, E, L):
 
 
 def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=None,
-                   B2=None, gate_up_slices: int = 1) -> np.ndarray:
+                   B2=None, gate_up_slices: int = 1, adapter_ranks=None) -> np.ndarray:
     """y[t] = sum_j w[t,j] * expert_{ids[t,j]}(x[t]) with the token's adapter.
 
     expert_e with adapter l (l = -1: none):
@@ -319,6 +353,8 @@ def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=N
     gate_up_slices = 2: the gate and up projections carry separate adapters,
     A1 [L, E, 2r, H] (rows [0, r) gate, [r, 2r) up), B1 [L, E, 2I, r]:
       g[:I] += (x A1_{l,e}[:r]^T) B1_{l,e}[:I]^T,  g[I:] += (x A1_{l,e}[r:]^T) B1_{l,e}[I:]^T
+    adapter_ranks [L]: adapter l has rank r_l <= r: it uses the first r_l rows of each
+    slice of A1 and of A2 and the first r_l columns of B1 and B2 (stored padded to r).
     Slots that share (e, l) are stacked into one matrix product per group; the
     arithmetic per slot is unchanged. Weights may be torch tensors or fp64
     numpy arrays (the latter skip the per-call conversion).
@@ -333,6 +369,12 @@ def moe_lora_layer(x, W1, W2, ids, w, token_adapter=None, A1=None, B1=None, A2=N
     if L == 0:
         ad = np.full(T, -1, dtype=np.int64)  # no adapter resident: adapter ids carry no meaning
     ok = _slots_ok(ids_, ad, E, L)
+    if adapter_ranks is not None and L > 0:
+        rk = B2.shape[3]
+        A1 = rank_mask_A(A1, adapter_ranks, rk)
+        B1 = rank_mask_B(B1, adapter_ranks)
+        A2 = rank_mask_A(A2, adapter_ranks, rk)
+        B2 = rank_mask_B(B2, adapter_ranks)
 
     y = np.zeros((T, X.shape[1]))
     tt, jj = np.nonzero(ok)

@@ -380,6 +380,93 @@ def test_planted_two_slice_swap(monkeypatch):
                                                 adapters="uniform_with_none"), 500)
 
 
+def pin_adapter_ranks(inp, ranks, slices=1, seed=0):
+    """Adapters of their own ranks, by brute force over slots with truncated weights: adapter
+    l of rank r_l uses A[:r_l] (per slice) and B[:, :r_l]. Checks the layer and the
+    shrink / expand ops the GPU kernels are compared with."""
+    X = om.as_f64(inp.x)
+    W1, W2 = om.as_f64(inp.W1), om.as_f64(inp.W2)
+    rng = np.random.default_rng(seed)
+    r = inp.r
+    A1 = torch.from_numpy(rng.standard_normal((inp.L, inp.E, slices * r, inp.H)) * 0.1)
+    B1, A2, B2 = om.as_f64(inp.B1), om.as_f64(inp.A2), om.as_f64(inp.B2)
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    ad = om.as_i64(inp.token_adapter)
+    A1f = om.as_f64(A1)
+    I = W2.shape[2]
+    y = np.zeros_like(X)
+    for t in range(inp.T):
+        for j in range(inp.k):
+            e, l = int(ids[t, j]), int(ad[t])
+            g = W1[e] @ X[t]
+            if l >= 0:
+                rl = int(ranks[l])
+                if slices == 1:
+                    g = g + B1[l, e][:, :rl] @ (A1f[l, e][:rl] @ X[t])
+                else:
+                    g[:I] += B1[l, e][:I, :rl] @ (A1f[l, e][:rl] @ X[t])
+                    g[I:] += B1[l, e][I:, :rl] @ (A1f[l, e][r: r + rl] @ X[t])
+            h = g[:I] / (1.0 + np.exp(-g[:I])) * g[I:]
+            o = W2[e] @ h
+            if l >= 0:
+                o = o + B2[l, e][:, :rl] @ (A2[l, e][:rl] @ h)
+            y[t] += float(w[t, j]) * o
+    yo = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, A1, inp.B1,
+                               inp.A2, inp.B2, gate_up_slices=slices,
+                               adapter_ranks=torch.as_tensor(ranks))
+    assert _rel(yo, y) < 1e-12, _rel(yo, y)
+    # the ops: shrink z (zero past r_l) and the expand delta
+    al = oracle.align(torch.as_tensor(ids, dtype=torch.int32), inp.token_adapter, inp.E, inp.L, 16, 4)
+    Z = oracle.lora_shrink(inp.x, A1, al, False, adapter_ranks=torch.as_tensor(ranks), rank=r)
+    Zb = np.zeros_like(Z)
+    D = np.zeros((al["n_valid"], B1.shape[2]))
+    for row in range(al["n_valid"]):
+        l = int(al["row_adapter"][row])
+        if l < 0:
+            continue
+        e, sl = int(al["row_expert"][row]), int(al["sorted_slots"][row])
+        rl = int(ranks[l])
+        for c in range(slices):
+            Zb[sl, c * r: c * r + rl] = A1f[l, e][c * r: c * r + rl] @ X[sl // inp.k]
+        if slices == 1:
+            D[row] = B1[l, e][:, :rl] @ Zb[sl, :rl]
+        else:
+            D[row, :I] = B1[l, e][:I, :rl] @ Zb[sl, :rl]
+            D[row, I:] = B1[l, e][I:, :rl] @ Zb[sl, r: r + rl]
+    assert _rel(Z, Zb) < 1e-12, _rel(Z, Zb)
+    Dq = om.lora_delta_rows(Zb, inp.B1, al, slices=slices, adapter_ranks=torch.as_tensor(ranks))
+    assert _rel(Dq, D) < 1e-12, _rel(Dq, D)
+
+
+@pytest.mark.parametrize("slices", [1, 2])
+def test_adapter_ranks(slices):
+    inp = make_layer_inputs(T=9, H=20, I=12, E=3, k=2, L=4, r=6, seed=600 + slices,
+                            adapters="uniform_with_none")
+    pin_adapter_ranks(inp, [6, 3, 0, 5], slices, seed=700 + slices)
+    # full ranks reproduce the unranked oracle
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    y0 = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, inp.A1, inp.B1,
+                               inp.A2, inp.B2)
+    y1 = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, inp.A1, inp.B1,
+                               inp.A2, inp.B2, adapter_ranks=torch.full((4,), 6))
+    assert _rel(y1, y0) == 0.0
+
+
+def test_planted_rank_off_by_one(monkeypatch):
+    """Keeping one row too many of a truncated adapter trips the rank pin."""
+    real = om.rank_mask_A
+
+    def loose(A, adapter_ranks, rank):
+        if adapter_ranks is None:
+            return real(A, None, rank)
+        return real(A, [min(int(v) + 1, rank) for v in om.as_i64(adapter_ranks)], rank)
+
+    monkeypatch.setattr(om, "rank_mask_A", loose)
+    inp = make_layer_inputs(T=9, H=20, I=12, E=3, k=2, L=4, r=6, seed=601, adapters="uniform_with_none")
+    with pytest.raises(AssertionError):
+        pin_adapter_ranks(inp, [6, 3, 0, 5], 1, seed=701)
+
+
 def test_dense_swiglu_mlp():
     pin_dense_swiglu_mlp()
 
