@@ -365,14 +365,14 @@ def test_planted_two_slice_swap(monkeypatch):
     """Feeding the up z to the gate columns (and the gate z to the up columns) trips the pin."""
     real = om.lora_delta_rows
 
-    def swapped(Z, B, al, slices=1):
+    def swapped(Z, B, al, slices=1, adapter_ranks=None):
         if slices == 1:
-            return real(Z, B, al, 1)
+            return real(Z, B, al, 1, adapter_ranks)
         Zf = np.array(om.as_f64(Z))
         r = om.as_f64(B).shape[3]
         Zs = Zf.copy()
         Zs[:, :r], Zs[:, r: 2 * r] = Zf[:, r: 2 * r], Zf[:, :r]
-        return real(Zs, B, al, 2)
+        return real(Zs, B, al, 2, adapter_ranks)
 
     monkeypatch.setattr(om, "lora_delta_rows", swapped)
     with pytest.raises(AssertionError):
