@@ -39,13 +39,14 @@ class MoeLoraError(RuntimeError):
 class AlignDesc(ctypes.Structure):
     _fields_ = [("buf", ctypes.c_void_p), ("T", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("L", ctypes.c_int32), ("bm_base", ctypes.c_int32),
-                ("bm_lora", ctypes.c_int32)]
+                ("bm_lora", ctypes.c_int32), ("adapter_ranks", ctypes.c_void_p)]
 
 
 class LayerOpts(ctypes.Structure):
     _fields_ = [("bm_base", ctypes.c_int32), ("bm_lora", ctypes.c_int32),
                 ("disable_pdl", ctypes.c_int32), ("num_events", ctypes.c_int32),
-                ("events", ctypes.POINTER(ctypes.c_void_p)), ("gate_up_slices", ctypes.c_int32)]
+                ("events", ctypes.POINTER(ctypes.c_void_p)), ("adapter_ranks", ctypes.c_void_p),
+                ("gate_up_slices", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p

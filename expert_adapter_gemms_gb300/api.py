@@ -168,9 +168,17 @@ def moe_grouped_gemm(a_sorted: torch.Tensor, W: torch.Tensor, al: Align,
     return out
 
 
+def _with_ranks(d: AlignDesc, adapter_ranks: Optional[torch.Tensor], L: int) -> AlignDesc:
+    if adapter_ranks is not None:
+        _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (L,))
+        d.adapter_ranks = ptr(adapter_ranks)
+    return d
+
+
 def lora_shrink(X: torch.Tensor, rows_are_slots: bool, A: torch.Tensor, al: Align,
-                out: Optional[torch.Tensor] = None):
-    """Z[s] = X[in(s)] @ A[l(s), e(s)].T for the slots with an adapter (fp32 out)."""
+                out: Optional[torch.Tensor] = None, adapter_ranks: Optional[torch.Tensor] = None):
+    """Z[s] = X[in(s)] @ A[l(s), e(s)].T for the slots with an adapter (fp32 out);
+    adapter_ranks [L] int32 (device): adapter l uses the first r_l rows of A."""
     _need(X, "X", torch.bfloat16, 2)
     _need(A, "A", torch.bfloat16, 4)
     Ln, E, r, K = A.shape
@@ -179,7 +187,7 @@ def lora_shrink(X: torch.Tensor, rows_are_slots: bool, A: torch.Tensor, al: Alig
     if out is None:
         out = torch.zeros((al.S, r), dtype=torch.float32, device=X.device)
     _need(out, "out", torch.float32, 2, (al.S, r))
-    d = al.desc()
+    d = _with_ranks(al.desc(), adapter_ranks, al.L)
     check(lib().lora_shrink(ptr(X), int(bool(rows_are_slots)), ptr(A), ctypes.byref(d), K, r,
                             ptr(out), stream_handle()), "lora_shrink")
     return out
@@ -187,9 +195,11 @@ def lora_shrink(X: torch.Tensor, rows_are_slots: bool, A: torch.Tensor, al: Alig
 
 def lora_expand_add(Z: torch.Tensor, B: Optional[torch.Tensor], al: Align, epilogue: int,
                     base: torch.Tensor, out: Optional[torch.Tensor] = None, out_fp32: bool = False,
-                    topk_w: Optional[torch.Tensor] = None, N: Optional[int] = None):
+                    topk_w: Optional[torch.Tensor] = None, N: Optional[int] = None,
+                    adapter_ranks: Optional[torch.Tensor] = None):
     """Expand with the base add fused; epilogue 0 (in place), 1 (SwiGLU), 2 (combine),
-    3 (SwiGLU with separate gate and up adapters: Z rows hold 2r values)."""
+    3 (SwiGLU with separate gate and up adapters: Z rows hold 2r values). adapter_ranks
+    [L] int32 (device): adapter l uses the first r_l columns of B."""
     _need(base, "base", torch.float32, 2)
     Nb = base.shape[1]
     r = 0
@@ -207,7 +217,7 @@ def lora_expand_add(Z: torch.Tensor, B: Optional[torch.Tensor], al: Align, epilo
                           device=dev)
     if epilogue == 2:
         _need(topk_w, "topk_w", torch.float32, 2, (al.T, al.k))
-    d = al.desc()
+    d = _with_ranks(al.desc(), adapter_ranks, al.L)
     check(lib().lora_expand_add(ptr(Z) if B is not None else 0, ptr(B), ctypes.byref(d), Nb, r,
                                 epilogue, ptr(base), ptr(out), int(out_fp32), ptr(topk_w),
                                 stream_handle()), "lora_expand_add")
@@ -242,9 +252,11 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
                    A1=None, B1=None, A2=None, B2=None, y: Optional[torch.Tensor] = None,
                    y_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
                    bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
-                   events: Optional[Sequence] = None, gate_up_slices: int = 1) -> torch.Tensor:
+                   events: Optional[Sequence] = None, gate_up_slices: int = 1,
+                   adapter_ranks: Optional[torch.Tensor] = None) -> torch.Tensor:
     """The whole fused MoE-LoRA layer; returns y [T, H]. gate_up_slices=2: separate gate
-    and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r]."""
+    and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r].
+    adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r)."""
     _need(x, "x", torch.bfloat16, 2)
     _need(W1, "W1", torch.bfloat16, 3)
     _need(W2, "W2", torch.bfloat16, 3)
@@ -284,6 +296,9 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     opts = LayerOpts()
     opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
     opts.gate_up_slices = gate_up_slices
+    if adapter_ranks is not None:
+        _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (Ln,))
+        opts.adapter_ranks = ptr(adapter_ranks)
     ev_arr = None
     if events:
         ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])

@@ -204,6 +204,7 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   al.L = L;
   al.bm_base = p.bm_base;
   al.bm_lora = p.bm_lora;
+  al.adapter_ranks = L > 0 ? o.adapter_ranks : nullptr;
   int32_t* ids = reinterpret_cast<int32_t*>(ws + p.off_ids);
   float* w = reinterpret_cast<float*>(ws + p.off_w);
   void* xs = ws + p.off_xs;
@@ -249,9 +250,9 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   if (L > 0) {
     // with separate gate and up adapters the gate_up shrink is one of rank 2r
     if (p.bm_lora <= 8)
-      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl));
     else
-      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl));
   }
   ML_STEP(mark(5));
   ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, L > 0 && slices == 2 ? 3 : 1, G, h, 0,
@@ -259,7 +260,7 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(mark(6));
   ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, 0));
   ML_STEP(mark(7));
-  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, Z2, stream, pdl, pdl));
+  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, pdl));
   ML_STEP(mark(8));
   ML_STEP(launch_expand_impl(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w,
                              stream, pdl, pdl && L > 0));

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kExpandThreads)
     expand_add_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                       const int* __restrict__ hdr, const int4* __restrict__ blocks,
                       const int* __restrict__ sorted_slots, int N, int r, int E,
-                      float* __restrict__ base, int early) {
+                      float* __restrict__ base, int early, const int* __restrict__ ranks) {
   extern __shared__ float zs[];  // [rows][r]
   if (!early) pdl_wait();
   const int nb = __ldcg(hdr + HDR_NBLOCKS);
@@ -89,12 +89,13 @@ __global__ void __launch_bounds__(kExpandThreads)
   const int n0 = blockIdx.y * (2 * kExpandThreads) + threadIdx.x;
   const int n1 = n0 + kExpandThreads;
   const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
+  const int rl = adapter_rank(ranks, l, r, hdr);  // B columns past it are not used
   uint4 b0[RV > 0 ? RV : 1], b1[RV > 0 ? RV : 1];
   if (RV > 0) {
 #pragma unroll
     for (int i = 0; i < RV; ++i) {
-      b0[i] = n0 < N ? __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n0 * r) + i) : make_uint4(0, 0, 0, 0);
-      b1[i] = n1 < N ? __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n1 * r) + i) : make_uint4(0, 0, 0, 0);
+      b0[i] = n0 < N ? b_group(reinterpret_cast<const uint4*>(bl + (size_t)n0 * r), i, rl) : make_uint4(0, 0, 0, 0);
+      b1[i] = n1 < N ? b_group(reinterpret_cast<const uint4*>(bl + (size_t)n1 * r), i, rl) : make_uint4(0, 0, 0, 0);
     }
   }
   if (early) pdl_wait();
@@ -113,12 +114,12 @@ __global__ void __launch_bounds__(kExpandThreads)
       if (RV > 0) {
 #pragma unroll
         for (int i = 0; i < RV; ++i) {
-          fma8(acc0[m], zs + m * r + 8 * i, b0[i]);
-          fma8(acc1[m], zs + m * r + 8 * i, b1[i]);
+          fma8(acc0[m], zs + m * r + 8 * i, b_tail(b0[i], 8 * i, rl));
+          fma8(acc1[m], zs + m * r + 8 * i, b_tail(b1[i], 8 * i, rl));
         }
       } else {
-        if (n0 < N) acc0[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n0 * r, r);
-        if (n1 < N) acc1[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n1 * r, r);
+        if (n0 < N) acc0[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n0 * r, rl);
+        if (n1 < N) acc1[m] = dot_zb_mem<false>(zs + m * r, bl + (size_t)n1 * r, rl);
       }
     }
   }
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kExpandThreads)
                          const int* __restrict__ row_expert, const int* __restrict__ row_adapter,
                          int I, int r, int E, const float* __restrict__ G,
                          __nv_bfloat16* __restrict__ h, int rows_per_cta, int early,
-                         int zstride, int zu_off) {
+                         int zstride, int zu_off, const int* __restrict__ ranks) {
   // z rows: zstride floats (r, or 2r with separate gate and up adapters); the gate
   // columns take z[0, r), the up columns z[zu_off, zu_off + r)
   extern __shared__ float zs[];  // [rows_per_cta][zstride]
@@ -174,14 +175,15 @@ __global__ void __launch_bounds__(kExpandThreads)
   }
   __syncthreads();
   uint4 bg[RV > 0 ? RV : 1], bu[RV > 0 ? RV : 1];
-  int cur = -1;
+  int cur = -1, cur_rl = r;
   auto load_b = [&](int key) {
     const int e = key >> 16, l = (key & 0xffff) - 1;
     const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+    cur_rl = adapter_rank(ranks, l, r, hdr);  // B columns past it are not used
 #pragma unroll
     for (int i = 0; i < RV; ++i) {
-      bg[i] = __ldg(reinterpret_cast<const uint4*>(bl + (size_t)n * r) + i);
-      bu[i] = __ldg(reinterpret_cast<const uint4*>(bl + (size_t)(I + n) * r) + i);
+      bg[i] = b_group(reinterpret_cast<const uint4*>(bl + (size_t)n * r), i, cur_rl);
+      bu[i] = b_group(reinterpret_cast<const uint4*>(bl + (size_t)(I + n) * r), i, cur_rl);
     }
   };
   // G values are fetched four rows at a time; the first batch and the first B rows
@@ -233,14 +235,15 @@ __global__ void __launch_bounds__(kExpandThreads)
           }
 #pragma unroll
           for (int i = 0; i < RV; ++i) {
-            fma8(g, zs + m * zstride + 8 * i, bg[i]);
-            fma8(u, zs + m * zstride + zu_off + 8 * i, bu[i]);
+            fma8(g, zs + m * zstride + 8 * i, b_tail(bg[i], 8 * i, cur_rl));
+            fma8(u, zs + m * zstride + zu_off + 8 * i, b_tail(bu[i], 8 * i, cur_rl));
           }
         } else {
           const int e = key >> 16, l = (key & 0xffff) - 1;
           const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
-          g += dot_zb_mem<false>(zs + m * zstride, bl + (size_t)n * r, r);
-          u += dot_zb_mem<false>(zs + m * zstride + zu_off, bl + (size_t)(I + n) * r, r);
+          const int rl = adapter_rank(ranks, l, r, hdr);
+          g += dot_zb_mem<false>(zs + m * zstride, bl + (size_t)n * r, rl);
+          u += dot_zb_mem<false>(zs + m * zstride + zu_off, bl + (size_t)(I + n) * r, rl);
         }
       }
       h[(size_t)(r0 + m) * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
@@ -262,7 +265,8 @@ __global__ void __launch_bounds__(kExpandThreads)
                           const int* __restrict__ slot_row, const int* __restrict__ row_expert,
                           const int* __restrict__ row_adapter, const float* __restrict__ w,
                           int T, int k, int N, int r, int E, const float* __restrict__ O,
-                          void* __restrict__ y, int tokens_per_cta, int early) {
+                          void* __restrict__ y, int tokens_per_cta, int early,
+                          const int* __restrict__ ranks) {
   extern __shared__ float zs[];  // [tokens_per_cta * k][r]
   __shared__ int s_row[256], s_key[256];
   __shared__ float s_w[256];
@@ -294,8 +298,9 @@ __global__ void __launch_bounds__(kExpandThreads)
     if (s_row[q] >= 0) o = __ldcg(O + (size_t)s_row[q] * N + n);
     if (RV > 0 && s_key[q] >= 0) {
       const uint4* p = reinterpret_cast<const uint4*>(brow(s_key[q]));
+      const int rl = adapter_rank(ranks, (s_key[q] & 0xffff) - 1, r, nullptr);
 #pragma unroll
-      for (int i = 0; i < RV; ++i) bv[i] = __ldg(p + i);
+      for (int i = 0; i < RV; ++i) bv[i] = b_group(p, i, rl);
     }
   };
   float o_cur = 0.f;
@@ -321,10 +326,11 @@ __global__ void __launch_bounds__(kExpandThreads)
         float o = o_cur;
         if (s_key[q] >= 0) {
           if (RV > 0) {
+            const int rl = adapter_rank(ranks, (s_key[q] & 0xffff) - 1, r, nullptr);
 #pragma unroll
-            for (int i = 0; i < RV; ++i) fma8(o, zs + q * r + 8 * i, bcur[i]);
+            for (int i = 0; i < RV; ++i) fma8(o, zs + q * r + 8 * i, b_tail(bcur[i], 8 * i, rl));
           } else {
-            o += dot_zb_mem<false>(zs + q * r, brow(s_key[q]), r);
+            o += dot_zb_mem<false>(zs + q * r, brow(s_key[q]), adapter_rank(ranks, (s_key[q] & 0xffff) - 1, r, nullptr));
           }
         }
         acc = fmaf(s_w[q], o, acc);
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(kExpandThreads)
                               const int* __restrict__ row_expert,
                               const int* __restrict__ row_adapter, int I, int r, int E,
                               const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
-                              int early, int zstride, int zu_off) {
+                              int early, int zstride, int zu_off, const int* __restrict__ ranks) {
   if (!early) pdl_wait();
   const int row = blockIdx.x;
   const int n = blockIdx.y * kExpandThreads + threadIdx.x;
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(kExpandThreads)
   }
   const bool active = row < n_valid;
   const bool lora = active && l >= 0;  // uniform over the CTA
+  const int rl = lora ? adapter_rank(ranks, l, r, hdr) : r;  // B columns past it are not used
   uint4 bg[RV], bu[RV];
 #pragma unroll
   for (int i = 0; i < RV; ++i) bg[i] = bu[i] = make_uint4(0, 0, 0, 0);
@@ -382,8 +389,8 @@ __global__ void __launch_bounds__(kExpandThreads)
     const uint4* pu = reinterpret_cast<const uint4*>(bl + (size_t)(I + n) * r);
 #pragma unroll
     for (int i = 0; i < RV; ++i) {
-      bg[i] = __ldg(pg + i);
-      bu[i] = __ldg(pu + i);
+      bg[i] = b_group(pg, i, rl);
+      bu[i] = b_group(pu, i, rl);
     }
   }
   if (early) pdl_wait();
@@ -411,8 +418,8 @@ __global__ void __launch_bounds__(kExpandThreads)
         zv[c] = __shfl_sync(0xffffffffu, zl[(8 * i + c) >> 5], (8 * i + c) & 31);
         zw[c] = kTwo ? __shfl_sync(0xffffffffu, zul[(8 * i + c) >> 5], (8 * i + c) & 31) : zv[c];
       }
-      fma8(g, zv, bg[i]);
-      fma8(u, zw, bu[i]);
+      fma8(g, zv, b_tail(bg[i], 8 * i, rl));
+      fma8(u, zw, b_tail(bu[i], 8 * i, rl));
     }
   }
   if (col) h[(size_t)row * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
@@ -475,11 +482,25 @@ struct ZFrag {
   }
 };
 
-// The B fragment of chunk c for this lane (zeros past the rank or the last column).
-__device__ __forceinline__ uint4 b_frag(const __nv_bfloat16* brow, int c, int r) {
+// The B fragment of chunk c for this lane (zeros past the adapter's rank rv or the last
+// column; 16-byte groups wholly past rv are not read).
+__device__ __forceinline__ uint4 b_frag(const __nv_bfloat16* brow, int c, int rv) {
   const int k0 = 32 * c + 8 * (threadIdx.x & 3);
-  if (!brow || k0 >= r) return make_uint4(0, 0, 0, 0);
-  return __ldg(reinterpret_cast<const uint4*>(brow + k0));
+  if (!brow || k0 >= rv) return make_uint4(0, 0, 0, 0);
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(brow + k0));
+  return u;  // entries past rv of a partial group: cleared with b_frag_mask where consumed
+}
+// Per-lane AND masks that clear a fragment's entries past rv (all ones unless this lane's
+// 8-rank group of chunk c is the partial one); built once per block, applied with and4.
+__device__ __forceinline__ uint4 b_frag_mask(int c, int rv) {
+  const int v = rv - (32 * c + 8 * (threadIdx.x & 3));
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = 2 * i + 1 < v ? 0xFFFFFFFFu : (2 * i < v ? 0x0000FFFFu : 0u);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint4 and4(uint4 a, uint4 m) {
+  return make_uint4(a.x & m.x, a.y & m.y, a.z & m.z, a.w & m.w);
 }
 
 template <int KC>
@@ -499,14 +520,16 @@ __device__ __forceinline__ void block_mma(float (&acc)[4], const ZFrag<KC>& z, c
 // epilogue 1 with tensor cores. CTAs [0, max_blocks): one LoRA block each, all
 // columns; CTAs beyond: (token tile, 512-column chunk) pairs applying the plain
 // SwiGLU to the tile's rows without adapter.
-template <int KC, bool kTwo>  // kTwo: separate gate and up adapters (two z slices)
+// kTwo: separate gate and up adapters (two z slices); kRanked: adapters of their own ranks
+template <int KC, bool kTwo, bool kRanked>
 __global__ void __launch_bounds__(kExpandThreads)
     expand_swiglu_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                              const int* __restrict__ hdr, const int4* __restrict__ blocks,
                              const int4* __restrict__ tiles, const int* __restrict__ sorted_slots,
                              const int* __restrict__ row_adapter, int I, int r, int E,
                              const float* __restrict__ G, __nv_bfloat16* __restrict__ h,
-                             int max_blocks, int col_chunks, int early, int zstride, int zu_off) {
+                             int max_blocks, int col_chunks, int early, int zstride, int zu_off,
+                             const int* __restrict__ ranks) {
   constexpr int kWarps = kExpandThreads / 32;
   constexpr int kChunk = 2 * kExpandThreads;  // columns per plain-SwiGLU CTA
   __shared__ int s_flag[256];
@@ -526,6 +549,10 @@ __global__ void __launch_bounds__(kExpandThreads)
     const int4 blk = __ldcg(blocks + b);
     const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
     const __nv_bfloat16* bl = B + ((size_t)l * E + e) * twoI * (size_t)r;
+    const int rl = kRanked ? adapter_rank(ranks, l, r, hdr) : r;  // z and B past it unused
+    uint4 bmask[KC];
+#pragma unroll
+    for (int c = 0; c < KC; ++c) bmask[c] = kRanked ? b_frag_mask(c, rl) : make_uint4(0, 0, 0, 0);
     // this CTA's 8-column tiles: [t_begin, t_end)
     const int all_tiles = (I + 7) / 8;
     const int per = (all_tiles + col_chunks - 1) / col_chunks;
@@ -542,8 +569,8 @@ __global__ void __launch_bounds__(kExpandThreads)
       const int nl = t * 8 + gid;
 #pragma unroll
       for (int c = 0; c < KC; ++c) {
-        bg[c] = b_frag(nl < I ? bl + (size_t)nl * r : nullptr, c, r);
-        bu[c] = b_frag(nl < I ? bl + (size_t)(I + nl) * r : nullptr, c, r);
+        bg[c] = b_frag(nl < I ? bl + (size_t)nl * r : nullptr, c, rl);
+        bu[c] = b_frag(nl < I ? bl + (size_t)(I + nl) * r : nullptr, c, rl);
       }
     };
     // shared memory: z of the gate columns, z of the up columns, then the G ring
@@ -567,8 +594,8 @@ __global__ void __launch_bounds__(kExpandThreads)
     if (early) pdl_wait();
     pdl_trigger();
     __nv_bfloat16* zbu = zb + zsmem_bytes(KC) / sizeof(__nv_bfloat16);
-    stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad, zstride, 0);
-    if (kTwo) stage_z_split(zbu, Z, sorted_slots, row0, rows, r, r_pad, zstride, zu_off);
+    stage_z_split(zb, Z, sorted_slots, row0, rows, rl, r_pad, zstride, 0);
+    if (kTwo) stage_z_split(zbu, Z, sorted_slots, row0, rows, rl, r_pad, zstride, zu_off);
     __syncthreads();
     ZFrag<KC> z, z2;
     z.load(zb, r_pad);
@@ -585,6 +612,13 @@ __global__ void __launch_bounds__(kExpandThreads)
         tu[c] = bu[c];
       }
       if (t + kWarps < ntiles) fetch_b(t + kWarps);  // next tile's B in flight
+      if (kRanked) {
+#pragma unroll
+        for (int c = 0; c < KC; ++c) {  // entries past the adapter's rank
+          tg[c] = and4(tg[c], bmask[c]);
+          tu[c] = and4(tu[c], bmask[c]);
+        }
+      }
       float dg[4], du[4];
       block_mma<KC>(dg, z, tg);
       block_mma<KC>(du, zu, tu);
@@ -650,12 +684,13 @@ __global__ void __launch_bounds__(kExpandThreads)
 // before any is reduced, so each warp keeps several KB of the read-modify-write
 // in flight (base is two or more launches old: with `early` the first batch goes
 // out before the wait).
-template <int KC>
+template <int KC, bool kRanked>  // kRanked: adapters of their own ranks
 __global__ void __launch_bounds__(kExpandThreads)
     expand_add_mma_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                           const int* __restrict__ hdr, const int4* __restrict__ blocks,
                           const int* __restrict__ sorted_slots, int N, int r, int E,
-                          float* __restrict__ base, int col_chunks, int early) {
+                          float* __restrict__ base, int col_chunks, int early,
+                          const int* __restrict__ ranks) {
   constexpr int kWarps = kExpandThreads / 32;
   constexpr int TB = 8 / KC > 1 ? 8 / KC : 1;  // tiles per batch
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -672,6 +707,10 @@ __global__ void __launch_bounds__(kExpandThreads)
   }
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
   const __nv_bfloat16* bl = B + ((size_t)l * E + e) * (size_t)N * r;
+  const int rl = kRanked ? adapter_rank(ranks, l, r, hdr) : r;  // z and B past it unused
+  uint4 bmask[KC];
+#pragma unroll
+  for (int c = 0; c < KC; ++c) bmask[c] = kRanked ? b_frag_mask(c, rl) : make_uint4(0, 0, 0, 0);
   const int all_tiles = (N + 7) / 8;
   const int per = (all_tiles + col_chunks - 1) / col_chunks;
   const int t_begin = chunk * per;
@@ -686,7 +725,7 @@ __global__ void __launch_bounds__(kExpandThreads)
       const bool tv = t < ntiles;
 #pragma unroll
       for (int c = 0; c < KC; ++c)
-        bf[j][c] = b_frag(tv && nl < N ? bl + (size_t)nl * r : nullptr, c, r);
+        bf[j][c] = b_frag(tv && nl < N ? bl + (size_t)nl * r : nullptr, c, rl);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int m = gid + 8 * half;
@@ -700,7 +739,7 @@ __global__ void __launch_bounds__(kExpandThreads)
   if (early && t0 < ntiles) fetch(t0);
   if (early) pdl_wait();
   pdl_trigger();
-  stage_z_split(zb, Z, sorted_slots, row0, rows, r, r_pad);
+  stage_z_split(zb, Z, sorted_slots, row0, rows, rl, r_pad, r, 0);
   __syncthreads();
   ZFrag<KC> z;
   z.load(zb, r_pad);
@@ -712,7 +751,10 @@ __global__ void __launch_bounds__(kExpandThreads)
       const int n = t * 8 + 2 * q;
       if (t >= ntiles || n >= N) continue;
       float d[4];
-      block_mma<KC>(d, z, bf[j]);
+      uint4 bt[KC];
+#pragma unroll
+      for (int c = 0; c < KC; ++c) bt[c] = kRanked ? and4(bf[j][c], bmask[c]) : bf[j][c];
+      block_mma<KC>(d, z, bt);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int m = gid + 8 * half;
@@ -810,6 +852,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   const int epilogue = epilogue_in == 3 ? 1 : epilogue_in;
   const int zstride = epilogue_in == 3 ? 2 * r : r, zu_off = epilogue_in == 3 ? r : 0;
   AlignView v = align_view(al->buf, a);
+  const int* ranks = al->L > 0 ? al->adapter_ranks : nullptr;
   const auto* Bp = (al->L > 0) ? static_cast<const __nv_bfloat16*>(B) : nullptr;
   const int rv = Bp ? reg_ranks(r, B) : 1;
   const int rr = Bp ? r : 0;
@@ -837,13 +880,17 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     auto go = [&](auto kern) {
       return launch_pdl(kern, grid, kExpandThreads, zsmem, stream, pdl, Z, Bp, (const int*)v.hdr,
                         (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base, cc,
-                        ea);
+                        ea, ranks);
     };
-    switch (kcp) {
-      case 1: return go(expand_add_mma_kernel<1>);
-      case 2: return go(expand_add_mma_kernel<2>);
-      case 4: return go(expand_add_mma_kernel<4>);
-      default: return go(expand_add_mma_kernel<8>);
+    switch (kcp * 2 + (ranks ? 1 : 0)) {
+      case 2: return go(expand_add_mma_kernel<1, false>);
+      case 3: return go(expand_add_mma_kernel<1, true>);
+      case 4: return go(expand_add_mma_kernel<2, false>);
+      case 5: return go(expand_add_mma_kernel<2, true>);
+      case 8: return go(expand_add_mma_kernel<4, false>);
+      case 9: return go(expand_add_mma_kernel<4, true>);
+      case 16: return go(expand_add_mma_kernel<8, false>);
+      default: return go(expand_add_mma_kernel<8, true>);
     }
   };
   if (epilogue == 0 && mma_ok) return add_mma(dim3(a.max_blocks));
@@ -862,14 +909,13 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     if (dev < 64 && !configured[dev]) {
       const int lim = (int)(2 * zsmem_bytes(8) + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float));
       const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<1, false>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<2, false>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<4, false>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<8, false>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<1, true>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<2, true>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<4, true>, attr, lim));
-      ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<8, true>, attr, lim));
+#define ML_SWIGLU_ATTR(KC_)                                                                  \
+  ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, false, false>, attr, lim)); \
+  ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, true, false>, attr, lim));  \
+  ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, false, true>, attr, lim));  \
+  ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, true, true>, attr, lim));
+      ML_SWIGLU_ATTR(1) ML_SWIGLU_ATTR(2) ML_SWIGLU_ATTR(4) ML_SWIGLU_ATTR(8)
+#undef ML_SWIGLU_ATTR
       configured[dev] = 1;
     }
     auto go = [&](auto kern) -> int {
@@ -877,18 +923,26 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
                         (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
                         (const int*)v.sorted_slots, (const int*)v.row_adapter, I, r, al->E,
                         (const float*)base, static_cast<__nv_bfloat16*>(out), a.max_blocks, cc,
-                        ea, Bp ? zstride : 0, Bp ? zu_off : 0);
+                        ea, Bp ? zstride : 0, Bp ? zu_off : 0, ranks);
     };
-    const bool two = Bp && zu_off != 0;
-    switch ((Bp ? kcp : 1) * 2 + (two ? 1 : 0)) {
-      case 2: return go(expand_swiglu_mma_kernel<1, false>);
-      case 3: return go(expand_swiglu_mma_kernel<1, true>);
-      case 4: return go(expand_swiglu_mma_kernel<2, false>);
-      case 5: return go(expand_swiglu_mma_kernel<2, true>);
-      case 8: return go(expand_swiglu_mma_kernel<4, false>);
-      case 9: return go(expand_swiglu_mma_kernel<4, true>);
-      case 16: return go(expand_swiglu_mma_kernel<8, false>);
-      default: return go(expand_swiglu_mma_kernel<8, true>);
+    const bool two = Bp && zu_off != 0, rk = Bp && ranks;
+    switch ((Bp ? kcp : 1) * 4 + (two ? 2 : 0) + (rk ? 1 : 0)) {
+      case 4: return go(expand_swiglu_mma_kernel<1, false, false>);
+      case 5: return go(expand_swiglu_mma_kernel<1, false, true>);
+      case 6: return go(expand_swiglu_mma_kernel<1, true, false>);
+      case 7: return go(expand_swiglu_mma_kernel<1, true, true>);
+      case 8: return go(expand_swiglu_mma_kernel<2, false, false>);
+      case 9: return go(expand_swiglu_mma_kernel<2, false, true>);
+      case 10: return go(expand_swiglu_mma_kernel<2, true, false>);
+      case 11: return go(expand_swiglu_mma_kernel<2, true, true>);
+      case 16: return go(expand_swiglu_mma_kernel<4, false, false>);
+      case 17: return go(expand_swiglu_mma_kernel<4, false, true>);
+      case 18: return go(expand_swiglu_mma_kernel<4, true, false>);
+      case 19: return go(expand_swiglu_mma_kernel<4, true, true>);
+      case 32: return go(expand_swiglu_mma_kernel<8, false, false>);
+      case 33: return go(expand_swiglu_mma_kernel<8, false, true>);
+      case 34: return go(expand_swiglu_mma_kernel<8, true, false>);
+      default: return go(expand_swiglu_mma_kernel<8, true, true>);
     }
   }
   if (epilogue == 0) {
@@ -897,7 +951,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     const size_t smem = (size_t)kMaxBmLora * r * sizeof(float);
     return launch_rv<AddK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
                            (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base,
-                           ea);
+                           ea, ranks);
   }
   if (epilogue == 1) {
     const int I = N / 2;
@@ -915,7 +969,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
         return launch_pdl(kern, g1, kExpandThreads, 0, stream, pdl, Z, Bp, (const int*)v.hdr,
                           (const int*)v.sorted_slots, (const int*)v.row_expert,
                           (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp, ea,
-                          zstride, zu_off);
+                          zstride, zu_off, ranks);
       };
       switch (rv * 2 + (zu_off != 0 ? 1 : 0)) {
         case 2: return go(expand_swiglu_row1_kernel<1, false>);
@@ -934,7 +988,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     return launch_rv<SwigluK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
                               (const int*)v.sorted_slots, (const int*)v.row_expert,
                               (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp,
-                              rpc, ea, zs_rows, Bp ? zu_off : 0);
+                              rpc, ea, zs_rows, Bp ? zu_off : 0, ranks);
   }
   if (epilogue == 2 && Bp && (int64_t)a.S >= 2 * (int64_t)al->E * al->L) {
     // several rows per (expert, adapter) pair: apply each B row once per LoRA block
@@ -947,7 +1001,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
       const size_t smem = (size_t)kMaxBmLora * r * sizeof(float);
       st = launch_rv<AddK>(rv, grid, smem, stream, pdl, Z, Bp, (const int*)v.hdr,
                            (const int4*)v.blocks, (const int*)v.sorted_slots, N, r, al->E, base,
-                           ea);
+                           ea, ranks);
     }
     if (st != MOE_LORA_OK) return st;
     const int ncol = ceil_div(N, kExpandThreads);
@@ -975,7 +1029,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
       return launch_pdl(kern, grid, kExpandThreads, smem, stream, pdl, Z, Bp,
                         (const int*)v.slot_row, (const int*)v.row_expert,
                         (const int*)v.row_adapter, topk_w, al->T, al->k, N, r, al->E,
-                        (const float*)base, out, tpc, ea);
+                        (const float*)base, out, tpc, ea, ranks);
     };
     if (out_fp32) {
       switch (rv) {

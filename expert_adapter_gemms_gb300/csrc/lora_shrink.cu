@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
     lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
-                       int K, int r, int E, float* __restrict__ Z, int ngroups, int early) {
+                       int K, int r, int E, float* __restrict__ Z, int ngroups, int early,
+                       const int* __restrict__ ranks, int rs) {
   constexpr int R = 8 * NT;  // ranks per CTA
   constexpr int XB = kSmallM ? 1 : U;  // kSmallM: blocks of at most 8 rows, no second row set
   __shared__ float red[kShrinkWarps][16][R + 1];
@@ -88,11 +89,14 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
   const int slot0 = (int)threadIdx.x < rows * R ? __ldcg(sorted_slots + row0 + threadIdx.x / R) : 0;
 
   const __nv_bfloat16* Ab = A + ((size_t)l * E + e) * (size_t)r * K;
+  // rank rows past the adapter's own rank (per slice of rs rows) are not read: their z is 0
+  const int rl = adapter_rank(ranks, l, rs, hdr);
+  const unsigned long long vmask = rank_row_mask(g * R, rs, rl);  // R <= 64 rows
   const __nv_bfloat16* ap[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int rank = g * R + nt * 8 + gid;
-    ap[nt] = rank < r ? Ab + (size_t)rank * K : nullptr;
+    ap[nt] = rank < r && ((vmask >> (nt * 8 + gid)) & 1ull) ? Ab + (size_t)rank * K : nullptr;
   }
   const __nv_bfloat16* x0 = nullptr;
   const __nv_bfloat16* x1 = nullptr;
@@ -200,13 +204,13 @@ constexpr int kShortUMax = 4;  // k-steps per warp: K <= 8 warps x 4 x 32 = 1024
 // of a fragment load fall in alternate bank halves
 inline int short_astride(int K) { return (K * 2 + 127) / 128 * 128 + 64; }
 
-template <int NT, bool kEvenK>
+template <int NT, bool kEvenK, bool kRanked>  // kRanked: adapters of their own ranks
 __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
     lora_shrink_smem_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                             const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                             const int4* __restrict__ blocks, const int* __restrict__ sorted_slots,
                             int k, int K, int r, int E, float* __restrict__ Z, int ngroups,
-                            int early, int astride) {
+                            int early, int astride, const int* __restrict__ ranks, int rs) {
   constexpr int R = 8 * NT;
   extern __shared__ __align__(16) uint8_t sA[];  // [R][astride] bytes; reused for the reduction
   if (!early) pdl_wait();
@@ -225,11 +229,15 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
   const int slot0 = (int)threadIdx.x < rows * R ? __ldcg(sorted_slots + row0 + threadIdx.x / R) : 0;
   // the slab: rank rows g R .. g R + nr - 1, 16 bytes per copy
   const int nr = min(R, r - g * R);
+  // rows past the adapter's rank (per slice) are not read
+  const unsigned long long vmask =
+      kRanked ? rank_row_mask(g * R, rs, adapter_rank(ranks, l, rs, hdr)) : ~0ull;  // R <= 64 rows
   const __nv_bfloat16* Ab = A + (((size_t)l * E + e) * r + (size_t)g * R) * K;
   const int cpr = K / 8;
   for (int i = threadIdx.x; i < nr * cpr; i += blockDim.x) {
     const int rho = i / cpr, c = i - rho * cpr;
-    shrink_cp_async16(sA + (size_t)rho * astride + c * 16, Ab + (size_t)rho * K + c * 8);
+    if ((vmask >> rho) & 1ull)
+      shrink_cp_async16(sA + (size_t)rho * astride + c * 16, Ab + (size_t)rho * K + c * 8);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   // activation fragments of this warp's k-steps (rows gid < rows)
@@ -262,7 +270,8 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
     for (int nt = 0; nt < NT; ++nt) {
       const int rho = nt * 8 + gid;
       uint4 av = make_uint4(0, 0, 0, 0);
-      if (rho < nr && kin) av = *reinterpret_cast<const uint4*>(sA + (size_t)rho * astride + k0 * 2);
+      if (rho < nr && ((vmask >> rho) & 1ull) && kin)
+        av = *reinterpret_cast<const uint4*>(sA + (size_t)rho * astride + k0 * 2);
       mma_16816(acc[nt], xa[u].x, 0u, xa[u].y, 0u, av.x, av.y);
       mma_16816(acc[nt], xa[u].z, 0u, xa[u].w, 0u, av.z, av.w);
     }
@@ -296,7 +305,7 @@ template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
                             float* Z, bool vec, cudaStream_t stream, bool pdl, int early,
-                            bool small_m) {
+                            bool small_m, const int* ranks, int rs) {
   const int ngroups = ceil_div(r, 8 * NT);
   const int64_t grid = (int64_t)max_blocks * ngroups;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
@@ -304,7 +313,7 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
   auto args = [&](auto kern) {
     return launch_pdl(kern, g, kShrinkWarps * 32, 0, stream, pdl, X, rows_are_slots, A,
                       (const int*)v.hdr, (const int4*)v.blocks, (const int*)v.sorted_slots, k, K,
-                      r, E, Z, ngroups, early);
+                      r, E, Z, ngroups, early, ranks, rs);
   };
   if (small_m) {
     if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true, true>);
@@ -317,8 +326,9 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
 }
 
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
-                       const moe_lora_align_t* al, const AlignLayout& a, int K, int r, float* Z,
-                       cudaStream_t stream, bool pdl, bool early) {
+                       const moe_lora_align_t* al, const AlignLayout& a, int K, int r, int rs,
+                       float* Z, cudaStream_t stream, bool pdl, bool early) {
+  const int* ranks = al->adapter_ranks;
   if (a.S == 0 || al->L == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   const auto* Xp = static_cast<const __nv_bfloat16*>(X);
@@ -335,8 +345,8 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   else if (r <= 32) nt = 4;
   else nt = 8;
   switch (nt) {
-    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
-    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
+    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
     case 4:  // short blocks: two k-steps per batch, still two CTAs per SM
       if (al->bm_lora <= 8 && vec && K <= 32 * kShrinkWarps * kShortUMax &&
           32 * short_astride(K) <= 56 * 1024) {  // short K: the slab in shared memory
@@ -350,29 +360,33 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
         int dev = 0;
         ML_CHECK_CUDA(cudaGetDevice(&dev));
         if (dev < 64 && !configured[dev]) {
-          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 56 * 1024));
-          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 56 * 1024));
+          const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, false>, attr, 56 * 1024));
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, false>, attr, 56 * 1024));
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, true>, attr, 56 * 1024));
+          ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, true>, attr, 56 * 1024));
           configured[dev] = 1;
         }
         auto go = [&](auto kern) -> int {
           return launch_pdl(kern, dim3((unsigned)grid), kShrinkWarps * 32, smem, stream, pdl, Xp,
                             rows_are_slots, Ap, (const int*)v.hdr, (const int4*)v.blocks,
-                            (const int*)v.sorted_slots, al->k, K, r, al->E, Z, ngroups, ea, astride);
+                            (const int*)v.sorted_slots, al->k, K, r, al->E, Z, ngroups, ea, astride,
+                            ranks, rs);
         };
-        return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true>) : go(lora_shrink_smem_kernel<4, false>);
+        if (ranks)
+          return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true, true>) : go(lora_shrink_smem_kernel<4, false, true>);
+        return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true, false>) : go(lora_shrink_smem_kernel<4, false, false>);
       }
       if (al->bm_lora <= 8)
-        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true);
-      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false);
-    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8);
+        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true, ranks, rs);
+      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false, ranks, rs);
+    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
   }
 }
 
 int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
                   const AlignLayout& a, int K, int r, float* Z, cudaStream_t stream, bool pdl) {
-  return launch_shrink_impl(X, rows_are_slots, A, al, a, K, r, Z, stream, pdl, false);
+  return launch_shrink_impl(X, rows_are_slots, A, al, a, K, r, r, Z, stream, pdl, false);
 }
 
 }  // namespace moe_lora

@@ -71,6 +71,7 @@ enum moe_lora_status {
 #define MOE_LORA_DEVERR_EXPERT_RANGE 0x1u  /* an expert id outside [0, E): slot dropped */
 #define MOE_LORA_DEVERR_ADAPTER_RANGE 0x2u /* an adapter id outside [-1, L): the token's slots dropped */
 #define MOE_LORA_DEVERR_TIMEOUT 0x4u       /* a bounded wait inside a kernel gave up; results invalid */
+#define MOE_LORA_DEVERR_RANK_RANGE 0x8u    /* an adapter rank outside [0, r]: clamped */
 
 /* Human-readable name of a status code (static string). */
 MOE_LORA_API const char* moe_lora_status_string(int status);
@@ -119,6 +120,14 @@ typedef struct moe_lora_align_t {
   int32_t L;       /* resident adapters (0: none) */
   int32_t bm_base; /* rows per grouped-GEMM token tile */
   int32_t bm_lora; /* rows per LoRA block */
+  const int32_t* adapter_ranks; /* optional device array [L]: adapter l has rank r_l in [0, r]
+                     and uses only the first r_l rows of each r-row slice of A and the
+                     first r_l columns of B (storage stays padded to r); NULL: every
+                     adapter has rank r. Used by lora_shrink and lora_expand_add (z
+                     entries past r_l are written as 0); 16-byte groups wholly past r_l
+                     are never read. Values outside [0, r] are clamped and flagged
+                     (MOE_LORA_DEVERR_RANK_RANGE). The pages give one rank per serving
+                     instance; per-adapter ranks are this library's extension. */
 } moe_lora_align_t;
 
 #define MOE_LORA_ALIGN_NFIELDS 12
@@ -233,6 +242,8 @@ typedef struct moe_lora_layer_opts {
                            after the last: [0] route, [1] align, [2] gather, [3] gate_up GEMM,
                            [4] gate_up shrink, [5] gate_up expand+SwiGLU, [6] down GEMM,
                            [7] down shrink, [8] down expand+combine, [9] end */
+  const int32_t* adapter_ranks; /* optional device array [L] of per-adapter ranks (see
+                           moe_lora_align_t.adapter_ranks); NULL: every adapter has rank r */
   int32_t gate_up_slices; /* 0 or 1: one adapter over the fused gate_up output (A1
                            [L,E,r,H]); 2: separate gate and up adapters, A1 [L,E,2r,H]
                            with the gate A in rows [0,r) and the up A in [r,2r), B1

@@ -333,3 +333,81 @@ def test_expand_two_slices(shape, r):
     h.check()
     assert_bf16_close(h.t[:n], oracle.lora_expand_add(Zh, inp.B1, ref, G[:n], epilogue=3),
                       f"epilogue 3, {shape} segments, r={r}")
+
+
+def _poison_A(A, ranks, rank):
+    """A with the rows past each adapter's rank (per slice of `rank` rows) set to NaN."""
+    A = A.clone()
+    for l, rl in enumerate(ranks):
+        for sl in range(A.shape[2] // rank):
+            A[l, :, sl * rank + min(max(rl, 0), rank): (sl + 1) * rank] = float("nan")
+    return A
+
+
+def _poison_B(B, ranks):
+    B = B.clone()
+    for l, rl in enumerate(ranks):
+        B[l, :, :, min(max(rl, 0), B.shape[3]):] = float("nan")
+    return B
+
+
+@pytest.mark.parametrize("case", ["decode", "stress_regs", "stress_smem", "prefill"])
+def test_shrink_adapter_ranks(case):
+    """Adapters of their own ranks (8, 0, 5, 16, full): the rows of A past an adapter's rank
+    hold NaN and must never be used; z past the rank is 0. Every shrink form."""
+    if case == "decode":
+        kw = dict(T=64, H=2880, E=32, k=4, L=8, r=32, bm_lora=8, adapters="round_robin_shuffled")
+    elif case == "stress_regs":
+        kw = dict(T=256, H=2048, E=128, k=8, L=16, r=32, bm_lora=8, adapters="zipf1.1")
+    elif case == "stress_smem":
+        kw = dict(T=256, H=768, E=128, k=8, L=16, r=32, bm_lora=8, adapters="zipf1.1")
+    else:
+        kw = dict(T=1024, H=512, E=8, k=2, L=16, r=16, bm_lora=16, adapters="one_per_request16")
+    m, inp, ids, w, al, ref = _setup(I=8, seed=22, **kw)
+    r = kw["r"]
+    ranks = [[8, 0, 5, 16, r][l % 5] for l in range(kw["L"])]
+    A = _poison_A(inp.A1, ranks, r)
+    rk = torch.as_tensor(ranks, dtype=torch.int32)
+    Z = m.lora_shrink(dev(inp.x), False, dev(A), al, adapter_ranks=dev(rk))
+    expect = oracle.lora_shrink(inp.x, A, ref, False, adapter_ranks=rk)
+    assert not torch.isnan(Z).any()
+    assert_close(Z, expect, KERNEL_RTOL, f"ranked shrink, {case}")
+    assert m.get_error(al.buf) == 0
+
+
+@pytest.mark.parametrize("epilogue", [0, 1, 2, 3])
+@pytest.mark.parametrize("seg", ["short", "long"])
+@pytest.mark.parametrize("r", [16, 64, 5])
+def test_expand_adapter_ranks(epilogue, seg, r):
+    """The expand with adapters of their own ranks: B columns past an adapter's rank hold NaN
+    and must never be used (z there is arbitrary); every epilogue on the CUDA-core forms
+    (short segments, r = 5) and the tensor-core forms (long segments)."""
+    if seg == "short":
+        T, H, I, E, k, L, adapters = 48, 96, 80, 32, 4, 8, "round_robin_shuffled"
+    else:
+        T, H, I, E, k, L, adapters = 512, 96, 80, 4, 2, 5, "uniform_with_none"
+    m, inp, ids, w, al, ref = _setup(T=T, H=H, I=I, E=E, k=k, L=L, r=r, seed=23, adapters=adapters)
+    n = ref["n_valid"]
+    ranks = [[r, 0, min(8, r), 3, max(r - 1, 0)][l % 5] for l in range(L)]
+    rk = torch.as_tensor(ranks, dtype=torch.int32)
+    rng = np.random.default_rng(11)
+    zc = 2 * r if epilogue == 3 else r
+    Zh = torch.from_numpy(rng.standard_normal((al.S, zc))).to(torch.float32)
+    if epilogue == 2:
+        B = _poison_B(inp.B2, ranks)
+        O = torch.from_numpy(rng.standard_normal((al.S, H), dtype=np.float32))
+        wt = torch.as_tensor(w, dtype=torch.float32)
+        y = m.lora_expand_add(dev(Zh), dev(B), al, 2, dev(O), out_fp32=True, topk_w=dev(wt),
+                              adapter_ranks=dev(rk))
+        expect = oracle.lora_expand_add(Zh, B, ref, O[:n], epilogue=2, w=wt, adapter_ranks=rk)
+        assert_close(y, expect, KERNEL_RTOL, f"ranked epilogue 2, {seg}, r={r}")
+        return
+    B = _poison_B(inp.B1 if epilogue else inp.B2, ranks)
+    N = B.shape[2]
+    G = torch.from_numpy(rng.standard_normal((al.S, N), dtype=np.float32))
+    out = m.lora_expand_add(dev(Zh), dev(B), al, epilogue, dev(G), adapter_ranks=dev(rk))
+    expect = oracle.lora_expand_add(Zh, B, ref, G[:n], epilogue=epilogue, adapter_ranks=rk)
+    if epilogue == 0:
+        assert_close(out[:n], expect, KERNEL_RTOL, f"ranked epilogue 0, {seg}, r={r}")
+    else:
+        assert_bf16_close(out[:n], expect, f"ranked epilogue {epilogue}, {seg}, r={r}")

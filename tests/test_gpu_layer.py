@@ -241,3 +241,65 @@ def test_layer_two_slice_gate_up(shape):
     ref = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, A1s, inp.B1,
                                 inp.A2, inp.B2, gate_up_slices=2)
     assert_close(y.t.cpu(), ref, LAYER_RTOL, f"two-slice gate_up, {shape}")
+
+
+@pytest.mark.parametrize("shape", ["decode", "prefill_like", "stress_like"])
+@pytest.mark.parametrize("slices", [1, 2])
+def test_layer_adapter_ranks(shape, slices):
+    """Adapters of their own ranks through the whole layer, with the padding of every A and B
+    past an adapter's rank holding NaN (never used), one or two gate_up slices."""
+    m = need_gpu()
+    if shape == "decode":
+        kw = dict(T=64, H=512, I=384, E=32, k=4, L=8, r=32, adapters="round_robin_shuffled")
+    elif shape == "prefill_like":
+        kw = dict(T=1024, H=256, I=256, E=8, k=2, L=16, r=16, adapters="one_per_request16")
+    else:
+        kw = dict(T=256, H=256, I=128, E=64, k=8, L=32, r=32, adapters="zipf1.1")
+    inp = make_layer_inputs(seed=33, lora_std=None, **kw)
+    r, L = kw["r"], kw["L"]
+    ranks = [[r, 8, 0, r // 2, 5][l % 5] for l in range(L)]
+    rng = np.random.default_rng(34)
+    A1 = torch.from_numpy(rng.standard_normal((L, inp.E, slices * r, inp.H)).astype(np.float32)
+                          * 0.05).to(torch.bfloat16)
+
+    def poison(t, rank_dim_rows):
+        t = t.clone()
+        for l, rl in enumerate(ranks):
+            if rank_dim_rows:
+                for sl in range(t.shape[2] // r):
+                    t[l, :, sl * r + rl: (sl + 1) * r] = float("nan")
+            else:
+                t[l, :, :, rl:] = float("nan")
+        return t
+
+    A1p, B1p = poison(A1, True), poison(inp.B1, False)
+    A2p, B2p = poison(inp.A2, True), poison(inp.B2, False)
+    rk = torch.as_tensor(ranks, dtype=torch.int32)
+    ws = m.new_workspace(inp.T, inp.k, inp.E, L, inp.H, inp.I, r)
+    y = Guarded((inp.T, inp.H), torch.bfloat16)
+    m.moe_lora_layer(dev(inp.x), dev(inp.W1), dev(inp.W2), logits=dev(inp.logits), k=inp.k,
+                     token_adapter=dev(inp.token_adapter), y=y.t, A1=dev(A1p), B1=dev(B1p),
+                     A2=dev(A2p), B2=dev(B2p), gate_up_slices=slices, adapter_ranks=dev(rk),
+                     workspace=ws)
+    y.check()
+    assert m.get_error(ws) == 0
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    tok = np.arange(min(inp.T, 64))
+    ref = oracle.moe_lora_layer(inp.x[tok], inp.W1, inp.W2, ids[tok], w[tok], inp.token_adapter[tok],
+                                A1p, B1p, A2p, B2p, gate_up_slices=slices, adapter_ranks=rk)
+    assert not torch.isnan(y.t).any()
+    assert_close(y.t.cpu()[tok], ref, LAYER_RTOL, f"ranked adapters, {shape}, slices={slices}")
+
+
+def test_layer_adapter_rank_out_of_range_flagged():
+    """A rank outside [0, r] is clamped and flagged in the error word."""
+    m = need_gpu()
+    inp = make_layer_inputs(T=8, H=128, I=128, E=4, k=2, L=2, r=8, seed=35, adapters="tiny")
+    ws = m.new_workspace(inp.T, inp.k, inp.E, 2, inp.H, inp.I, 8)
+    rk = torch.as_tensor([12, -1], dtype=torch.int32)
+    y = run_layer(m, inp, workspace=ws, adapter_ranks=dev(rk))
+    assert m.get_error(ws) & 0x8
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    ref = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, inp.A1, inp.B1,
+                                inp.A2, inp.B2, adapter_ranks=torch.as_tensor([8, 0]))
+    assert_close(y.cpu(), ref, LAYER_RTOL, "clamped ranks")
