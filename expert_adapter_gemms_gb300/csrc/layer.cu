@@ -258,7 +258,9 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, L > 0 && slices == 2 ? 3 : 1, G, h, 0,
                              nullptr, stream, pdl, pdl && L > 0));
   ML_STEP(mark(6));
-  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, 0));
+  // the down GEMM likewise runs expert-major when experts hold few rows: its weights stream
+  // while the SwiGLU expand drains
+  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, em_bn));
   ML_STEP(mark(7));
   if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, pdl));
   ML_STEP(mark(8));
