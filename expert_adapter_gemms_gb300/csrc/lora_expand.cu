@@ -353,7 +353,8 @@ __global__ void __launch_bounds__(kExpandThreads)
 // barrier for another thread's table reads; the one barrier stages z (r floats)
 // after the B rows are in flight.
 // ----------------------------------------------------------------------------
-template <int RV, bool kTwo>  // kTwo: separate gate and up adapters (two z slices)
+// kTwo: separate gate and up adapters (two z slices); kRanked: adapters of their own ranks
+template <int RV, bool kTwo, bool kRanked>
 __global__ void __launch_bounds__(kExpandThreads)
     expand_swiglu_row1_kernel(const float* __restrict__ Z, const __nv_bfloat16* __restrict__ B,
                               const int* __restrict__ hdr, const int* __restrict__ sorted_slots,
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kExpandThreads)
   }
   const bool active = row < n_valid;
   const bool lora = active && l >= 0;  // uniform over the CTA
-  const int rl = lora ? adapter_rank(ranks, l, r, hdr) : r;  // B columns past it are not used
+  const int rl = kRanked && lora ? adapter_rank(ranks, l, r, hdr) : r;  // B columns past it unused
   uint4 bg[RV], bu[RV];
 #pragma unroll
   for (int i = 0; i < RV; ++i) bg[i] = bu[i] = make_uint4(0, 0, 0, 0);
@@ -418,8 +419,8 @@ __global__ void __launch_bounds__(kExpandThreads)
         zv[c] = __shfl_sync(0xffffffffu, zl[(8 * i + c) >> 5], (8 * i + c) & 31);
         zw[c] = kTwo ? __shfl_sync(0xffffffffu, zul[(8 * i + c) >> 5], (8 * i + c) & 31) : zv[c];
       }
-      fma8(g, zv, b_tail(bg[i], 8 * i, rl));
-      fma8(u, zw, b_tail(bu[i], 8 * i, rl));
+      fma8(g, zv, kRanked ? b_tail(bg[i], 8 * i, rl) : bg[i]);
+      fma8(u, zw, kRanked ? b_tail(bu[i], 8 * i, rl) : bu[i]);
     }
   }
   if (col) h[(size_t)row * I + n] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
@@ -971,15 +972,23 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
                           (const int*)v.row_adapter, I, r, al->E, (const float*)base, hp, ea,
                           zstride, zu_off, ranks);
       };
-      switch (rv * 2 + (zu_off != 0 ? 1 : 0)) {
-        case 2: return go(expand_swiglu_row1_kernel<1, false>);
-        case 3: return go(expand_swiglu_row1_kernel<1, true>);
-        case 4: return go(expand_swiglu_row1_kernel<2, false>);
-        case 5: return go(expand_swiglu_row1_kernel<2, true>);
-        case 8: return go(expand_swiglu_row1_kernel<4, false>);
-        case 9: return go(expand_swiglu_row1_kernel<4, true>);
-        case 16: return go(expand_swiglu_row1_kernel<8, false>);
-        default: return go(expand_swiglu_row1_kernel<8, true>);
+      switch (rv * 4 + (zu_off != 0 ? 2 : 0) + (ranks ? 1 : 0)) {
+        case 4: return go(expand_swiglu_row1_kernel<1, false, false>);
+        case 5: return go(expand_swiglu_row1_kernel<1, false, true>);
+        case 6: return go(expand_swiglu_row1_kernel<1, true, false>);
+        case 7: return go(expand_swiglu_row1_kernel<1, true, true>);
+        case 8: return go(expand_swiglu_row1_kernel<2, false, false>);
+        case 9: return go(expand_swiglu_row1_kernel<2, false, true>);
+        case 10: return go(expand_swiglu_row1_kernel<2, true, false>);
+        case 11: return go(expand_swiglu_row1_kernel<2, true, true>);
+        case 16: return go(expand_swiglu_row1_kernel<4, false, false>);
+        case 17: return go(expand_swiglu_row1_kernel<4, false, true>);
+        case 18: return go(expand_swiglu_row1_kernel<4, true, false>);
+        case 19: return go(expand_swiglu_row1_kernel<4, true, true>);
+        case 32: return go(expand_swiglu_row1_kernel<8, false, false>);
+        case 33: return go(expand_swiglu_row1_kernel<8, false, true>);
+        case 34: return go(expand_swiglu_row1_kernel<8, true, false>);
+        default: return go(expand_swiglu_row1_kernel<8, true, true>);
       }
     }
     const dim3 grid(ceil_div(a.S, rpc), ncol);

@@ -183,6 +183,7 @@ MOE_LORA_API int moe_grouped_gemm(const void* a, const void* W, const moe_lora_a
  * rows_are_slots = 1: in(s) = slot_row[s], X is [S, K] (sorted rows, e.g. the
  *                     SwiGLU output feeding the down projection).
  * A [L, E, r, K] bf16; Z [S, r] fp32 (slots without adapter untouched).
+ * With al->adapter_ranks, adapter l uses rows [0, r_l) of A and Z[s, i >= r_l] = 0.
  * Any K >= 1 and 1 <= r <= 256; K % 8 == 0 with 16-byte aligned X and A takes the
  * 128-bit load path, and K % 32 == 0 also drops the bounds masks (EVEN_K).
  * Deterministic (fixed-order reductions, no atomics).
@@ -193,7 +194,7 @@ MOE_LORA_API int lora_shrink(const void* X, int rows_are_slots, const void* A, c
 /* ---------------------------------------------------------------------------
  * LoRA expand with the base add fused in (vllm.com.cn, section "Kernel
  * optimizations": the LoRA result is added to the base output inside the expand
- * kernel), plus the layer's two epilogues:
+ * kernel), plus the layer's epilogues:
  *   delta[row, n] = sum_i Z[s, i] * B[l, e, n, i]      (rows with an adapter)
  *   epilogue 0: base[row, n] += delta[row, n]           in place, fp32 [S, N]
  *   epilogue 1: out[row, n] = silu(g) * u with g = base[row, n] + delta[row, n],
@@ -202,10 +203,11 @@ MOE_LORA_API int lora_shrink(const void* X, int rows_are_slots, const void* A, c
  *   epilogue 2: out[t, n] = sum_j w[t, j] * (base[row(t,j), n] + delta[row(t,j), n]),
  *               j in increasing order; out [T, N] bf16 (out_fp32 = 0) or fp32.
  *               base is only read.
- * Z [S, r] fp32; B [L, E, N, r] bf16 (NULL or L = 0: no adapter term);
  *   epilogue 3: as epilogue 1 with separate gate and up adapters: Z rows hold 2r
  *               values, columns [0, N/2) take z[0, r) and B rows [0, N/2), columns
  *               [N/2, N) take z[r, 2r) and B rows [N/2, N); B stays [L, E, N, r].
+ * Z [S, r] fp32 ([S, 2r] for epilogue 3); B [L, E, N, r] bf16 (NULL or L = 0: no
+ * adapter term). With al->adapter_ranks, adapter l uses columns [0, r_l) of B only.
  * topk_w [T, k] fp32 (epilogue 2 only). Requires L < 65535. Deterministic.
  * ------------------------------------------------------------------------- */
 MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_align_t* al, int N, int r,
