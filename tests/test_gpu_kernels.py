@@ -291,6 +291,22 @@ def test_shrink_short_blocks_all_ranks(K, r):
                  f"sorted rows K={K} r={r}")
 
 
+@pytest.mark.parametrize("K", [768, 136])
+def test_shrink_short_blocks_fewer_items_than_ctas(K):
+    """The short-K shrink's grid covers the host's block bound (~1000 here): with one adapter
+    (a third of the tokens without one) only ~135 blocks are live, so most CTAs find no
+    block and leave before any copy."""
+    T = 128
+    adapters = np.where(np.arange(T) % 3 == 0, -1, 0).astype(np.int32)
+    m, inp, ids, w, al, ref = _setup(T=T, H=K, I=8, E=128, k=8, L=16, r=32, seed=23,
+                                     bm_lora=8, adapters=adapters)
+    assert len(ref["lora_blocks"]) < 304
+    Z = Guarded((al.S, 32), torch.float32, fill=0.0)
+    m.lora_shrink(dev(inp.x), False, dev(inp.A1), al, out=Z.t)
+    Z.check()
+    assert_close(Z.t, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"K={K}")
+
+
 @pytest.mark.parametrize("I", [300, 302, 1024])
 @pytest.mark.parametrize("r", [16, 64])
 def test_expand_swiglu_long_segments_ragged(I, r):
