@@ -187,15 +187,20 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
 // Short K, short blocks, all ranks of a block in one CTA (the many-adapter shape's
 // down shrink: K = 768, r = 32, thousands of blocks of one or two rows). Register
 // loads cap the bytes a CTA keeps in flight and, at 124 registers, the CTAs per SM;
-// here the block's A slab (8 NT rows x K) lands in shared memory through 16-byte
-// asynchronous copies, only the activation fragments sit in registers, and four
-// CTAs fit an SM. The same mma.sync products and fixed-order warp reduction (done in
-// the slab's space once the products are formed) as the kernel above.
+// here the block's A slab (8 NT rows x K) lands in shared memory through one bulk copy
+// per rank row (the copy engine, not the load/store path), only the activation
+// fragments sit in registers, and four CTAs fit an SM. The same mma.sync products and
+// fixed-order warp reduction (done in the slab's space once the products are formed)
+// as the kernel above.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void shrink_cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-               "l"(reinterpret_cast<uint64_t>(src))
-               : "memory");
+// One contiguous global -> shared copy by the bulk-copy (TMA) engine, completing on an
+// mbarrier; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 constexpr int kShortUMax = 4;  // k-steps per warp: K <= 8 warps x 4 x 32 = 1024
@@ -212,7 +217,9 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
                             int k, int K, int r, int E, float* __restrict__ Z, int ngroups,
                             int early, int astride, const int* __restrict__ ranks, int rs) {
   constexpr int R = 8 * NT;
+  static_assert(R == 32, "one rank row per lane of warp 0");
   extern __shared__ __align__(16) uint8_t sA[];  // [R][astride] bytes; reused for the reduction
+  __shared__ uint64_t bar;                       // the slab's copies complete here
   if (!early) pdl_wait();
   const int b = blockIdx.x / ngroups;
   const int g = blockIdx.x - b * ngroups;
@@ -232,14 +239,21 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
   // rows past the adapter's rank (per slice) are not read
   const unsigned long long vmask =
       kRanked ? rank_row_mask(g * R, rs, adapter_rank(ranks, l, rs, hdr)) : ~0ull;  // R <= 64 rows
+  // one bulk copy per rank row (2K bytes: K % 8 == 0 and 16-byte aligned bases, checked
+  // on the host), issued by lane rho of warp 0 and completing on one mbarrier
   const __nv_bfloat16* Ab = A + (((size_t)l * E + e) * r + (size_t)g * R) * K;
-  const int cpr = K / 8;
-  for (int i = threadIdx.x; i < nr * cpr; i += blockDim.x) {
-    const int rho = i / cpr, c = i - rho * cpr;
-    if ((vmask >> rho) & 1ull)
-      shrink_cp_async16(sA + (size_t)rho * astride + c * 16, Ab + (size_t)rho * K + c * 8);
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_init(&bar, 1);
+      fence_barrier_init();
+    }
+    __syncwarp();
+    const bool take = lane < nr && ((vmask >> lane) & 1ull);
+    const unsigned tk = __ballot_sync(0xffffffffu, take);
+    if (lane == 0) mbar_arrive_expect_tx(&bar, (uint32_t)__popc(tk) * (uint32_t)(2 * K));
+    __syncwarp();
+    if (take) bulk_g2s(sA + (size_t)lane * astride, Ab + (size_t)lane * K, (uint32_t)(2 * K), &bar);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
   // activation fragments of this warp's k-steps (rows gid < rows)
   const int nsteps = (K + 31) >> 5;
   const __nv_bfloat16* x0 = nullptr;
@@ -255,8 +269,11 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
     xa[u] = make_uint4(0, 0, 0, 0);
     if (x0 && st < nsteps && (kEvenK || k0 < K)) xa[u] = __ldcg(reinterpret_cast<const uint4*>(x0 + k0));
   }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
+  __syncthreads();  // the barrier is initialised before any thread waits on it
+  if (!mbar_wait_bounded(&bar, 0)) {
+    set_dev_error(const_cast<int*>(hdr), MOE_LORA_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&bar, 0);  // copies still in flight land before the slab is reused
+  }
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
