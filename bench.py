@@ -438,20 +438,18 @@ def run_ours(args):
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed steps")
 
-    # end to end through the same public call, inputs from pinned host memory
-    x_h = inp.x.pin_memory()
-    lg_h = inp.logits.pin_memory()
-    ta_h = inp.token_adapter.pin_memory()
-    y_h = torch.empty((inp.T, inp.H), dtype=torch.bfloat16).pin_memory()
-    h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ta_h.numel() * 4
-    d2h = y_h.numel() * 2
+    # end to end through the host-staged C-ABI call: every step copies its inputs (x, logits,
+    # adapter ids) from one page-locked host block and reads y back into host memory
+    io = m.new_host_io(inp.T, inp.H, inp.E, with_adapter=inp.L > 0)
+    io.x.copy_(inp.x)
+    io.logits.copy_(inp.logits)
+    if io.token_adapter is not None:
+        io.token_adapter.copy_(inp.token_adapter)
+    h2d = io.in_bytes
+    d2h = io.y_host.numel() * io.y_host.element_size()
 
     def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        lg_d.copy_(lg_h, non_blocking=True)
-        ta_d.copy_(ta_h, non_blocking=True)
-        step()
-        y_h.copy_(y_d, non_blocking=True)
+        m.moe_lora_layer_host(io, W1, W2, k=inp.k, workspace=ws, **lora)
 
     for _ in range(3):
         e2e_step()
@@ -463,6 +461,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_max, e2e_tokens = combine_ranks(e0.elapsed_time(e1) / 1e3, inp.T * args.steps)
+    if not torch.equal(io.y_host, y_d.cpu()):
+        raise RuntimeError("the host-staged step's y differs from the device-pointer call's")
 
     # per-stage durations (events between the launches; a separate instrumented pass)
     nst = len(STAGES)

@@ -15,6 +15,7 @@ from ._lib import (  # noqa: F401
 )
 from .api import (  # noqa: F401
     Align,
+    HostIO,
     align_layout,
     clear_error,
     get_error,
@@ -23,10 +24,13 @@ from .api import (  # noqa: F401
     moe_gather_rows,
     moe_grouped_gemm,
     moe_lora_align,
+    moe_lora_host_io_layout,
     moe_lora_layer,
+    moe_lora_layer_host,
     moe_lora_layer_tiles,
     moe_lora_workspace_size,
     moe_topk_softmax,
     new_align,
+    new_host_io,
     new_workspace,
 )

@@ -74,6 +74,10 @@ SIGNATURES = {
                                _I, _I, _P, _I, _P, _SZ, ctypes.POINTER(LayerOpts), _P]),
     "moe_lora_layer_tiles": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32),
                                   ctypes.POINTER(ctypes.c_int32)]),
+    "moe_lora_host_io_layout": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int64),
+                                     ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "moe_lora_layer_host": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                 _P, _I, _I, _I, _P, _SZ, ctypes.POINTER(LayerOpts), _P]),
 }
 
 _lock = threading.Lock()

@@ -245,6 +245,46 @@ def new_workspace(T: int, k: int, E: int, L: int, H: int, I: int, r: int, device
     return ws
 
 
+def _layer_weights(H: int, W1, W2, A1, B1, A2, B2, gate_up_slices: int):
+    """Checks the layer's weights against hidden size H; returns (E, I, L, r)."""
+    _need(W1, "W1", torch.bfloat16, 3)
+    _need(W2, "W2", torch.bfloat16, 3)
+    E, twoI, H1 = W1.shape
+    I = twoI // 2
+    if H1 != H or tuple(W2.shape) != (E, H, I):
+        raise ValueError("W1/W2 shapes do not match x")
+    Ln, r = 0, 0
+    if gate_up_slices not in (1, 2):
+        raise ValueError("gate_up_slices must be 1 or 2")
+    if A1 is not None:
+        _need(A1, "A1", torch.bfloat16, 4)
+        Ln, _, r, _ = A1.shape
+        if r % gate_up_slices:
+            raise ValueError("A1 rows must hold gate_up_slices adapters of equal rank")
+        r //= gate_up_slices
+        _need(B1, "B1", torch.bfloat16, 4, (Ln, E, twoI, r))
+        _need(A2, "A2", torch.bfloat16, 4, (Ln, E, r, I))
+        _need(B2, "B2", torch.bfloat16, 4, (Ln, E, H, r))
+    return E, I, Ln, r
+
+
+def _layer_opts(Ln: int, bm_base: int, bm_lora: int, disable_pdl: bool, events,
+                gate_up_slices: int, adapter_ranks):
+    """The layer options struct, and the event array it points to (keep it alive)."""
+    opts = LayerOpts()
+    opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
+    opts.gate_up_slices = gate_up_slices
+    if adapter_ranks is not None:
+        _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (Ln,))
+        opts.adapter_ranks = ptr(adapter_ranks)
+    ev_arr = None
+    if events:
+        ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        opts.num_events = len(events)
+        opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
+    return opts, ev_arr
+
+
 def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
                    logits: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
                    topk_w: Optional[torch.Tensor] = None, k: Optional[int] = None,
@@ -258,13 +298,8 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r].
     adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r)."""
     _need(x, "x", torch.bfloat16, 2)
-    _need(W1, "W1", torch.bfloat16, 3)
-    _need(W2, "W2", torch.bfloat16, 3)
     T, H = x.shape
-    E, twoI, H1 = W1.shape
-    I = twoI // 2
-    if H1 != H or tuple(W2.shape) != (E, H, I):
-        raise ValueError("W1/W2 shapes do not match x")
+    E, I, Ln, r = _layer_weights(H, W1, W2, A1, B1, A2, B2, gate_up_slices)
     if logits is not None:
         _need(logits, "logits", torch.float32, 2, (T, E))
         if k is None:
@@ -273,18 +308,6 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
         _need(topk_ids, "topk_ids", torch.int32, 2)
         k = topk_ids.shape[1]
         _need(topk_w, "topk_w", torch.float32, 2, (T, k))
-    Ln, r = 0, 0
-    if gate_up_slices not in (1, 2):
-        raise ValueError("gate_up_slices must be 1 or 2")
-    if A1 is not None:
-        _need(A1, "A1", torch.bfloat16, 4)
-        Ln, _, r, _ = A1.shape
-        if r % gate_up_slices:
-            raise ValueError("A1 rows must hold gate_up_slices adapters of equal rank")
-        r //= gate_up_slices
-        _need(B1, "B1", torch.bfloat16, 4, (Ln, E, twoI, r))
-        _need(A2, "A2", torch.bfloat16, 4, (Ln, E, r, I))
-        _need(B2, "B2", torch.bfloat16, 4, (Ln, E, H, r))
     if token_adapter is not None:
         _need(token_adapter, "token_adapter", torch.int32, 1, (T,))
     if y is None:
@@ -293,20 +316,90 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     _need(y, "y", torch.float32 if y_fp32 else torch.bfloat16, 2, (T, H))
     if workspace is None:
         workspace = new_workspace(T, k, E, Ln, H, I, r, x.device)
-    opts = LayerOpts()
-    opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
-    opts.gate_up_slices = gate_up_slices
-    if adapter_ranks is not None:
-        _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (Ln,))
-        opts.adapter_ranks = ptr(adapter_ranks)
-    ev_arr = None
-    if events:
-        ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
-        opts.num_events = len(events)
-        opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
+    opts, _ev = _layer_opts(Ln, bm_base, bm_lora, disable_pdl, events, gate_up_slices,
+                            adapter_ranks)
     check(lib().moe_lora_layer_ex(
         ptr(x), ptr(logits), ptr(topk_ids), ptr(topk_w), ptr(token_adapter), T, H, I, E, k,
         ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2), ptr(B2), Ln, r, ptr(y), int(y_fp32),
         ptr(workspace), workspace.numel(), ctypes.byref(opts), stream_handle()),
         "moe_lora_layer")
     return y
+
+
+def moe_lora_host_io_layout(T: int, H: int, E: int, with_adapter: bool = True,
+                            y_fp32: bool = False) -> dict:
+    """Byte offsets (x, logits, token_adapter or -1, y) of the host-staged layer call, the
+    length of the host input block and of the device staging area."""
+    off = (ctypes.c_int64 * 4)()
+    ib, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    check(lib().moe_lora_host_io_layout(T, H, E, int(with_adapter), int(y_fp32), off,
+                                        ctypes.byref(ib), ctypes.byref(sb)),
+          "moe_lora_host_io_layout")
+    return {"offsets": tuple(off), "in_bytes": ib.value, "staging_bytes": sb.value}
+
+
+@dataclass
+class HostIO:
+    """Buffers of moe_lora_layer_host: the page-locked host input block, with views x [T, H]
+    bf16, logits [T, E] fp32 and token_adapter [T] int32 (None without adapter ids) for the
+    caller to fill; the page-locked host y; and the device staging area."""
+    in_host: torch.Tensor
+    y_host: torch.Tensor
+    staging: torch.Tensor
+    x: torch.Tensor
+    logits: torch.Tensor
+    token_adapter: Optional[torch.Tensor]
+    T: int
+    H: int
+    E: int
+    with_adapter: bool
+    y_fp32: bool
+
+    @property
+    def in_bytes(self) -> int:
+        return moe_lora_host_io_layout(self.T, self.H, self.E, self.with_adapter,
+                                       self.y_fp32)["in_bytes"]
+
+
+def new_host_io(T: int, H: int, E: int, with_adapter: bool = True, y_fp32: bool = False,
+                device="cuda") -> HostIO:
+    lay = moe_lora_host_io_layout(T, H, E, with_adapter, y_fp32)
+    o = lay["offsets"]
+    in_host = torch.zeros(max(lay["in_bytes"], 1), dtype=torch.uint8).pin_memory()
+
+    def view(at, n, dt, shape):
+        return in_host[at:at + n].view(dt).view(shape)
+
+    x = view(o[0], T * H * 2, torch.bfloat16, (T, H))
+    lg = view(o[1], T * E * 4, torch.float32, (T, E))
+    ta = view(o[2], T * 4, torch.int32, (T,)) if with_adapter else None
+    y_host = torch.empty((T, H), dtype=torch.float32 if y_fp32 else torch.bfloat16).pin_memory()
+    staging = torch.empty(max(lay["staging_bytes"], 1), dtype=torch.uint8, device=device)
+    return HostIO(in_host, y_host, staging, x, lg, ta, T, H, E, with_adapter, y_fp32)
+
+
+def moe_lora_layer_host(io: HostIO, W1: torch.Tensor, W2: torch.Tensor, *, k: int,
+                        A1=None, B1=None, A2=None, B2=None,
+                        workspace: Optional[torch.Tensor] = None, bm_base: int = 0,
+                        bm_lora: int = 0, disable_pdl: bool = False,
+                        events: Optional[Sequence] = None, gate_up_slices: int = 1,
+                        adapter_ranks: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One step from host memory: copies io's input block to the device, runs the layer
+    (routed from io.logits) and copies y back into io.y_host, all enqueued on the current
+    stream. Returns io.y_host, valid once the stream has been synchronised."""
+    T, H, E = io.T, io.H, io.E
+    E1, I, Ln, r = _layer_weights(H, W1, W2, A1, B1, A2, B2, gate_up_slices)
+    if E1 != E:
+        raise ValueError("W1 has a different expert count than the host block's logits")
+    if not io.in_host.is_pinned() or not io.y_host.is_pinned():
+        raise ValueError("the host buffers must be page-locked (new_host_io allocates them so)")
+    if workspace is None:
+        workspace = new_workspace(T, k, E, Ln, H, I, r, io.staging.device)
+    opts, _ev = _layer_opts(Ln, bm_base, bm_lora, disable_pdl, events, gate_up_slices,
+                            adapter_ranks)
+    check(lib().moe_lora_layer_host(
+        ptr(io.in_host), ptr(io.y_host), ptr(io.staging), io.staging.numel(),
+        int(io.with_adapter), T, H, I, E, k, ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2),
+        ptr(B2), Ln, r, int(io.y_fp32), ptr(workspace), workspace.numel(), ctypes.byref(opts),
+        stream_handle()), "moe_lora_layer_host")
+    return io.y_host

@@ -156,14 +156,14 @@ extern "C" size_t moe_lora_workspace_size(int T, int k, int E, int L, int H, int
   return p.valid ? (size_t)p.total : 0;
 }
 
-extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32_t* topk_ids,
-                                 const float* topk_w, const int32_t* token_adapter, int T, int H,
-                                 int I, int E, int k, const void* W1, const void* W2,
-                                 const void* A1, const void* B1, const void* A2, const void* B2,
-                                 int L, int r, void* y, int y_fp32, void* workspace,
-                                 size_t workspace_bytes, const moe_lora_layer_opts* opts,
-                                 moe_lora_stream_t stream_) {
-  // ---- host-side validation: nothing is launched on error ----
+// Host-side checks of a layer call; nothing is launched or copied on error. On success
+// *plan holds the layer's workspace plan (T = 0 passes with nothing to do).
+static int check_layer_args(const void* x, const float* logits, const int32_t* topk_ids,
+                            const float* topk_w, int T, int H, int I, int E, int k,
+                            const void* W1, const void* W2, const void* A1, const void* B1,
+                            const void* A2, const void* B2, int L, int r, const void* y,
+                            const void* workspace, size_t workspace_bytes,
+                            const moe_lora_layer_opts& o, LayerPlan* plan) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E || L < 0) return MOE_LORA_ERR_INVALID_ARG;
   if (k > 32 || E > 1024 || L >= 65535) return MOE_LORA_ERR_UNSUPPORTED;
   if (L > 0 && (r < 1 || !A1 || !B1 || !A2 || !B2)) return MOE_LORA_ERR_INVALID_ARG;
@@ -181,17 +181,31 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   }
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return MOE_LORA_ERR_INVALID_ARG;
+  if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return MOE_LORA_ERR_INVALID_ARG;
+  if (o.gate_up_slices < 0 || o.gate_up_slices > 2) return MOE_LORA_ERR_INVALID_ARG;
+  *plan = plan_layer(T, k, E, L, H, I, r, o.bm_base, o.bm_lora);
+  if (!plan->valid) return MOE_LORA_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_LORA_OK;
+  if (workspace_bytes < (size_t)plan->total) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  return check_device();
+}
+
+extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32_t* topk_ids,
+                                 const float* topk_w, const int32_t* token_adapter, int T, int H,
+                                 int I, int E, int k, const void* W1, const void* W2,
+                                 const void* A1, const void* B1, const void* A2, const void* B2,
+                                 int L, int r, void* y, int y_fp32, void* workspace,
+                                 size_t workspace_bytes, const moe_lora_layer_opts* opts,
+                                 moe_lora_stream_t stream_) {
+  // ---- host-side validation: nothing is launched on error ----
   moe_lora_layer_opts o = {};
   if (opts) o = *opts;
-  if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return MOE_LORA_ERR_INVALID_ARG;
+  LayerPlan p;
+  int st = check_layer_args(x, logits, topk_ids, topk_w, T, H, I, E, k, W1, W2, A1, B1, A2, B2,
+                            L, r, y, workspace, workspace_bytes, o, &p);
+  if (st != MOE_LORA_OK || T == 0) return st;
   const int slices = o.gate_up_slices == 0 ? 1 : o.gate_up_slices;
-  if (slices != 1 && slices != 2) return MOE_LORA_ERR_INVALID_ARG;
-  LayerPlan p = plan_layer(T, k, E, L, H, I, r, o.bm_base, o.bm_lora);
-  if (!p.valid) return MOE_LORA_ERR_UNSUPPORTED;
-  if (T == 0) return MOE_LORA_OK;
-  if (workspace_bytes < (size_t)p.total) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
-  int st = check_device();
-  if (st != MOE_LORA_OK) return st;
+  const bool have_logits = logits != nullptr;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool pdl = !o.disable_pdl;
@@ -280,4 +294,61 @@ extern "C" int moe_lora_layer(const void* x, const float* logits, const int32_t*
   return moe_lora_layer_ex(x, logits, topk_ids, topk_w, token_adapter, T, H, I, E, k, W1, W2, A1,
                            B1, A2, B2, L, r, y, y_fp32, workspace, workspace_bytes, nullptr,
                            stream);
+}
+
+extern "C" int moe_lora_host_io_layout(int T, int H, int E, int with_adapter, int y_fp32,
+                                       int64_t* offsets, size_t* in_bytes, size_t* staging_bytes) {
+  if (T < 0 || H < 1 || E < 1 || !offsets) return MOE_LORA_ERR_INVALID_ARG;
+  if ((with_adapter != 0 && with_adapter != 1) || (y_fp32 != 0 && y_fp32 != 1))
+    return MOE_LORA_ERR_INVALID_ARG;
+  int64_t o = 0, end = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t at = (int64_t)round_up((size_t)o, 256);
+    o = end = at + bytes;
+    return at;
+  };
+  offsets[0] = take((int64_t)T * H * 2);
+  offsets[1] = take((int64_t)T * E * 4);
+  offsets[2] = with_adapter ? take((int64_t)T * 4) : -1;
+  const int64_t in_end = end;
+  offsets[3] = take((int64_t)T * H * (y_fp32 ? 4 : 2));
+  if (in_bytes) *in_bytes = (size_t)in_end;
+  if (staging_bytes) *staging_bytes = (size_t)end;
+  return MOE_LORA_OK;
+}
+
+extern "C" int moe_lora_layer_host(const void* in_host, void* y_host, void* staging,
+                                   size_t staging_bytes, int with_adapter, int T, int H, int I,
+                                   int E, int k, const void* W1, const void* W2, const void* A1,
+                                   const void* B1, const void* A2, const void* B2, int L, int r,
+                                   int y_fp32, void* workspace, size_t workspace_bytes,
+                                   const moe_lora_layer_opts* opts, moe_lora_stream_t stream_) {
+  int64_t off[4];
+  size_t in_bytes = 0, need = 0;
+  int st = moe_lora_host_io_layout(T, H, E, with_adapter, y_fp32, off, &in_bytes, &need);
+  if (st != MOE_LORA_OK) return st;
+  if (T > 0 && (!in_host || !y_host || !staging)) return MOE_LORA_ERR_INVALID_ARG;
+  if (staging && (reinterpret_cast<uintptr_t>(staging) & 255u) != 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (T > 0 && staging_bytes < need) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
+  char* sg = static_cast<char*>(staging);
+  const void* x = sg ? sg + off[0] : nullptr;
+  const float* logits = sg ? reinterpret_cast<const float*>(sg + off[1]) : nullptr;
+  const int32_t* ta = sg && with_adapter ? reinterpret_cast<const int32_t*>(sg + off[2]) : nullptr;
+  void* y = sg ? sg + off[3] : nullptr;
+  moe_lora_layer_opts o = {};
+  if (opts) o = *opts;
+  LayerPlan p;
+  st = check_layer_args(x, logits, nullptr, nullptr, T, H, I, E, k, W1, W2, A1, B1, A2, B2, L, r,
+                        y, workspace, workspace_bytes, o, &p);
+  if (st != MOE_LORA_OK || T == 0) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaMemcpyAsync(sg, in_host, in_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return MOE_LORA_ERR_CUDA;
+  st = moe_lora_layer_ex(x, logits, nullptr, nullptr, ta, T, H, I, E, k, W1, W2, A1, B1, A2, B2,
+                         L, r, y, y_fp32, workspace, workspace_bytes, opts, stream_);
+  if (st != MOE_LORA_OK) return st;
+  const size_t y_bytes = (size_t)T * H * (y_fp32 ? 4 : 2);
+  if (cudaMemcpyAsync(y_host, y, y_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return MOE_LORA_ERR_CUDA;
+  return MOE_LORA_OK;
 }

@@ -263,6 +263,43 @@ MOE_LORA_API int moe_lora_layer_ex(const void* x, const float* logits, const int
                       int y_fp32, void* workspace, size_t workspace_bytes,
                       const moe_lora_layer_opts* opts, moe_lora_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * One serving step with its per-step inputs and its output in host memory: the
+ * same layer as moe_lora_layer_ex, routed from logits, with the copies in and out
+ * issued by the library on the same stream. The pages describe the device-side
+ * computation only; this call stages it for a caller whose batch arrives in host
+ * memory (the router logits and adapter ids of a decode step, for instance).
+ *
+ * moe_lora_host_io_layout (host only) gives the byte offsets, each 256-byte aligned:
+ *   offsets[0] x [T, H] bf16, offsets[1] logits [T, E] fp32,
+ *   offsets[2] token_adapter [T] int32 (with_adapter = 1; else -1),
+ *   offsets[3] y [T, H] bf16 (y_fp32 = 0) or fp32.
+ * The caller's host input block holds x, logits and (with_adapter) the adapter ids
+ * at offsets[0..2] and is *in_bytes long; the device staging area, *staging_bytes
+ * long, holds the same inputs plus y at offsets[3].
+ *
+ * moe_lora_layer_host enqueues on `stream`, in order: one cudaMemcpyAsync of the
+ * whole input block (in_bytes) into `staging`; the layer on the staged views
+ * (moe_lora_layer_ex with logits routing; token_adapter NULL when with_adapter = 0;
+ * weights, workspace and opts as there); one cudaMemcpyAsync of y into y_host
+ * (T*H*2 bytes, or T*H*4 with y_fp32). It returns without waiting: synchronise the
+ * stream before reading y_host or rewriting in_host. Page-locked host memory keeps
+ * both copies asynchronous; pageable memory works but the copies then synchronise
+ * with the host. staging: device memory, 256-byte aligned, at least staging_bytes.
+ * Errors: every argument, the layer's included, is checked before anything is
+ * copied or launched (MOE_LORA_ERR_WORKSPACE_TOO_SMALL for a short staging area).
+ * ------------------------------------------------------------------------- */
+MOE_LORA_API int moe_lora_host_io_layout(int T, int H, int E, int with_adapter, int y_fp32,
+                                         int64_t* offsets, size_t* in_bytes,
+                                         size_t* staging_bytes);
+
+MOE_LORA_API int moe_lora_layer_host(const void* in_host, void* y_host, void* staging,
+                                     size_t staging_bytes, int with_adapter, int T, int H, int I,
+                                     int E, int k, const void* W1, const void* W2, const void* A1,
+                                     const void* B1, const void* A2, const void* B2, int L, int r,
+                                     int y_fp32, void* workspace, size_t workspace_bytes,
+                                     const moe_lora_layer_opts* opts, moe_lora_stream_t stream);
+
 /* Tile sizes the layer picks for a shape (host only): bm_base, bm_lora. */
 MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r, int32_t* bm_base,
                          int32_t* bm_lora);

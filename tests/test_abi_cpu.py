@@ -158,6 +158,52 @@ def test_host_validation_before_any_cuda_call(L):
     assert L.moe_lora_layer(*a) == 0
 
 
+def test_host_io_layout(L):
+    """The host-staged call's block: x, logits, adapter ids, then y, each at a 256-byte
+    aligned offset, back to back, and the input block ending where the last input ends."""
+    off = (ctypes.c_int64 * 4)()
+    ib, sb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    for T, H, E, wa, yf in [(64, 2880, 32, 1, 0), (5, 8, 3, 0, 1), (7, 24, 128, 1, 1)]:
+        assert L.moe_lora_host_io_layout(T, H, E, wa, yf, off, ctypes.byref(ib),
+                                         ctypes.byref(sb)) == 0
+        sizes = [T * H * 2, T * E * 4, T * 4 if wa else 0, T * H * (4 if yf else 2)]
+        used = [i for i in range(4) if i != 2 or wa]
+        assert off[0] == 0 and (off[2] == -1) == (not wa)
+        prev_end = 0
+        for i in used:
+            assert off[i] % 256 == 0 and off[i] >= prev_end and off[i] - prev_end < 256
+            prev_end = off[i] + sizes[i]
+        last_in = 2 if wa else 1
+        assert ib.value == off[last_in] + sizes[last_in]
+        assert sb.value == off[3] + sizes[3]
+    assert L.moe_lora_host_io_layout(4, 8, 2, 2, 0, off, None, None) == 1   # with_adapter 0/1
+    assert L.moe_lora_host_io_layout(4, 8, 2, 1, 0, None, None, None) == 1  # no offsets array
+
+
+def test_host_staged_layer_validation(L):
+    """moe_lora_layer_host checks its own arguments and the layer's before any copy."""
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    args = [fake, fake, P(0x100000), 1 << 30, 1, 8, 256, 512, 4, 2, fake, fake, fake, fake, fake,
+            fake, 2, 8, 0, P(0x200000), 1 << 30, None, None]
+    a = list(args); a[0] = None                                              # no host block
+    assert L.moe_lora_layer_host(*a) == 1
+    a = list(args); a[2] = P(0x100010)                                       # staging alignment
+    assert L.moe_lora_layer_host(*a) == 1
+    a = list(args); a[3] = 1024                                              # staging too short
+    assert L.moe_lora_layer_host(*a) == 4
+    a = list(args); a[6] = 100                                               # H % 8
+    assert L.moe_lora_layer_host(*a) == 2
+    a = list(args); a[9] = 5                                                 # k > E
+    assert L.moe_lora_layer_host(*a) == 1
+    a = list(args); a[20] = 16                                               # workspace too small
+    assert L.moe_lora_layer_host(*a) == 4
+    a = list(args); a[4] = 3                                                 # with_adapter 0/1
+    assert L.moe_lora_layer_host(*a) == 1
+    a = list(args); a[5] = 0                                                 # T = 0: nothing to do
+    assert L.moe_lora_layer_host(*a) == 0
+
+
 def test_product_path_never_imports_the_oracle():
     pkg = os.path.join(ROOT, "expert_adapter_gemms_gb300")
     for dirpath, _, files in os.walk(pkg):

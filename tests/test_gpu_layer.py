@@ -303,3 +303,32 @@ def test_layer_adapter_rank_out_of_range_flagged():
     ref = oracle.moe_lora_layer(inp.x, inp.W1, inp.W2, ids, w, inp.token_adapter, inp.A1, inp.B1,
                                 inp.A2, inp.B2, adapter_ranks=torch.as_tensor([8, 0]))
     assert_close(y.cpu(), ref, LAYER_RTOL, "clamped ranks")
+
+
+@pytest.mark.parametrize("idx,with_adapter,y_fp32", [(0, True, True), (1, True, False),
+                                                     (1, False, False)])
+def test_layer_host_staged(idx, with_adapter, y_fp32):
+    """moe_lora_layer_host: the inputs copied from one page-locked host block, the chain on
+    the staged views, y copied back. Bit-identical to the device-pointer call on the same
+    inputs (same kernels), and within tolerance of the oracle (the tiny workload on every
+    token, the decode workload on a sample); without adapter ids the base MoE alone."""
+    m = need_gpu()
+    inp = make_config_inputs(idx)
+    io = m.new_host_io(inp.T, inp.H, inp.E, with_adapter=with_adapter, y_fp32=y_fp32)
+    io.x.copy_(inp.x)
+    io.logits.copy_(inp.logits)
+    if with_adapter:
+        io.token_adapter.copy_(inp.token_adapter)
+    lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
+    W1, W2 = dev(inp.W1), dev(inp.W2)
+    io.y_host.fill_(float("nan"))
+    y_host = m.moe_lora_layer_host(io, W1, W2, k=inp.k, **lora)
+    torch.cuda.synchronize()
+    ta = dev(inp.token_adapter) if with_adapter else None
+    y_dev = m.moe_lora_layer(dev(inp.x), W1, W2, logits=dev(inp.logits), k=inp.k,
+                             token_adapter=ta, y_fp32=y_fp32, **lora).cpu()
+    assert torch.equal(y_host, y_dev)
+    tokens = np.arange(inp.T) if inp.T <= 16 else np.arange(0, inp.T, 4)
+    no_adapter = np.full(inp.T, -1, dtype=np.int32)
+    ref = oracle_layer(inp, tokens, token_adapter=None if with_adapter else no_adapter)
+    assert_close(y_host[tokens], ref, LAYER_RTOL, f"host-staged {CONFIGS[idx]['name']}")
