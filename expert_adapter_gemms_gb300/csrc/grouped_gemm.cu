@@ -20,6 +20,7 @@
 //   tiles so CTAs that share a weight block run together (L2 reuse).
 // * Every mbarrier wait is bounded; on timeout the CTA records
 //   MOE_LORA_DEVERR_TIMEOUT, drains its own copies and frees TMEM.
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -400,13 +401,13 @@ static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const Ali
                          int max_tiles, int E, int N, int K, float* out, cudaStream_t stream,
                          bool pdl, int mode, int early) {
   using C = GemmCfg<BN, STAGES>;
-  static int configured[64] = {0};
+  static std::atomic<int> configured[64];
   int dev = 0;
   ML_CHECK_CUDA(cudaGetDevice(&dev));
-  if (dev < 64 && !configured[dev]) {
+  if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
     ML_CHECK_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
-    configured[dev] = 1;
+    configured[dev].store(1, std::memory_order_release);
   }
   const int n_wblocks = ceil_div(N, kBM);
   int64_t grid = (int64_t)(mode == kModeExpert ? E : max_tiles) * n_wblocks;

@@ -18,6 +18,7 @@
 // holds), a kernel reads such older data -- B weights, align tables, the base
 // output of the GEMM two launches back -- before its own wait, and waits only for
 // the z produced by its immediate predecessor.
+#include <atomic>
 #include "internal.h"
 
 namespace moe_lora {
@@ -910,10 +911,10 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     const int cc = chunks_for(I);
     const dim3 grid(a.max_blocks * cc + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
     const size_t smem1 = Bp ? 2 * zsmem + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float) : 0;
-    static int configured[64] = {0};  // every instance at once, once per device
+    static std::atomic<int> configured[64];  // every instance at once, once per device
     int dev = 0;
     ML_CHECK_CUDA(cudaGetDevice(&dev));
-    if (dev < 64 && !configured[dev]) {
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
       const int lim = (int)(2 * zsmem_bytes(8) + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float));
       const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
 #define ML_SWIGLU_ATTR(KC_)                                                                  \
@@ -923,7 +924,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, true, true>, attr, lim));
       ML_SWIGLU_ATTR(1) ML_SWIGLU_ATTR(2) ML_SWIGLU_ATTR(4) ML_SWIGLU_ATTR(8)
 #undef ML_SWIGLU_ATTR
-      configured[dev] = 1;
+      configured[dev].store(1, std::memory_order_release);
     }
     auto go = [&](auto kern) -> int {
       return launch_pdl(kern, grid, kExpandThreads, smem1, stream, pdl, Z, Bp,

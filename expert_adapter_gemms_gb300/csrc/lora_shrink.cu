@@ -15,6 +15,7 @@
 // keeping every load 16 bytes wide. Masks on K are compiled out when
 // K % 32 == 0 (the EVEN_K specialisation); K % 8 != 0 or unaligned bases fall
 // back to element loads.
+#include <atomic>
 #include <algorithm>
 
 #include "internal.h"
@@ -373,16 +374,16 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
         const int ngroups = ceil_div(r, 32);
         const int64_t grid = (int64_t)a.max_blocks * ngroups;
         if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
-        static int configured[64] = {0};  // both instances at once, once per device
+        static std::atomic<int> configured[64];  // both instances at once, once per device
         int dev = 0;
         ML_CHECK_CUDA(cudaGetDevice(&dev));
-        if (dev < 64 && !configured[dev]) {
+        if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
           const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, false>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, false>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, true>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, true>, attr, 56 * 1024));
-          configured[dev] = 1;
+          configured[dev].store(1, std::memory_order_release);
         }
         auto go = [&](auto kern) -> int {
           return launch_pdl(kern, dim3((unsigned)grid), kShrinkWarps * 32, smem, stream, pdl, Xp,
