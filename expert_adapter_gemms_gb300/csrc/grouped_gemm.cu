@@ -50,6 +50,8 @@ struct GemmCfg {
 // ----------------------------------------------------------------------------
 // gather: xs[row] = x[token of sorted slot row]
 // ----------------------------------------------------------------------------
+constexpr int kGatherU = 4;  // 16-byte chunks per lane per row segment
+
 template <bool kVec>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const int* __restrict__ hdr,
@@ -65,13 +67,31 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16* _
   if (!trigger_first) pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < n_valid; row += warps) {
-    const int t = __ldcg(sorted_slots + row) / k;
-    if (kVec) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (kVec) {
+    // A warp copies one segment of a row (32 x kGatherU 16-byte chunks): one slot lookup,
+    // then every load of the segment before the first store, so a row costs two round
+    // trips rather than one per 512 bytes, and rows x segments spread over the whole GPU.
+    const int n8 = H / 8;
+    const int segs = (n8 + 32 * kGatherU - 1) / (32 * kGatherU);
+    const int64_t items = (int64_t)n_valid * segs;
+    for (int64_t item = gw; item < items; item += warps) {
+      const int row = (int)(item / segs), seg = (int)(item - (int64_t)row * segs);
+      const int t = __ldcg(sorted_slots + row) / k;
       const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
       uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)row * H);
-      for (int c = lane; c < H / 8; c += 32) dst[c] = __ldcg(src + c);
-    } else {
+      const int c0 = seg * 32 * kGatherU + lane;
+      uint4 v[kGatherU];
+#pragma unroll
+      for (int u = 0; u < kGatherU; ++u)
+        if (c0 + 32 * u < n8) v[u] = __ldcg(src + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kGatherU; ++u)
+        if (c0 + 32 * u < n8) dst[c0 + 32 * u] = v[u];
+    }
+  } else {
+    for (int row = gw; row < n_valid; row += warps) {
+      const int t = __ldcg(sorted_slots + row) / k;
       for (int c = lane; c < H; c += 32) xs[(size_t)row * H + c] = __ldcg(x + (size_t)t * H + c);
     }
   }
@@ -81,14 +101,17 @@ int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& 
                   cudaStream_t stream, bool pdl, bool trigger_first) {
   if (a.S == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
-  int blocks = ceil_div(a.S, 8);
-  if (blocks > num_sms() * 8) blocks = num_sms() * 8;
   const auto* xp = static_cast<const __nv_bfloat16*>(x);
   auto* xsp = static_cast<__nv_bfloat16*>(xs);
-  if (H % 8 == 0 && aligned16(x) && aligned16(xs))
-    return launch_pdl(gather_rows_kernel<true>, blocks, 256, 0, stream, pdl, xp, v.hdr,
+  const bool vec = H % 8 == 0 && aligned16(x) && aligned16(xs);
+  // one warp per row segment (vector path) or per row, eight warps per CTA, at most
+  // eight CTAs per SM
+  const int segs = vec ? ceil_div(H / 8, 32 * kGatherU) : 1;
+  const int64_t blocks = std::min<int64_t>(ceil_div64((int64_t)a.S * segs, 8), (int64_t)num_sms() * 8);
+  if (vec)
+    return launch_pdl(gather_rows_kernel<true>, (unsigned)blocks, 256, 0, stream, pdl, xp, v.hdr,
                       v.sorted_slots, al->k, H, xsp, trigger_first ? 1 : 0);
-  return launch_pdl(gather_rows_kernel<false>, blocks, 256, 0, stream, pdl, xp, v.hdr,
+  return launch_pdl(gather_rows_kernel<false>, (unsigned)blocks, 256, 0, stream, pdl, xp, v.hdr,
                     v.sorted_slots, al->k, H, xsp, trigger_first ? 1 : 0);
 }
 
