@@ -27,8 +27,11 @@ def _setup(T, H, I, E, k, L, r, seed, bm_base=16, bm_lora=16, adapters="uniform_
     return m, inp, ids, w, al, ref
 
 
-@pytest.mark.parametrize("H", [256, 136, 8])
+@pytest.mark.parametrize("H", [256, 136, 8, 1024, 1032, 2880])
 def test_gather_exact(H):
+    """Bit-exact row gather. A warp copies a segment of 128 16-byte chunks of a row: H = 1024
+    is one full segment, 1032 adds a second segment of one chunk, 2880 three segments with a
+    partial last one; H = 8 and 136 are single short segments."""
     m, inp, ids, w, al, ref = _setup(T=19, H=H, I=16, E=5, k=3, L=2, r=8, seed=1)
     xs = Guarded((al.S, H), torch.bfloat16)
     m.moe_gather_rows(dev(inp.x), al, out=xs.t)
