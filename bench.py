@@ -289,8 +289,8 @@ def run_reference(args):
     nw, rank, _ = world()
     if rank != 0:
         return 0
-    from workloads import make_config_inputs
-    inp = make_config_inputs(args.workload)
+    from workloads import make_workload_inputs
+    inp = make_workload_inputs(args.workload)
     full = OracleStep(inp)
     t0 = time.perf_counter()
     full()
@@ -398,9 +398,9 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     import expert_adapter_gemms_gb300 as m
-    from workloads import make_config_inputs
+    from workloads import make_workload_inputs
 
-    inp = make_config_inputs(args.workload)
+    inp = make_workload_inputs(args.workload)
     d = lambda t: None if t is None else t.to("cuda").contiguous()  # noqa: E731
     W1, W2 = d(inp.W1), d(inp.W2)
     lora = dict(A1=d(inp.A1), B1=d(inp.B1), A2=d(inp.A2), B2=d(inp.B2)) if inp.L else {}

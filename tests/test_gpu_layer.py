@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import CONFIGS, make_config_inputs, make_layer_inputs
+from workloads import WORKLOAD_NAMES, make_workload_inputs, make_layer_inputs
 
 from gpu_util import LAYER_RTOL, Guarded, assert_close, dev, f64, need_gpu
 
@@ -34,24 +34,24 @@ def oracle_layer(inp, tokens=None, adapters=True, token_adapter=None):
     return oracle.moe_lora_layer(inp.x[sel], inp.W1, inp.W2, ids[sel], w[sel], ta[sel], *lora)
 
 
-@pytest.mark.parametrize("idx", range(len(CONFIGS)))
-def test_layer_workloads(idx):
+@pytest.mark.parametrize("name", WORKLOAD_NAMES)
+def test_layer_workloads(name):
     """All five workloads; the oracle runs on every token of the small ones and on a
     sample of 48 tokens of the large ones (tokens are independent of each other)."""
     m = need_gpu()
-    inp = make_config_inputs(idx)
+    inp = make_workload_inputs(name)
     y = run_layer(m, inp).cpu()
     if inp.T <= 256:
         tokens = np.arange(inp.T)
     else:
-        tokens = np.sort(np.random.default_rng(idx).choice(inp.T, size=48, replace=False))
+        tokens = np.sort(np.random.default_rng(WORKLOAD_NAMES.index(name)).choice(inp.T, size=48, replace=False))
     ref = oracle_layer(inp, tokens)
-    assert_close(y[tokens], ref, LAYER_RTOL, CONFIGS[idx]["name"])
+    assert_close(y[tokens], ref, LAYER_RTOL, name)
 
 
 def test_layer_error_word_clean_on_workload():
     m = need_gpu()
-    inp = make_config_inputs(1)
+    inp = make_workload_inputs("gptoss20b_decode")
     ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
     run_layer(m, inp, workspace=ws)
     assert m.get_error(ws) == 0
@@ -75,7 +75,7 @@ def test_layer_lora_delta_matches_oracle():
     """With the workloads' own N(0, 0.02) adapters on the tiny layer the LoRA term is below
     the layer bound; check the GPU's delta y_lora - y_base against the oracle's directly."""
     m = need_gpu()
-    inp = make_config_inputs(0)
+    inp = make_workload_inputs("tiny")
     y_l = run_layer(m, inp, y_fp32=True).cpu().double().numpy()
     y_b = run_layer(m, inp, y_fp32=True, adapters=False).cpu().double().numpy()
     d_gpu = y_l - y_b
@@ -88,7 +88,7 @@ def test_layer_lora_delta_matches_oracle():
 def test_layer_base_reductions_bitwise():
     """Adapter -1 everywhere, or B = 0, give exactly the base-only output."""
     m = need_gpu()
-    inp = make_config_inputs(0)
+    inp = make_workload_inputs("tiny")
     y_base = run_layer(m, inp, y_fp32=True, adapters=False)
     none = torch.full((inp.T,), -1, dtype=torch.int32)
     y_none = run_layer(m, inp, y_fp32=True, token_adapter=none)
@@ -305,15 +305,16 @@ def test_layer_adapter_rank_out_of_range_flagged():
     assert_close(y.cpu(), ref, LAYER_RTOL, "clamped ranks")
 
 
-@pytest.mark.parametrize("idx,with_adapter,y_fp32", [(0, True, True), (1, True, False),
-                                                     (1, False, False)])
-def test_layer_host_staged(idx, with_adapter, y_fp32):
+@pytest.mark.parametrize("name,with_adapter,y_fp32", [("tiny", True, True),
+                                                      ("gptoss20b_decode", True, False),
+                                                      ("gptoss20b_decode", False, False)])
+def test_layer_host_staged(name, with_adapter, y_fp32):
     """moe_lora_layer_host: the inputs copied from one page-locked host block, the chain on
     the staged views, y copied back. Bit-identical to the device-pointer call on the same
     inputs (same kernels), and within tolerance of the oracle (the tiny workload on every
     token, the decode workload on a sample); without adapter ids the base MoE alone."""
     m = need_gpu()
-    inp = make_config_inputs(idx)
+    inp = make_workload_inputs(name)
     io = m.new_host_io(inp.T, inp.H, inp.E, with_adapter=with_adapter, y_fp32=y_fp32)
     io.x.copy_(inp.x)
     io.logits.copy_(inp.logits)
@@ -331,4 +332,4 @@ def test_layer_host_staged(idx, with_adapter, y_fp32):
     tokens = np.arange(inp.T) if inp.T <= 16 else np.arange(0, inp.T, 4)
     no_adapter = np.full(inp.T, -1, dtype=np.int32)
     ref = oracle_layer(inp, tokens, token_adapter=None if with_adapter else no_adapter)
-    assert_close(y_host[tokens], ref, LAYER_RTOL, f"host-staged {CONFIGS[idx]['name']}")
+    assert_close(y_host[tokens], ref, LAYER_RTOL, f"host-staged {name}")

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import make_config_routing
+from workloads import WORKLOAD_NAMES, make_workload_routing
 
 from gpu_util import dev, need_gpu
 
@@ -51,10 +51,10 @@ def test_route_golden_cases(golden_dir):
         np.testing.assert_allclose(w.cpu().numpy(), np.array(c["w"]), rtol=0, atol=1e-6)
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
-def test_route_workloads_bitexact_ids(idx):
+@pytest.mark.parametrize("name", WORKLOAD_NAMES)
+def test_route_workloads_bitexact_ids(name):
     m = need_gpu()
-    lg, _, c = make_config_routing(idx)
+    lg, _, c = make_workload_routing(name)
     ids, w = m.moe_topk_softmax(dev(lg), c["k"])
     rid, rw = oracle.route_topk_softmax(lg, c["k"])
     assert np.array_equal(ids.cpu().numpy(), rid)
@@ -85,11 +85,11 @@ def test_route_empty():
 
 
 # ---------------------------------------------------------------- align
-@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("name", WORKLOAD_NAMES)
 @pytest.mark.parametrize("bm_base,bm_lora", [(16, 16), (64, 1), (256, 7)])
-def test_align_workloads(idx, bm_base, bm_lora):
+def test_align_workloads(name, bm_base, bm_lora):
     m = need_gpu()
-    lg, ad, c = make_config_routing(idx)
+    lg, ad, c = make_workload_routing(name)
     ids, _ = oracle.route_topk_softmax(lg, c["k"])
     _check_align(m, ids, ad, c["E"], c["L"], bm_base, bm_lora)
 
@@ -132,7 +132,7 @@ def test_align_out_of_range_ids_flagged_not_trapped():
 
 def test_align_is_deterministic():
     m = need_gpu()
-    lg, ad, c = make_config_routing(2)
+    lg, ad, c = make_workload_routing("gptoss20b_prefill")
     ids, _ = oracle.route_topk_softmax(lg, c["k"])
     ids_d = dev(torch.as_tensor(ids, dtype=torch.int32))
     a1 = m.moe_lora_align(ids_d, dev(ad), c["E"], c["L"], 256, 16)

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from oracle import moe_lora as om
-from workloads import make_config_inputs, make_config_routing, make_layer_inputs
+from workloads import WORKLOAD_NAMES, make_layer_inputs, make_workload_inputs, make_workload_routing
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -298,9 +298,9 @@ def test_align_invalid_ids():
     pin_align_invalid_ids()
 
 
-@pytest.mark.parametrize("idx", [0, 1, 2, 3, 4])
-def test_align_invariants_on_workloads(idx):
-    lg, ad, c = make_config_routing(idx)
+@pytest.mark.parametrize("name", WORKLOAD_NAMES)
+def test_align_invariants_on_workloads(name):
+    lg, ad, c = make_workload_routing(name)
     ids, _ = oracle.route_topk_softmax(lg, c["k"])
     al = oracle.align(ids, ad, c["E"], c["L"], 64, 16)
     S = c["T"] * c["k"]
@@ -317,7 +317,7 @@ def test_align_invariants_on_workloads(idx):
 
 
 def test_layer_scalar_vs_vectorised_tiny_workload():
-    pin_layer_scalar_vs_vectorised(make_config_inputs(0))
+    pin_layer_scalar_vs_vectorised(make_workload_inputs("tiny"))
 
 
 @pytest.mark.parametrize("seed", range(20))

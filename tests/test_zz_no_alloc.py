@@ -13,7 +13,7 @@ import ctypes
 import pytest
 import torch
 
-from workloads import make_config_inputs, make_layer_inputs
+from workloads import make_workload_inputs, make_layer_inputs
 
 from gpu_util import LAYER_RTOL, assert_close, dev, need_gpu
 
@@ -38,7 +38,7 @@ def test_noalloc_matches_layer_on_two_calls():
     m = need_gpu()
     fn = _noalloc_fn(m.lib())
     stream = torch.cuda.current_stream().cuda_stream
-    cases = [make_config_inputs(0),
+    cases = [make_workload_inputs("tiny"),
              make_layer_inputs(T=37, H=192, I=160, E=6, k=3, L=3, r=16, seed=5, lora_std=None)]
     for inp in cases:
         x, W1, W2 = dev(inp.x), dev(inp.W1), dev(inp.W2)

@@ -6,10 +6,11 @@ matrix products or activations), so that both the fp64 CPU oracle and the CUDA
 path can consume the very same inputs without sharing any computation.
 """
 from .generators import (  # noqa: F401
-    CONFIGS,
+    WORKLOADS,
+    WORKLOAD_NAMES,
     LayerInputs,
-    config_by_name,
-    make_config_inputs,
-    make_config_routing,
+    workload_by_name,
+    make_workload_inputs,
+    make_workload_routing,
     make_layer_inputs,
 )

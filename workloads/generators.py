@@ -33,7 +33,7 @@ import numpy as np
 import torch
 
 # The five workloads the layer is measured on. "std" of weights is 0.02.
-CONFIGS = [
+WORKLOADS = [
     dict(name="tiny", T=8, H=256, I=512, E=4, k=2, L=2, r=8,
          routing="gaussian", adapters="tiny"),
     dict(name="gptoss20b_decode", T=64, H=2880, I=2880, E=32, k=4, L=8, r=32,
@@ -47,8 +47,11 @@ CONFIGS = [
 ]
 
 
-def config_by_name(name: str) -> dict:
-    for c in CONFIGS:
+WORKLOAD_NAMES = [w["name"] for w in WORKLOADS]
+
+
+def workload_by_name(name: str) -> dict:
+    for c in WORKLOADS:
         if c["name"] == name:
             return dict(c)
     raise KeyError(name)
@@ -209,29 +212,29 @@ def make_layer_inputs(T: int, H: int, I: int, E: int, k: int, L: int, r: int, se
                        A2=A2, B2=B2, name=name, seed=seed)
 
 
-def make_config_inputs(index_or_name: Union[int, str], seed: Optional[int] = None) -> LayerInputs:
+def make_workload_inputs(index_or_name: Union[int, str], seed: Optional[int] = None) -> LayerInputs:
     """Inputs of one of the five named workloads; workload i is seeded with 1000 + i."""
     if isinstance(index_or_name, int):
         idx = index_or_name
     else:
-        idx = [c["name"] for c in CONFIGS].index(index_or_name)
-    c = CONFIGS[idx]
+        idx = [c["name"] for c in WORKLOADS].index(index_or_name)
+    c = WORKLOADS[idx]
     return make_layer_inputs(c["T"], c["H"], c["I"], c["E"], c["k"], c["L"], c["r"],
                              seed=1000 + idx if seed is None else seed,
                              routing=c["routing"], adapters=c["adapters"], name=c["name"])
 
 
-def make_config_routing(index_or_name: Union[int, str], seed: Optional[int] = None):
+def make_workload_routing(index_or_name: Union[int, str], seed: Optional[int] = None):
     """Only the router logits and adapter ids of a named workload.
 
-    Same generator and draw order as :func:`make_config_inputs`, stopped before
+    Same generator and draw order as :func:`make_workload_inputs`, stopped before
     the activations and weights, so the values equal that function's.
     """
     if isinstance(index_or_name, int):
         idx = index_or_name
     else:
-        idx = [c["name"] for c in CONFIGS].index(index_or_name)
-    c = CONFIGS[idx]
+        idx = [c["name"] for c in WORKLOADS].index(index_or_name)
+    c = WORKLOADS[idx]
     rng = np.random.default_rng(1000 + idx if seed is None else seed)
     logits = _routing_logits(rng, c["T"], c["E"], c["routing"])
     token_adapter = _adapters(rng, c["T"], c["L"], c["adapters"])
