@@ -272,6 +272,45 @@ def cpu_cores():
     return n
 
 
+def host_info() -> dict:
+    """CPU model and BLAS thread pool of the host the oracle runs on (best effort: a field
+    that cannot be read is reported as unknown, never an error)."""
+    import platform
+    import subprocess
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    blas = None
+    try:
+        import numpy  # noqa: F401  (loads the BLAS library the oracle uses)
+        from threadpoolctl import threadpool_info
+        pools = [p for p in threadpool_info() if p.get("user_api") == "blas"]
+        if pools:
+            blas = {"library": pools[0].get("internal_api"), "threads": pools[0].get("num_threads")}
+    except Exception:  # threadpoolctl absent or unable to inspect the loaded libraries
+        pass
+    if blas is None:
+        env = {v: os.environ[v] for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS",
+                                           "MKL_NUM_THREADS") if v in os.environ}
+        blas = {"library": "unknown", "threads": env or "library default"}
+    return {"cpu_model": model or platform.processor() or platform.machine(), "blas": blas}
+
+
 # ----------------------------------------------------------------------------
 # arms
 # ----------------------------------------------------------------------------
@@ -311,7 +350,8 @@ def run_reference(args):
             "data": "synthetic",
             "config": workload_config(inp, {"parallelism": "host cores"}),
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": f"{step.n} of {inp.T} tokens per step (fp64 NumPy oracle)"},
+                             "sample": f"{step.n} of {inp.T} tokens per step (fp64 NumPy oracle)",
+                             **host_info()},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -523,7 +563,8 @@ def run_ours(args):
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cpu_cores(),
                                 "kind": "oracle",
                                 "sample": f"{reps} whole batches of {inp.T} tokens, "
-                                          f"{el:.1f} s (fp64 NumPy oracle, weights pre-converted)"}
+                                          f"{el:.1f} s (fp64 NumPy oracle, weights pre-converted)",
+                                **host_info()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if nw > 1:

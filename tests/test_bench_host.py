@@ -62,3 +62,30 @@ def test_stage_bytes_by_hand():
 def test_arguments():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_host_info_fields():
+    info = bench.host_info()
+    assert isinstance(info["cpu_model"], str) and info["cpu_model"]
+    assert set(info["blas"]) == {"library", "threads"}
+
+
+def test_reference_arm_line(capsys):
+    """The reference arm (the oracle on the host cores) prints one JSON line with the
+    contract's keys; the tiny workload keeps it to a second."""
+    import json
+    assert bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3",
+                       "--warmup", "3"]) in (0, None)
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "impl", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["value"] > 0
+    assert d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["cpu_model"] and "threads" in cb["blas"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
