@@ -89,3 +89,18 @@ def test_reference_arm_line(capsys):
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert cb["cpu_model"] and "threads" in cb["blas"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_launch_accounting_matches_launch_lists():
+    """gpu_launches counts kernels per layer call as the ncu launch lists in profiles/ show
+    them: 9 at decode (one-CTA align, down expand with the combine fused) and 12 at prefill
+    (three-kernel align, separate combine after the in-place down expand)."""
+    from types import SimpleNamespace
+    from workloads import workload_by_name
+
+    def count(name):
+        c = workload_by_name(name)
+        return bench.launches_per_layer(SimpleNamespace(S=c["T"] * c["k"], **c))
+
+    assert count("gptoss20b_decode") == 9
+    assert count("gptoss20b_prefill") == 12
