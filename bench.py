@@ -67,6 +67,16 @@ def barrier():
 # ----------------------------------------------------------------------------
 # algorithmic bytes / flops per launch (the minimum data each stage must move)
 # ----------------------------------------------------------------------------
+# Stage names in the order of the layer's event marks ([0] .. [8]); the fused chain
+# (expand inside the grouped GEMMs) has an empty slot where the SwiGLU expand was.
+FUSED_STAGES = ["route", "align", "gather", "gate_up_shrink", "gate_up_gemm_expand_swiglu", None,
+                "down_shrink", "down_gemm_expand", "combine"]
+
+
+def chain_stages(fused: bool):
+    return FUSED_STAGES if fused else STAGES
+
+
 def workload_stats(ids, token_adapter, E: int):
     """Counts that set the algorithmic traffic: touched experts, (e, l) pairs, rows."""
     import numpy as np
@@ -84,90 +94,151 @@ def workload_stats(ids, token_adapter, E: int):
                 T_L=int(lora_tok.sum()), S_L=int(lora_tok.sum()) * k)
 
 
-def stage_bytes(st: dict, H: int, I: int, E: int, r: int) -> dict:
-    """Minimum bytes each stage reads + writes (bf16 = 2, fp32/int32 = 4)."""
+def stage_bytes(st: dict, H: int, I: int, E: int, r: int, fused: bool = False) -> dict:
+    """Minimum bytes each stage reads + writes (bf16 = 2, fp32/int32 = 4). z is fp32 by
+    slot in the unfused chain and a bf16 pair (4 bytes) by sorted row in the fused one."""
     S, T, S_L, T_L, P, Et = st["S"], st["T"], st["S_L"], st["T_L"], st["P"], st["E_touched"]
-    return {
+    common = {
         "route": T * E * 4 + S * 8,
         "align": S * 4 + T * 4 + S * 16,
         "gather": T * H * 2 + S * H * 2,
-        "gate_up_gemm": Et * 2 * I * H * 2 + S * H * 2 + S * 2 * I * 4,
         "gate_up_shrink": P * r * H * 2 + T_L * H * 2 + S_L * r * 4,
+        "down_shrink": P * r * I * 2 + S_L * I * 2 + S_L * r * 4,
+    }
+    if fused:
+        common.update({
+            # W1, gathered rows, B1, z in; h out
+            "gate_up_gemm_expand_swiglu": Et * 2 * I * H * 2 + S * H * 2 + P * 2 * I * r * 2
+            + S_L * r * 4 + S * I * 2,
+            # W2, h rows, B2, z in; fp32 rows out
+            "down_gemm_expand": Et * H * I * 2 + S * I * 2 + P * H * r * 2 + S_L * r * 4
+            + S * H * 4,
+            "combine": S * H * 4 + S * 8 + T * H * 2,
+        })
+        return common
+    common.update({
+        "gate_up_gemm": Et * 2 * I * H * 2 + S * H * 2 + S * 2 * I * 4,
         "gate_up_expand_swiglu": P * 2 * I * r * 2 + S_L * r * 4 + S * 2 * I * 4 + S * I * 2,
         "down_gemm": Et * H * I * 2 + S * I * 2 + S * H * 4,
-        "down_shrink": P * r * I * 2 + S_L * I * 2 + S_L * r * 4,
         "down_expand_combine": P * H * r * 2 + S_L * r * 4 + 2 * S_L * H * 4 + S * H * 4
         + S * 4 + T * H * 2,
-    }
+    })
+    return common
 
 
-def stage_flops(st: dict, H: int, I: int, r: int) -> dict:
+def stage_flops(st: dict, H: int, I: int, r: int, fused: bool = False) -> dict:
     S, S_L = st["S"], st["S_L"]
-    return {"gate_up_gemm": 2 * S * 2 * I * H, "down_gemm": 2 * S * H * I,
-            "gate_up_shrink": 2 * S_L * r * H, "down_shrink": 2 * S_L * r * I,
-            "gate_up_expand_swiglu": 2 * S_L * 2 * I * r, "down_expand_combine": 2 * S_L * H * r}
+    f = {"gate_up_shrink": 2 * S_L * r * H, "down_shrink": 2 * S_L * r * I}
+    if fused:
+        f["gate_up_gemm_expand_swiglu"] = 2 * S * 2 * I * H + 2 * S_L * 2 * I * r
+        f["down_gemm_expand"] = 2 * S * H * I + 2 * S_L * H * r
+        return f
+    f.update({"gate_up_gemm": 2 * S * 2 * I * H, "down_gemm": 2 * S * H * I,
+              "gate_up_expand_swiglu": 2 * S_L * 2 * I * r, "down_expand_combine": 2 * S_L * H * r})
+    return f
+
+
+GEMM_STAGES = ("gate_up_gemm", "down_gemm", "gate_up_gemm_expand_swiglu", "down_gemm_expand")
 
 
 # ----------------------------------------------------------------------------
-# clocks during the timed region
+# clocks during the timed region (read only: NVML queries, or nvidia-smi)
 # ----------------------------------------------------------------------------
-class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+class NvmlClock:
+    """The GPU's SM clock, power and clock-event reasons, read through NVML every
+    millisecond on a thread while started. Reading only: nothing is set."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: str):
+    def __init__(self, local_rank: int):
+        import ctypes
+        self.ok = False
         self.samples = []
-        self.proc = None
+        self._thread = None
+        self._stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, ValueError):
-            self.proc = None
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        if nv.nvmlInit_v2() != 0:
+            return
+        h = ctypes.c_void_p()
+        rc = 1
+        bus = pci_bus_id(local_rank)
+        if bus:
+            rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h))
+        if rc != 0:
+            rc = nv.nvmlDeviceGetHandleByIndex_v2(int(gpu_index_for_smi(local_rank)),
+                                                   ctypes.byref(h))
+        if rc != 0:
+            return
+        self.ct, self.nv, self.h = ctypes, nv, h
+        mx = ctypes.c_uint(0)
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # 1: the SM clock
+        self.max_mhz = mx.value
+        self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.ok = True
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.samples.append((time.time(), [p.strip() for p in line.split(",")]))
+    def read(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        c, p, r = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(c))
+        nv.nvmlDeviceGetPowerUsage(h, ct.byref(p))
+        self._reasons(h, ct.byref(r))
+        return time.time(), c.value, p.value / 1000.0, r.value
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self.read())
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 2.0:
+                time.sleep(0.001)
 
     def stop(self):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
     def summary(self, t0: float, t1: float):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        win = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not self.ok:
+            return None
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
         note = None
-        if not win and self.samples:  # timed region shorter than the sampling period
+        if not win and self.samples:
             mid = 0.5 * (t0 + t1)
-            win = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))]
             note = "timed region shorter than one sample; nearest sample used"
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
         for s in win:
-            try:
-                sm.append(float(s[1]))
-                mx.append(float(s[2]))
-            except (ValueError, IndexError):
-                continue
-            for n, v in zip(names, s[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        out = {"sm_mhz": statistics.median(sm) if sm else None,
-               "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-               "samples": len(sm)}
+            for bit, name in self.REASONS.items():
+                if s[3] & bit:
+                    reasons.add(name)
+        after = self.read()
+        out = {"sm_mhz": statistics.median(s[1] for s in win) if win else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons), "samples": len(win),
+               "power_w_max": max((s[2] for s in win), default=None), "source": "nvml, 1 ms",
+               "after_timed": {"sm_mhz": after[1],
+                               "reasons": sorted(n for b, n in self.REASONS.items() if after[3] & b)}}
         if note:
             out["note"] = note
         return out
+
+
+def pci_bus_id(local_rank: int):
+    """NVML's PCI bus id string of torch's device local_rank, or None."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(local_rank)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:  # attributes absent in this torch build
+        return None
 
 
 def gpu_index_for_smi(local_rank: int) -> str:
@@ -193,6 +264,8 @@ STAGE_SOURCES = {
     "gate_up_gemm": ["grouped_gemm.cu"], "down_gemm": ["grouped_gemm.cu"],
     "gate_up_shrink": ["lora_shrink.cu"], "down_shrink": ["lora_shrink.cu"],
     "gate_up_expand_swiglu": ["lora_expand.cu"], "down_expand_combine": ["lora_expand.cu"],
+    "gate_up_gemm_expand_swiglu": ["fused_gemm.cu"], "down_gemm_expand": ["fused_gemm.cu"],
+    "combine": ["lora_expand.cu"],
 }
 
 
@@ -348,7 +421,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": workload_config(inp, {"parallelism": "host cores"}),
+            "config": workload_config(inp, {"parallelism": f"replicas x{nw}" if nw > 1
+                                            else "single device"}),
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"{step.n} of {inp.T} tokens per step (fp64 NumPy oracle)",
                              **host_info()},
@@ -357,18 +431,9 @@ def run_reference(args):
     return 0
 
 
-def launches_per_layer(inp) -> int:
-    """Kernels one layer call launches: route, align (three kernels with many slots),
-    gather, two grouped GEMMs, the SwiGLU expand and the down expand (+ combine), plus
-    the two shrinks with adapters; with several rows per (expert, adapter) pair the down
-    expand adds in place and a separate combine kernel follows."""
-    nb = inp.E * (inp.L + 1) + 1
-    ctas = (inp.S + 511) // 512
-    multi = inp.S >= 2048 and 2 * nb <= inp.S and nb * ctas <= (1 << 22)
-    align = 3 if multi else 1  # the multi-CTA align is three kernels
-    if not inp.L:
-        return 6 + align
-    return 8 + align + (1 if inp.S >= 2 * inp.E * inp.L else 0)
+def launches_per_layer(m, inp) -> int:
+    """Kernels one layer call launches (routed from logits), as the library plans it."""
+    return m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)["launches"]
 
 
 def multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, n_layers, steps, warmup):
@@ -428,8 +493,109 @@ def multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, n_layers, steps, warm
             "graph_matches_eager": same, "device_error": err}
 
 
-def run_ours(args):
+class Layer:
+    """One workload's inputs on the device and a layer call over them."""
+
+    def __init__(self, m, name):
+        import torch
+        from workloads import make_workload_inputs
+        self.m = m
+        self.inp = inp = make_workload_inputs(name)
+        d = lambda t: None if t is None else t.to("cuda").contiguous()  # noqa: E731
+        self.W1, self.W2 = d(inp.W1), d(inp.W2)
+        self.lora = dict(A1=d(inp.A1), B1=d(inp.B1), A2=d(inp.A2), B2=d(inp.B2)) if inp.L else {}
+        self.x, self.lg, self.ta = d(inp.x), d(inp.logits), d(inp.token_adapter)
+        self.y = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
+        self.ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+        self.plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+
+    def __call__(self, events=None, adapters=True):
+        inp = self.inp
+        if adapters:
+            self.m.moe_lora_layer(self.x, self.W1, self.W2, logits=self.lg, k=inp.k,
+                                  token_adapter=self.ta, y=self.y, workspace=self.ws,
+                                  events=events, **self.lora)
+        else:  # the base MoE alone (L = 0): the same layer without adapters
+            self.m.moe_lora_layer(self.x, self.W1, self.W2, logits=self.lg, k=inp.k, y=self.y,
+                                  workspace=self.ws, events=events)
+
+
+def timed_steps(fn, steps, stream):
+    """Seconds for `steps` calls of fn on `stream`, by CUDA events recorded on it."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def stage_table(layer, kernel_steps, stream, peaks):
+    """Per-stage CUDA-event durations (a separate instrumented pass with events between the
+    launches) against each stage's algorithmic bytes and flops."""
     import numpy as np
+    import torch
+    inp, fused = layer.inp, bool(layer.plan["fused_expand"])
+    names = chain_stages(fused)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    for ev in evs:  # torch creates CUDA events lazily, on first record
+        ev.record(stream)
+    torch.cuda.synchronize()
+    acc = [0.0] * len(names)
+    for _ in range(kernel_steps):
+        layer(events=evs)
+        torch.cuda.synchronize()
+        for i in range(len(names)):
+            acc[i] += evs[i].elapsed_time(evs[i + 1])
+    ids = torch.topk(inp.logits, inp.k, dim=1).indices.numpy()  # accounting only
+    st = workload_stats(ids, inp.token_adapter.numpy() if inp.L else np.full(inp.T, -1), inp.E)
+    sb = stage_bytes(st, inp.H, inp.I, inp.E, inp.r, fused)
+    sf = stage_flops(st, inp.H, inp.I, inp.r, fused)
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    kernels = {}
+    for name, a in zip(names, acc):
+        if name is None:
+            continue
+        ms = a / kernel_steps
+        gbs = sb[name] / (ms * 1e-3) / 1e9 if ms > 0 else None
+        k = {"us": round(ms * 1e3, 2), "alg_bytes": int(sb[name]),
+             "GB_s": round(gbs, 1) if gbs else None,
+             "hbm_frac": round(gbs / hbm, 3) if gbs else None}
+        if name in sf and ms > 0:
+            k["TFLOP_s"] = round(sf[name] / (ms * 1e-3) / 1e12, 2)
+            if name in GEMM_STAGES:
+                k["tensor_frac_of_sustained"] = round(k["TFLOP_s"] / tflops, 3)
+        kernels[name] = k
+    return kernels, sb
+
+
+def measure(layer, steps, warmup, kernel_steps, stream, peaks):
+    """ms per step (CUDA events over exactly `steps` calls after `warmup`), the base MoE
+    alone for the marginal cost of the adapters, and the per-stage table."""
+    import torch
+    for _ in range(warmup):
+        layer()
+    torch.cuda.synchronize()
+    el = timed_steps(layer, steps, stream)
+    out = {"tokens_s": layer.inp.T * steps / el, "ms_per_step": 1e3 * el / steps,
+           "fused_expand": layer.plan["fused_expand"], "launches": layer.plan["launches"]}
+    if layer.inp.L:
+        for _ in range(warmup):
+            layer(adapters=False)
+        torch.cuda.synchronize()
+        base = timed_steps(lambda: layer(adapters=False), steps, stream)
+        out["base_moe_ms_per_step"] = 1e3 * base / steps
+        out["lora_marginal_us"] = round(1e6 * (el - base) / steps, 2)
+    out["kernels"], _ = stage_table(layer, kernel_steps, stream, peaks)
+    if layer.m.get_error(layer.ws):
+        raise RuntimeError(f"device error word set on {layer.inp.name}")
+    return out
+
+
+def run_ours(args):
     import torch
     import torch.distributed as dist
 
@@ -438,43 +604,30 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     import expert_adapter_gemms_gb300 as m
-    from workloads import make_workload_inputs
 
-    inp = make_workload_inputs(args.workload)
-    d = lambda t: None if t is None else t.to("cuda").contiguous()  # noqa: E731
-    W1, W2 = d(inp.W1), d(inp.W2)
-    lora = dict(A1=d(inp.A1), B1=d(inp.B1), A2=d(inp.A2), B2=d(inp.B2)) if inp.L else {}
-    x_d, lg_d, ta_d = d(inp.x), d(inp.logits), d(inp.token_adapter)
-    y_d = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
-    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
-    bm_base, bm_lora = m.moe_lora_layer_tiles(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    layer = Layer(m, args.workload)
+    inp = layer.inp
     stream = torch.cuda.current_stream()
+    peaks, peak_kind = measured_peaks()
 
-    def step(events=None):
-        m.moe_lora_layer(x_d, W1, W2, logits=lg_d, k=inp.k, token_adapter=ta_d, y=y_d,
-                         workspace=ws, events=events, **lora)
-
-    clocks = ClockSampler(gpu_index_for_smi(local))
+    clocks = NvmlClock(local)
+    clocks.start()  # returns once the first sample is in
     for _ in range(args.warmup):
-        step()
+        layer()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    el_s = timed_steps(layer, args.steps, stream)
     t1 = time.time()
     barrier()
-    el_s = e0.elapsed_time(e1) / 1e3
     el_max, tokens_all = combine_ranks(el_s, inp.T * args.steps)
     value = tokens_all / el_max
     clk = clocks.summary(t0, t1)
     clocks.stop()
-    err = m.get_error(ws)
+    if clk is None:
+        clk = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["NVML unavailable"], "samples": 0}
+    err = m.get_error(layer.ws)
     if err:
         raise RuntimeError(f"device error word {err:#x} after the timed steps")
 
@@ -489,74 +642,47 @@ def run_ours(args):
     d2h = io.y_host.numel() * io.y_host.element_size()
 
     def e2e_step():
-        m.moe_lora_layer_host(io, W1, W2, k=inp.k, workspace=ws, **lora)
+        m.moe_lora_layer_host(io, layer.W1, layer.W2, k=inp.k, workspace=layer.ws, **layer.lora)
 
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
     barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_max, e2e_tokens = combine_ranks(e0.elapsed_time(e1) / 1e3, inp.T * args.steps)
-    if not torch.equal(io.y_host, y_d.cpu()):
+    e2e_max, e2e_tokens = combine_ranks(timed_steps(e2e_step, args.steps, stream),
+                                        inp.T * args.steps)
+    if not torch.equal(io.y_host, layer.y.cpu()):
         raise RuntimeError("the host-staged step's y differs from the device-pointer call's")
 
-    # per-stage durations (events between the launches; a separate instrumented pass)
-    nst = len(STAGES)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
-    for ev in evs:  # torch creates CUDA events lazily, on first record
-        ev.record(stream)
-    torch.cuda.synchronize()
-    acc = [0.0] * nst
-    for i in range(args.kernel_steps):
-        step(events=evs)
-        torch.cuda.synchronize()
-        for s in range(nst):
-            acc[s] += evs[s].elapsed_time(evs[s + 1])
-    stage_ms = [a / args.kernel_steps for a in acc]
-
-    ids = torch.topk(inp.logits, inp.k, dim=1).indices.numpy()  # accounting only
-    st = workload_stats(ids, inp.token_adapter.numpy() if inp.L else np.full(inp.T, -1), inp.E)
-    sb = stage_bytes(st, inp.H, inp.I, inp.E, inp.r)
-    sf = stage_flops(st, inp.H, inp.I, inp.r)
-    peaks, peak_kind = measured_peaks()
+    # per stage, and the base MoE alone
+    head = measure(layer, max(args.steps, 20), 3, args.kernel_steps, stream, peaks)
+    kernels = head["kernels"]
+    dname = max(kernels, key=lambda n: kernels[n]["us"])
+    dk = kernels[dname]
     hbm = float(peaks["hbm_gbs"])
-    kernels = {}
-    for name, ms in zip(STAGES, stage_ms):
-        gbs = sb[name] / (ms * 1e-3) / 1e9 if ms > 0 else None
-        kernels[name] = {"us": round(ms * 1e3, 2), "alg_bytes": int(sb[name]),
-                         "GB_s": round(gbs, 1) if gbs else None,
-                         "hbm_frac": round(gbs / hbm, 3) if gbs else None}
-        if name in sf and ms > 0:
-            kernels[name]["TFLOP_s"] = round(sf[name] / (ms * 1e-3) / 1e12, 2)
-    dom = max(range(nst), key=lambda i: stage_ms[i])
-    dname = STAGES[dom]
-    bound = "hbm"  # at decode every stage streams weights; see the design notes
-    achieved = sb[dname] / (stage_ms[dom] * 1e-3) / 1e9
-    roof = {"kernel": dname, "bound": bound, "achieved": round(achieved, 1),
-            "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+    achieved = dk["alg_bytes"] / (dk["us"] * 1e-6) / 1e9
+    roof = {"kernel": dname, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4),
             "traffic": profiled_traffic(dname, inp.name),
             "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
-            "alg_bytes_per_launch": int(sb[dname])}
+            "alg_bytes_per_launch": dk["alg_bytes"]}
 
+    parallelism = f"replicas x{nw}" if nw > 1 else "single device"
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": nw, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * el_max / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": workload_config(inp, {
-                "parallelism": f"replicas x{nw}" if nw > 1 else "single GPU",
-                "bm_base": bm_base, "bm_lora": bm_lora,
-                "l2": "inputs larger than L2: %.2f GB of weights streamed per step" % (
-                    (sb["gate_up_gemm"] + sb["down_gemm"]) / 1e9)}),
+            "data": "synthetic", "config": workload_config(inp, {"parallelism": parallelism}),
+            "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step" % (
+                (inp.E * 3 * inp.I * inp.H * 2) / 1e9),
+            "plan": layer.plan,
             "e2e": {"value": e2e_tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * launches_per_layer(inp),
-            "clocks": clk, "roofline": roof, "kernels": kernels}
+            "gpu_launches": args.steps * layer.plan["launches"],
+            "clocks": clk, "roofline": roof, "kernels": kernels,
+            "base_moe_ms_per_step": head.get("base_moe_ms_per_step"),
+            "lora_marginal_us": head.get("lora_marginal_us")}
     if args.layers > 1:
-        line["multi_layer"] = multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, args.layers,
+        line["multi_layer"] = multi_layer(m, inp, layer.W1, layer.W2, layer.lora, layer.lg,
+                                          layer.ta, layer.x, layer.ws, args.layers,
                                           max(10, args.steps // 4), max(3, args.warmup // 4))
     if rank == 0 and nw == 1 and not args.no_cpu_baseline:
         rate, reps, el = cpu_oracle_rate(inp, args.cpu_seconds)
@@ -565,6 +691,25 @@ def run_ours(args):
                                 "sample": f"{reps} whole batches of {inp.T} tokens, "
                                           f"{el:.1f} s (fp64 NumPy oracle, weights pre-converted)",
                                 **host_info()}
+    # every other configuration of the pages' workloads: throughput and per-stage roofline
+    # fractions (fewer steps; no CPU baseline)
+    if rank == 0 and args.workloads != "none":
+        from workloads import WORKLOAD_NAMES
+        names = WORKLOAD_NAMES if args.workloads == "all" else args.workloads.split(",")
+        wl = {inp.name: {k: v for k, v in head.items()}}
+        del layer
+        torch.cuda.empty_cache()
+        for name in names:
+            if name in wl:
+                continue
+            other = Layer(m, name)
+            wl[name] = measure(other, args.extra_steps, 5, max(5, args.kernel_steps // 5),
+                               stream, peaks)
+            wl[name]["l2"] = ("fits in L2: launch-bound" if name == "tiny"
+                              else "inputs larger than L2")
+            del other
+            torch.cuda.empty_cache()
+        line["workloads"] = wl
     if rank == 0:
         print(json.dumps(line), flush=True)
     if nw > 1:
@@ -585,6 +730,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=4,
                     help="also chain this many layers (eager and one CUDA graph); < 2 skips it")
+    ap.add_argument("--workloads", default="all",
+                    help="'all', 'none' or a comma list: other workloads measured after the "
+                         "headline one (fewer steps, no CPU baseline)")
+    ap.add_argument("--extra-steps", type=int, default=20)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

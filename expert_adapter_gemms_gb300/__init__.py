@@ -27,6 +27,7 @@ from .api import (  # noqa: F401
     moe_lora_host_io_layout,
     moe_lora_layer,
     moe_lora_layer_host,
+    moe_lora_layer_plan,
     moe_lora_layer_tiles,
     moe_lora_workspace_size,
     moe_topk_softmax,

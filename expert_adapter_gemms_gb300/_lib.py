@@ -46,7 +46,14 @@ class LayerOpts(ctypes.Structure):
     _fields_ = [("bm_base", ctypes.c_int32), ("bm_lora", ctypes.c_int32),
                 ("disable_pdl", ctypes.c_int32), ("num_events", ctypes.c_int32),
                 ("events", ctypes.POINTER(ctypes.c_void_p)), ("adapter_ranks", ctypes.c_void_p),
-                ("gate_up_slices", ctypes.c_int32)]
+                ("gate_up_slices", ctypes.c_int32), ("expand_mode", ctypes.c_int32),
+                ("wait_limit_ns", ctypes.c_int64)]
+
+
+class LayerPlan(ctypes.Structure):
+    _fields_ = [("bm_base", ctypes.c_int32), ("bm_lora", ctypes.c_int32),
+                ("expert_major_rows", ctypes.c_int32), ("fused_expand", ctypes.c_int32),
+                ("launches", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -74,6 +81,8 @@ SIGNATURES = {
                                _I, _I, _P, _I, _P, _SZ, ctypes.POINTER(LayerOpts), _P]),
     "moe_lora_layer_tiles": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32),
                                   ctypes.POINTER(ctypes.c_int32)]),
+    "moe_lora_layer_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(LayerOpts),
+                                 ctypes.POINTER(LayerPlan)]),
     "moe_lora_host_io_layout": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int64),
                                      ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "moe_lora_layer_host": (_I, [_P, _P, _P, _SZ, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,

@@ -13,7 +13,7 @@ from typing import Optional, Sequence
 import torch
 
 from . import _lib as L_
-from ._lib import AlignDesc, LayerOpts, check, lib, ptr, stream_handle
+from ._lib import AlignDesc, LayerOpts, LayerPlan, check, lib, ptr, stream_handle
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None, shape=None):
@@ -236,6 +236,23 @@ def moe_lora_layer_tiles(T: int, k: int, E: int, L: int, H: int, I: int, r: int)
     return b.value, l_.value
 
 
+def moe_lora_layer_plan(T: int, k: int, E: int, L: int, H: int, I: int, r: int, *,
+                        bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
+                        gate_up_slices: int = 1, adapter_ranks: bool = False,
+                        expand_mode: int = 0) -> dict:
+    """How the layer runs this shape with these options: tiles, expert-major chunk rows,
+    whether the expand is fused into the grouped GEMMs, and kernels per call."""
+    opts = LayerOpts()
+    opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
+    opts.gate_up_slices, opts.expand_mode = gate_up_slices, expand_mode
+    if adapter_ranks:  # only whether an array is given matters to the plan
+        opts.adapter_ranks = 1
+    out = LayerPlan()
+    check(lib().moe_lora_layer_plan(T, k, E, L, H, I, r, ctypes.byref(opts), ctypes.byref(out)),
+          "moe_lora_layer_plan")
+    return {f: getattr(out, f) for f, _ in LayerPlan._fields_}
+
+
 def new_workspace(T: int, k: int, E: int, L: int, H: int, I: int, r: int, device="cuda"):
     n = moe_lora_workspace_size(T, k, E, L, H, I, r)
     if n == 0:
@@ -269,11 +286,14 @@ def _layer_weights(H: int, W1, W2, A1, B1, A2, B2, gate_up_slices: int):
 
 
 def _layer_opts(Ln: int, bm_base: int, bm_lora: int, disable_pdl: bool, events,
-                gate_up_slices: int, adapter_ranks):
+                gate_up_slices: int, adapter_ranks, wait_limit_ns: int = 0,
+                expand_mode: int = 0):
     """The layer options struct, and the event array it points to (keep it alive)."""
     opts = LayerOpts()
     opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
     opts.gate_up_slices = gate_up_slices
+    opts.wait_limit_ns = int(wait_limit_ns)
+    opts.expand_mode = int(expand_mode)
     if adapter_ranks is not None:
         _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (Ln,))
         opts.adapter_ranks = ptr(adapter_ranks)
@@ -293,10 +313,13 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
                    y_fp32: bool = False, workspace: Optional[torch.Tensor] = None,
                    bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
                    events: Optional[Sequence] = None, gate_up_slices: int = 1,
-                   adapter_ranks: Optional[torch.Tensor] = None) -> torch.Tensor:
+                   adapter_ranks: Optional[torch.Tensor] = None,
+                   wait_limit_ns: int = 0, expand_mode: int = 0) -> torch.Tensor:
     """The whole fused MoE-LoRA layer; returns y [T, H]. gate_up_slices=2: separate gate
     and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r].
-    adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r)."""
+    adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r).
+    wait_limit_ns (tests of the give-up path): 0 default 4 s, < 0 give up at once.
+    expand_mode: 0 the library picks, 1 the expand in kernels of its own."""
     _need(x, "x", torch.bfloat16, 2)
     T, H = x.shape
     E, I, Ln, r = _layer_weights(H, W1, W2, A1, B1, A2, B2, gate_up_slices)
@@ -317,7 +340,7 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     if workspace is None:
         workspace = new_workspace(T, k, E, Ln, H, I, r, x.device)
     opts, _ev = _layer_opts(Ln, bm_base, bm_lora, disable_pdl, events, gate_up_slices,
-                            adapter_ranks)
+                            adapter_ranks, wait_limit_ns, expand_mode)
     check(lib().moe_lora_layer_ex(
         ptr(x), ptr(logits), ptr(topk_ids), ptr(topk_w), ptr(token_adapter), T, H, I, E, k,
         ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2), ptr(B2), Ln, r, ptr(y), int(y_fp32),
@@ -383,7 +406,8 @@ def moe_lora_layer_host(io: HostIO, W1: torch.Tensor, W2: torch.Tensor, *, k: in
                         workspace: Optional[torch.Tensor] = None, bm_base: int = 0,
                         bm_lora: int = 0, disable_pdl: bool = False,
                         events: Optional[Sequence] = None, gate_up_slices: int = 1,
-                        adapter_ranks: Optional[torch.Tensor] = None) -> torch.Tensor:
+                        adapter_ranks: Optional[torch.Tensor] = None,
+                        expand_mode: int = 0) -> torch.Tensor:
     """One step from host memory: copies io's input block to the device, runs the layer
     (routed from io.logits) and copies y back into io.y_host, all enqueued on the current
     stream. Returns io.y_host, valid once the stream has been synchronised."""
@@ -396,7 +420,7 @@ def moe_lora_layer_host(io: HostIO, W1: torch.Tensor, W2: torch.Tensor, *, k: in
     if workspace is None:
         workspace = new_workspace(T, k, E, Ln, H, I, r, io.staging.device)
     opts, _ev = _layer_opts(Ln, bm_base, bm_lora, disable_pdl, events, gate_up_slices,
-                            adapter_ranks)
+                            adapter_ranks, expand_mode=expand_mode)
     check(lib().moe_lora_layer_host(
         ptr(io.in_host), ptr(io.y_host), ptr(io.staging), io.staging.numel(),
         int(io.with_adapter), T, H, I, E, k, ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2),

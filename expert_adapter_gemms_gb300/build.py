@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmoe_lora.so")
-SOURCES = ["route.cu", "align.cu", "grouped_gemm.cu", "lora_shrink.cu", "lora_expand.cu",
-           "layer.cu", "layer_noalloc.cu"]
+SOURCES = ["route.cu", "align.cu", "grouped_gemm.cu", "fused_gemm.cu", "lora_shrink.cu",
+           "lora_expand.cu", "layer.cu", "layer_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -537,14 +537,13 @@ static int launch_align_t(const int* ids, const int* token_adapter, const moe_lo
                           const AlignLayout& a, cudaStream_t stream, bool pdl) {
   AlignView v = align_view(al->buf, a);
   const AlignSmem plan = align_smem_plan(a.S, a.nbuckets, NT);
-  static std::atomic<int> configured[64];
-  int dev = 0;
-  ML_CHECK_CUDA(cudaGetDevice(&dev));
-  if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+  static std::atomic<uint64_t> configured[kMaxDevices];
+  int st = once_per_context(configured, [] {
     ML_CHECK_CUDA(cudaFuncSetAttribute(align_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)(kAlignSmemBudget + 16 * 1024)));
-    configured[dev].store(1, std::memory_order_release);
-  }
+    return MOE_LORA_OK;
+  });
+  if (st != MOE_LORA_OK) return st;
   return launch_pdl(align_kernel<NT>, 1, NT, plan.bytes, stream, pdl, ids, token_adapter, v,
                     al->T, al->k, al->E, al->L, al->bm_base, al->bm_lora, a.S, a.nbuckets,
                     a.key_bits, a.slot_bits);

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/moe_lora.h"
@@ -31,6 +32,30 @@ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Checks once per device that it is an sm_103 part (the only target compiled).
 int check_device();
 int num_sms();
+
+// An id of the CUDA context current on this thread; it changes when the primary
+// context is destroyed and re-created (cudaDeviceReset), so state that belongs to a
+// context -- function attributes, the device address of a __device__ array -- is
+// cached per (device, context id). 0 when no context is current or the id cannot be
+// read.
+uint64_t current_context_id();
+
+constexpr int kMaxDevices = 64;
+
+// Runs `set` (which returns a status) unless it already succeeded in the current
+// context of the current device; `seen` holds, per device, the context id it last
+// succeeded in. Concurrent first calls may both run `set`: it must be idempotent.
+template <typename F>
+inline int once_per_context(std::atomic<uint64_t> (&seen)[kMaxDevices], F&& set) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_LORA_ERR_CUDA;
+  const uint64_t id = current_context_id();
+  const bool cache = dev >= 0 && dev < kMaxDevices && id != 0;
+  if (cache && seen[dev].load(std::memory_order_acquire) == id) return MOE_LORA_OK;
+  const int st = set();
+  if (st == MOE_LORA_OK && cache) seen[dev].store(id, std::memory_order_release);
+  return st;
+}
 
 // Launch with programmatic dependent launch (the kernel may start while its
 // predecessor on the stream drains; it must call pdl_wait() before touching
@@ -231,14 +256,18 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar_addr, uint32_t pa
       : "memory");
   return done;
 }
-// Waits for the phase of `parity` to complete; false if the wall-time limit passed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase of `parity` to complete; false once `limit_ns` of wall time has
+// passed. limit_ns == 0 gives up at the first unsuccessful poll (a test of the give-up
+// paths uses it; the layer passes the default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
+  if (limit_ns == 0) return false;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -40,7 +40,7 @@ struct GemmCfg {
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-  static_assert((2 * STAGES + 4) * 8 + 16 <= 256, "barrier area");
+  static_assert((2 * STAGES + 5) * 8 + 16 <= 256, "barrier area");
   static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;  // one fp32 accumulator
   static constexpr uint32_t kTmemCols = 2 * kAccCols;     // two, used alternately
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const __grid_constant__ CUtensorMap tm_a, int* __restrict__ hdr,
                         const int4* __restrict__ tiles, const int* __restrict__ expert_begin,
                         float* __restrict__ out, int N, int K, int n_wblocks, int max_tiles,
-                        int mode, int early) {
+                        int mode, int early, unsigned long long wait_ns) {
   using C = GemmCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tmem_full = empty + STAGES;  // [2]: one per accumulator
   uint64_t* tmem_empty = tmem_full + 2;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 2);
+  uint64_t* mma_done = tmem_empty + 2;   // after an abort: every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // expert-major: first row, row count
 
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tmem_full[a], 1);
       mbar_init(&tmem_empty[a], 4);  // one arrival per epilogue warp
     }
+    mbar_init(mma_done, 1);
     *s_abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t ph = (g / STAGES) & 1;
           uint8_t* sw = smem + s * C::kStageBytes;
           if (g >= pre) {
-            if (*s_abort || !mbar_wait_bounded(&empty[s], ph ^ 1)) {
+            if (*s_abort || !mbar_wait_bounded(&empty[s], ph ^ 1, wait_ns)) {
               *s_abort = 1;
               break;
             }
@@ -298,7 +300,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       if (*s_abort) {  // drain own copies in flight before the CTA may exit
-        for (int g = issued - 1; g >= 0 && g >= issued - STAGES; --g)
+        // prefetched weight stages whose token copy was never issued miss one arrival
+        for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
+        for (int g = (issued > pre ? issued : pre) - 1; g >= 0 && g >= issued - STAGES; --g)
           mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1);
       }
     }
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t acc = tmem + static_cast<uint32_t>(a * C::kAccCols);
         const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>((rows + 15) & ~15));
         if (j >= 2) {  // the epilogue must have read this buffer's previous job
-          if (!mbar_wait_bounded(&tmem_empty[a], ((j >> 1) - 1) & 1)) {
+          if (!mbar_wait_bounded(&tmem_empty[a], ((j >> 1) - 1) & 1, wait_ns)) {
             *s_abort = 1;
             break;
           }
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int g = j * nk + kb;
           const int s = g % STAGES;
           const uint32_t ph = (g / STAGES) & 1;
-          if (*s_abort || !mbar_wait_bounded(&full[s], ph)) {
+          if (*s_abort || !mbar_wait_bounded(&full[s], ph, wait_ns)) {
             *s_abort = 1;
             break;
           }
@@ -337,6 +341,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_commit(&tmem_full[a]);  // fires when every MMA issued above has completed
       }
+      if (*s_abort) {  // MMAs still in flight read shared memory and write TMEM: drain them
+        tc_commit(mma_done);
+        mbar_wait_bounded(mma_done, 0);
+      }
     }
   } else {
     // epilogue: warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
@@ -345,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
       const int a = j & 1;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1) ? 1 : 0);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1, wait_ns) ? 1 : 0);
       if (!ok) *s_abort = 1;
       if (!ok || *s_abort) break;
       tc_fence_after();
@@ -402,7 +410,7 @@ static EncodeTiledFn get_encode_fn() {
 }
 
 // bf16 tensor map, innermost dimension K (contiguous), 128-byte swizzle, box {64, box_rows[, 1]}.
-static int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                           const uint64_t* strides_bytes, const uint32_t* box) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return MOE_LORA_ERR_CUDA;
@@ -422,16 +430,15 @@ static int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint
 template <int BN, int STAGES>
 static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const AlignView& v,
                          int max_tiles, int E, int N, int K, float* out, cudaStream_t stream,
-                         bool pdl, int mode, int early) {
+                         bool pdl, int mode, int early, unsigned long long wait_ns) {
   using C = GemmCfg<BN, STAGES>;
-  static std::atomic<int> configured[64];
-  int dev = 0;
-  ML_CHECK_CUDA(cudaGetDevice(&dev));
-  if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+  static std::atomic<uint64_t> configured[kMaxDevices];
+  int st = once_per_context(configured, [] {
     ML_CHECK_CUDA(cudaFuncSetAttribute(grouped_gemm_kernel<BN, STAGES>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
-    configured[dev].store(1, std::memory_order_release);
-  }
+    return MOE_LORA_OK;
+  });
+  if (st != MOE_LORA_OK) return st;
   const int n_wblocks = ceil_div(N, kBM);
   int64_t grid = (int64_t)(mode == kModeExpert ? E : max_tiles) * n_wblocks;
   if (mode == kModePersistent) {  // one resident CTA per SM slot, each looping over jobs
@@ -444,12 +451,14 @@ static int launch_gemm_t(const CUtensorMap& tw, const CUtensorMap& ta, const Ali
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
   return launch_pdl(grouped_gemm_kernel<BN, STAGES>, dim3((unsigned)grid), kGemmThreads,
                     C::kSmemBytes, stream, pdl, tw, ta, v.hdr, (const int4*)v.tiles,
-                    (const int*)v.expert_begin, out, N, K, n_wblocks, max_tiles, mode, early);
+                    (const int*)v.expert_begin, out, N, K, n_wblocks, max_tiles, mode, early,
+                    wait_ns);
 }
 
 int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora_align_t* al,
                              const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
-                             bool pdl, bool early, int expert_major_bn) {
+                             bool pdl, bool early, int expert_major_bn,
+                             unsigned long long wait_ns) {
   if (a.S == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   // expert-major when asked; else persistent for large token tiles (prefill), whose
@@ -473,11 +482,11 @@ int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora
     if (st != MOE_LORA_OK) return st;
   }
   switch (bn) {
-    case 16: return launch_gemm_t<16, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
-    case 32: return launch_gemm_t<32, 5>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
-    case 64: return launch_gemm_t<64, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
-    case 128: return launch_gemm_t<128, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
-    case 256: return launch_gemm_t<256, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea);
+    case 16: return launch_gemm_t<16, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea, wait_ns);
+    case 32: return launch_gemm_t<32, 5>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea, wait_ns);
+    case 64: return launch_gemm_t<64, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea, wait_ns);
+    case 128: return launch_gemm_t<128, 6>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea, wait_ns);
+    case 256: return launch_gemm_t<256, 4>(tw, ta, v, a.max_tiles, al->E, N, K, out, stream, pdl, em, ea, wait_ns);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
 }

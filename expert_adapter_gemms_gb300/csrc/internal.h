@@ -15,6 +15,18 @@ int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_
 int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& a, int H,
                   void* xs, cudaStream_t stream, bool pdl, bool trigger_first);
 
+// bf16 tensor map over `rank` (2 or 3) dimensions, innermost first (dims[0] contiguous),
+// byte strides of dimensions 1.. in strides_bytes, box `box`, 128-byte swizzle, zero fill
+// out of bounds. Host only; no device work.
+int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                   const uint64_t* strides_bytes, const uint32_t* box);
+
+// silu(v) = v / (1 + exp(-v)) with the hardware exponential and a reciprocal-based
+// divide (CUDA's __expf, __fdividef): a few fp32 ulps, far below the bf16 rounding of the
+// SwiGLU output; for v below about -87 it returns 0 where the exact form gives a value
+// under 1e-36.
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+
 // Tensor maps are built on the host for every call (cheap; no device work).
 int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_align_t* al,
                         const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
@@ -22,6 +34,43 @@ int launch_grouped_gemm(const void* a_sorted, const void* W, const moe_lora_alig
 
 int launch_shrink(const void* X, int rows_are_slots, const void* A, const moe_lora_align_t* al,
                   const AlignLayout& a, int K, int r, float* Z, cudaStream_t stream, bool pdl);
+
+// ---- the shifted z buffer of the fused expand (fused_gemm.cu) ----
+// z of sorted row j of pair (e, l) is row j + (e L + l + 1) gap, as bf16 high parts in
+// columns [0, r) and the bf16 remainders in [lo_off, lo_off + r); columns [r, rp16) of each
+// half are zero, and so are the gap rows before and after every pair written.
+struct ZPadLayout {
+  int rp16;      // rank rounded up to 16
+  int zw;        // row width (bf16 elements, a multiple of 64)
+  int lo_off;    // first column of the low parts
+  int zk;        // > 0: high and low share one 64-column row (zk K16 steps each)
+  int zchunks;   // LoRA stages per adapter run in a token tile
+  int gap;       // zero rows between pairs (>= the fused GEMM's token tile)
+  int64_t rows;  // rows of the buffer
+};
+ZPadLayout zpad_layout(int S, int E, int L, int r, int gap);
+
+// Where a shrink publishes z: Z [S, r] fp32 by slot (p == nullptr), or the shifted buffer.
+struct ZPadOut {
+  __nv_bfloat16* p;
+  int zw, lo_off, rp16, gap, L;
+  const int* row_expert;
+  const int* row_adapter;
+};
+
+// The fused expand: the grouped GEMM over sorted rows a_sorted [S, K] and W [E, N_w, K]
+// with, for rows with an adapter, the K-steps of z (the shifted buffer) against B
+// [L, E, N_w, r]. glu: N_w = 2I and out is h [S, I] bf16 = silu(gate) * up; else out is
+// [S, N_w] fp32. B or zpad null (or L = 0): the base GEMM only. `early`: everything but z
+// may be read before griddepcontrol.wait.
+int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const void* zpad,
+                      const ZPadLayout& zl, const moe_lora_align_t* al, const AlignLayout& a,
+                      int N_w, int K, int r, bool glu, void* out, cudaStream_t stream, bool pdl,
+                      bool early, int expert_major_bn, unsigned long long wait_ns);
+
+// y[t] = sum_j w[t, j] O[row(t, j)] (j ascending) over O [S, N] fp32 by sorted row.
+int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
+                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl);
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,
                   int N, int r, int epilogue, float* base, void* out, int out_fp32,
@@ -34,13 +83,17 @@ int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, con
 // slice, the unit that al->adapter_ranks truncates.
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
                        const moe_lora_align_t* al, const AlignLayout& a, int K, int r, int rs,
-                       float* Z, cudaStream_t stream, bool pdl, bool early);
+                       float* Z, cudaStream_t stream, bool pdl, bool early,
+                       unsigned long long wait_ns = kWaitLimitNs, const ZPadOut* zpad = nullptr);
 // expert_major_bn > 0: one CTA per (expert, weight block) taking the expert's rows in
 // chunks of that many rows (16..256), which lets the weights stream before the align
 // tables exist; 0: one CTA per (token tile of bm_base rows, weight block).
+// wait_ns: limit of the main-loop mbarrier waits (the shrink's short-K slab wait too);
+// the waits that drain copies and MMAs before a CTA exits always use kWaitLimitNs.
 int launch_grouped_gemm_impl(const void* a_sorted, const void* W, const moe_lora_align_t* al,
                              const AlignLayout& a, int N, int K, float* out, cudaStream_t stream,
-                             bool pdl, bool early, int expert_major_bn);
+                             bool pdl, bool early, int expert_major_bn,
+                             unsigned long long wait_ns = kWaitLimitNs);
 int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al,
                        const AlignLayout& a, int N, int r, int epilogue, float* base, void* out,
                        int out_fp32, const float* topk_w, cudaStream_t stream, bool pdl,

@@ -10,8 +10,10 @@
 // host, no device count is read back, and every size is a runtime argument, so a
 // new token count never triggers a compile or a module load. Intermediates live
 // in the caller's workspace, carved here.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -21,10 +23,35 @@ namespace moe_lora {
 // device checks
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
 std::atomic<int> g_dev_sms[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
 }  // namespace
+
+uint64_t current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!g_ctx_current || !g_ctx_id) return 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  unsigned long long id = 0;
+  if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id);
+}
 
 int check_device() {
   int dev = 0;
@@ -73,39 +100,89 @@ static void pick_tiles(int T, int k, int E, int L, int32_t* bm_base, int32_t* bm
   *bm_lora = S <= 2 * (int64_t)E * (L > 0 ? L : 1) ? 8 : 16;
 }
 
+// Rows per expert-major chunk: with few rows per expert (decode) each grouped-GEMM CTA
+// takes one (expert, weight block) and all of the expert's rows, so it can stream its
+// weights before routing and alignment have finished; 0: token tiles.
+static int expert_major_rows(int T, int k, int E) {
+  const int64_t per_expert = ((int64_t)T * k + E - 1) / E;
+  return per_expert <= 16 ? 32 : per_expert <= 32 ? 64 : 0;
+}
+
+// The fused expand's token tile (and so the zero gap of its shifted z buffers) that the
+// heuristics give a shape: the expert-major chunk, else the token tile capped at 128 rows
+// (the gate and up accumulators of two jobs fill TMEM at 128).
+static int fused_gap(int T, int k, int E, int L) {
+  const int em = expert_major_rows(T, k, E);
+  if (em) return em;
+  int32_t hb, hl;
+  pick_tiles(T, k, E, L, &hb, &hl);
+  return hb < 128 ? hb : 128;
+}
+
 struct LayerPlan {
   AlignLayout al;
-  int bm_base, bm_lora;
-  int64_t off_align, off_ids, off_w, off_xs, off_G, off_Z1, off_h, off_Z2, off_O, total;
+  int bm_base, bm_lora, em_bn;
+  bool fused;    // expand (and SwiGLU) inside the grouped GEMMs
+  ZPadLayout z;  // the shifted z buffers of the fused chain (both the same shape)
+  int launches;  // kernels of one call routed from logits
+  int64_t off_align, off_ids, off_w, off_xs, off_G, off_Z1, off_h, off_Z2, off_O, off_Z1p,
+      off_Z2p, total;
   bool valid;
 };
 
-static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r, int bm_base,
-                            int bm_lora) {
+// The workspace layout depends on the shape only; the chain (fused or not) and the tiles
+// may also depend on the options. The fp32 gate_up output G of the unfused chain and the
+// two shifted z buffers of the fused chain share one region.
+static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r,
+                            const moe_lora_layer_opts& opt) {
   LayerPlan p = {};
   p.valid = false;
   int32_t hb, hl;
   pick_tiles(T, k, E, L, &hb, &hl);
-  p.bm_base = bm_base > 0 ? bm_base : hb;
-  p.bm_lora = bm_lora > 0 ? bm_lora : hl;
+  const int64_t S = (int64_t)T * k;
+  const int64_t rr = L > 0 ? r : 0;
+  const bool pdl = !opt.disable_pdl;
+  const int slices = opt.gate_up_slices == 0 ? 1 : opt.gate_up_slices;
+  // the fused chain: shapes whose shifted z buffers stay small next to G (they grow with
+  // E L); adapters of one rank with one gate_up slice and r % 8 == 0 (the B tensor maps)
+  const int gap = fused_gap(T, k, E, L);
+  p.z = zpad_layout((int)S, E, L, (int)rr, gap);
+  const int64_t zbytes = L > 0 ? (int64_t)round_up((size_t)(p.z.rows * p.z.zw * 2), 256) : 0;
+  const int64_t g_bytes = S * 2 * (int64_t)I * 4;
+  const bool shape_ok = L == 0 || (r % 8 == 0 && 2 * zbytes <= std::max<int64_t>(g_bytes, 64ll << 20));
+  const bool want = shape_ok && opt.expand_mode != 1 &&
+                    (L == 0 || (opt.adapter_ranks == nullptr && slices == 1));
+  p.em_bn = pdl ? expert_major_rows(T, k, E) : 0;
+  p.bm_base = opt.bm_base > 0 ? opt.bm_base : (want && hb > 128 ? 128 : hb);
+  p.bm_lora = opt.bm_lora > 0 ? opt.bm_lora : hl;
+  const int chunk = p.em_bn > 0 ? p.em_bn : p.bm_base;
+  p.fused = want && chunk <= gap && chunk <= 128;
   p.al = align_layout(T, k, E, L, p.bm_base, p.bm_lora);
   // the align region is sized for the smallest tiles so any tile choice fits
   AlignLayout worst = align_layout(T, k, E, L, 16, 1);
   if (!p.al.valid || !worst.valid) return p;
-  const int64_t S = (int64_t)T * k;
-  const int64_t rr = L > 0 ? r : 0;
   int64_t o = 0;
   auto take = [&](int64_t bytes) { int64_t at = o; o = (int64_t)round_up(o + bytes, 256); return at; };
   p.off_align = take(worst.off[MOE_LORA_AF_TOTAL_BYTES]);
   p.off_ids = take(S * 4);
   p.off_w = take(S * 4);
   p.off_xs = take(S * H * 2);
-  p.off_G = take(S * 2 * (int64_t)I * 4);
+  p.off_G = take(std::max<int64_t>(g_bytes, shape_ok ? 2 * zbytes : 0));
+  p.off_Z1p = p.off_G;
+  p.off_Z2p = p.off_G + zbytes;
   p.off_Z1 = take(S * 2 * rr * 4);  // two z slices with separate gate and up adapters
   p.off_h = take(S * (int64_t)I * 2);
   p.off_Z2 = take(S * rr * 4);
   p.off_O = take(S * (int64_t)H * 4);
   p.total = o;
+  // launches of one call routed from logits
+  const int align_n = p.al.ctas > 0 ? 3 : 1;
+  if (p.fused) {
+    p.launches = 1 + align_n + 1 + 2 + 1 + (L > 0 ? 2 : 0);
+  } else {
+    const bool add_then_combine = L > 0 && S >= 2 * (int64_t)E * L;
+    p.launches = 1 + align_n + 1 + 2 + 2 + (L > 0 ? 2 : 0) + (add_then_combine ? 1 : 0);
+  }
   p.valid = true;
   return p;
 }
@@ -152,8 +229,25 @@ extern "C" int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, in
 
 extern "C" size_t moe_lora_workspace_size(int T, int k, int E, int L, int H, int I, int r) {
   if (T < 0 || k < 1 || E < 1 || L < 0 || H < 1 || I < 1 || (L > 0 && r < 1)) return 0;
-  LayerPlan p = plan_layer(T, k, E, L, H, I, r, 0, 0);
+  const moe_lora_layer_opts o = {};
+  LayerPlan p = plan_layer(T, k, E, L, H, I, r, o);
   return p.valid ? (size_t)p.total : 0;
+}
+
+extern "C" int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int r,
+                                   const moe_lora_layer_opts* opts, moe_lora_layer_plan_t* out) {
+  if (!out || T < 0 || k < 1 || E < 1 || L < 0 || H < 1 || I < 1 || (L > 0 && r < 1))
+    return MOE_LORA_ERR_INVALID_ARG;
+  moe_lora_layer_opts o = {};
+  if (opts) o = *opts;
+  LayerPlan p = plan_layer(T, k, E, L, H, I, r, o);
+  if (!p.valid) return MOE_LORA_ERR_UNSUPPORTED;
+  out->bm_base = p.bm_base;
+  out->bm_lora = p.bm_lora;
+  out->expert_major_rows = p.em_bn;
+  out->fused_expand = p.fused ? 1 : 0;
+  out->launches = T > 0 ? p.launches : 0;
+  return MOE_LORA_OK;
 }
 
 // Host-side checks of a layer call; nothing is launched or copied on error. On success
@@ -183,7 +277,8 @@ static int check_layer_args(const void* x, const float* logits, const int32_t* t
     return MOE_LORA_ERR_INVALID_ARG;
   if (o.num_events < 0 || (o.num_events > 0 && !o.events)) return MOE_LORA_ERR_INVALID_ARG;
   if (o.gate_up_slices < 0 || o.gate_up_slices > 2) return MOE_LORA_ERR_INVALID_ARG;
-  *plan = plan_layer(T, k, E, L, H, I, r, o.bm_base, o.bm_lora);
+  if (o.expand_mode < 0 || o.expand_mode > 2) return MOE_LORA_ERR_INVALID_ARG;
+  *plan = plan_layer(T, k, E, L, H, I, r, o);
   if (!plan->valid) return MOE_LORA_ERR_UNSUPPORTED;
   if (T == 0) return MOE_LORA_OK;
   if (workspace_bytes < (size_t)plan->total) return MOE_LORA_ERR_WORKSPACE_TOO_SMALL;
@@ -228,6 +323,9 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   float* Z2 = reinterpret_cast<float*>(ws + p.off_Z2);
   float* O = reinterpret_cast<float*>(ws + p.off_O);
   const int rr = L > 0 ? r : 0;
+  const unsigned long long wait_ns = o.wait_limit_ns == 0 ? kWaitLimitNs
+                                     : o.wait_limit_ns < 0 ? 0ull
+                                                           : (unsigned long long)o.wait_limit_ns;
 
   auto mark = [&](int i) -> int {
     if (i < o.num_events && o.events[i])
@@ -251,22 +349,61 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(mark(1));
   ML_STEP(launch_align(ids, L > 0 ? token_adapter : nullptr, &al, p.al, stream, pdl));
   ML_STEP(mark(2));
+  const int em_bn = p.em_bn;
+  if (p.fused) {
+    // route -> align -> gather -> gate_up shrink -> gate_up GEMM with the expand and
+    // SwiGLU -> down shrink -> down GEMM with the expand -> combine. Each shrink writes
+    // z into its shifted buffer; each GEMM reads everything but z before its wait (its
+    // predecessor, the shrink, triggers only after its own wait).
+    __nv_bfloat16* Z1p = reinterpret_cast<__nv_bfloat16*>(ws + p.off_Z1p);
+    __nv_bfloat16* Z2p = reinterpret_cast<__nv_bfloat16*>(ws + p.off_Z2p);
+    ZPadOut zo = {};
+    zo.zw = p.z.zw;
+    zo.lo_off = p.z.lo_off;
+    zo.rp16 = p.z.rp16;
+    zo.gap = p.z.gap;
+    zo.L = L;
+    AlignView av = align_view(al.buf, p.al);
+    zo.row_expert = av.row_expert;
+    zo.row_adapter = av.row_adapter;
+    const bool lora = L > 0;
+    ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, false));
+    ML_STEP(mark(3));
+    if (lora) {  // by token: x is a caller input, the align tables two launches back
+      zo.p = Z1p;
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, r, nullptr, stream, pdl, pdl, wait_ns, &zo));
+    }
+    ML_STEP(mark(4));
+    ML_STEP(launch_fused_gemm(xs, W1, lora ? B1 : nullptr, Z1p, p.z, &al, p.al, 2 * I, H, r, true, h,
+                              stream, pdl, pdl && lora, em_bn, wait_ns));
+    ML_STEP(mark(5));
+    ML_STEP(mark(6));
+    if (lora) {  // h comes from the predecessor: the shrink waits first
+      zo.p = Z2p;
+      ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, nullptr, stream, pdl, false, wait_ns, &zo));
+    }
+    ML_STEP(mark(7));
+    ML_STEP(launch_fused_gemm(h, W2, lora ? B2 : nullptr, Z2p, p.z, &al, p.al, H, I, r, false, O,
+                              stream, pdl, pdl && lora, em_bn, wait_ns));
+    ML_STEP(mark(8));
+    ML_STEP(launch_combine(O, w, &al, p.al, H, y, y_fp32, stream, pdl));
+    ML_STEP(mark(9));
+    return MOE_LORA_OK;
+  }
   // Few rows per expert (decode): the gate_up GEMM runs expert-major, so its weights
   // stream from the start of the layer while routing, align and gather finish.
-  const int64_t per_expert = ((int64_t)T * k + E - 1) / E;
-  const int em_bn = !pdl ? 0 : per_expert <= 16 ? 32 : per_expert <= 32 ? 64 : 0;
   ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, em_bn > 0));
   ML_STEP(mark(3));
-  ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, pdl, em_bn));
+  ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, pdl, em_bn, wait_ns));
   ML_STEP(mark(4));
   // Short LoRA blocks (decode-like) read the gathered rows: addressed by sorted row, they
   // need no slot lookup before the load (and are recent in L2).
   if (L > 0) {
     // with separate gate and up adapters the gate_up shrink is one of rank 2r
     if (p.bm_lora <= 8)
-      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl, wait_ns));
     else
-      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl));
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl, wait_ns));
   }
   ML_STEP(mark(5));
   ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, L > 0 && slices == 2 ? 3 : 1, G, h, 0,
@@ -274,9 +411,9 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   ML_STEP(mark(6));
   // the down GEMM likewise runs expert-major when experts hold few rows: its weights stream
   // while the SwiGLU expand drains
-  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, em_bn));
+  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, em_bn, wait_ns));
   ML_STEP(mark(7));
-  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, pdl));
+  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, pdl, wait_ns));
   ML_STEP(mark(8));
   ML_STEP(launch_expand_impl(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w,
                              stream, pdl, pdl && L > 0));

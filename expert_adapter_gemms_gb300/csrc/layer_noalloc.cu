@@ -18,8 +18,10 @@
 // * All calls on a device share the one array and it keeps the previous call's
 //   contents. Calls whose work overlaps on the GPU (different streams without
 //   ordering between them) race on it; order such calls on one stream.
-// * The first call on each device looks up the array's device address (once,
-//   with that device current); make that first call before any stream capture.
+// * The first call on each device looks up the array's device address (with that
+//   device current); make that first call before any stream capture. The address
+//   belongs to the device's current context: when that context is replaced (after
+//   cudaDeviceReset, say) the next call looks it up again.
 #include <mutex>
 
 #include "internal.h"
@@ -33,20 +35,25 @@ constexpr size_t kNoallocBytes = 64ull << 20;
 // symbol, never a device address: host code uses the address looked up below.
 __device__ __align__(256) unsigned char g_noalloc_ws[kNoallocBytes];
 
-constexpr int kMaxDev = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDev] = {nullptr};
+void* g_addr[kMaxDevices] = {nullptr};
+uint64_t g_addr_ctx[kMaxDevices] = {0};  // context id the address was looked up in
 
-// Device address of g_noalloc_ws on the current device (looked up once per device).
+// Device address of g_noalloc_ws in the current context of the current device:
+// looked up on the first call in each context (a module's __device__ arrays are
+// placed anew in every context that loads it) and cached against the context id.
 int noalloc_workspace(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_LORA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDev) return MOE_LORA_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_LORA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  uint64_t id = current_context_id();
+  if (!g_addr[dev] || id == 0 || g_addr_ctx[dev] != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) return MOE_LORA_ERR_CUDA;
+    if (id == 0) id = current_context_id();  // the lookup made the primary context current
     g_addr[dev] = p;
+    g_addr_ctx[dev] = id;
   }
   *out = g_addr[dev];
   return MOE_LORA_OK;

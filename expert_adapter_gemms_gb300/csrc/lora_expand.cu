@@ -54,12 +54,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// silu(v) = v / (1 + exp(-v)) with the hardware exponential and a reciprocal-based
-// divide (CUDA's __expf, __fdividef): a few fp32 ulps, far below the bf16 rounding of the
-// SwiGLU output; for v below about -87 it returns 0 where the exact form gives a value
-// under 1e-36.
-__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f + __expf(-v)); }
-
 // dot(z[0..r), B row) reading the B row from memory (any r, any alignment when !kVec).
 template <bool kVec>
 __device__ __forceinline__ float dot_zb_mem(const float* zs, const __nv_bfloat16* brow, int r) {
@@ -911,10 +905,8 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     const int cc = chunks_for(I);
     const dim3 grid(a.max_blocks * cc + a.max_tiles * ceil_div(I, 2 * kExpandThreads));
     const size_t smem1 = Bp ? 2 * zsmem + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float) : 0;
-    static std::atomic<int> configured[64];  // every instance at once, once per device
-    int dev = 0;
-    ML_CHECK_CUDA(cudaGetDevice(&dev));
-    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+    static std::atomic<uint64_t> configured[kMaxDevices];  // every instance, once per context
+    const int cst = once_per_context(configured, [] {
       const int lim = (int)(2 * zsmem_bytes(8) + (size_t)(kExpandThreads / 32) * kGStages * 256 * sizeof(float));
       const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
 #define ML_SWIGLU_ATTR(KC_)                                                                  \
@@ -924,8 +916,9 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
   ML_CHECK_CUDA(cudaFuncSetAttribute(expand_swiglu_mma_kernel<KC_, true, true>, attr, lim));
       ML_SWIGLU_ATTR(1) ML_SWIGLU_ATTR(2) ML_SWIGLU_ATTR(4) ML_SWIGLU_ATTR(8)
 #undef ML_SWIGLU_ATTR
-      configured[dev].store(1, std::memory_order_release);
-    }
+      return MOE_LORA_OK;
+    });
+    if (cst != MOE_LORA_OK) return cst;
     auto go = [&](auto kern) -> int {
       return launch_pdl(kern, grid, kExpandThreads, smem1, stream, pdl, Z, Bp,
                         (const int*)v.hdr, (const int4*)v.blocks, (const int4*)v.tiles,
@@ -1020,18 +1013,7 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
                            ea, ranks);
     }
     if (st != MOE_LORA_OK) return st;
-    const int ncol = ceil_div(N, kExpandThreads);
-    int tpc = 1;
-    while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms &&
-           tpc * 2 * al->k <= kExpandThreads)
-      tpc *= 2;
-    const dim3 g2(ceil_div(al->T, tpc), ncol);
-    return out_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl,
-                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
-                                 N, out, tpc)
-                    : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl,
-                                 (const float*)base, topk_w, (const int*)v.slot_row, al->T, al->k,
-                                 N, out, tpc);
+    return launch_combine(base, topk_w, al, a, N, out, out_fp32, stream, pdl);
   }
   if (epilogue == 2) {
     const int ncol = ceil_div(N, kExpandThreads);
@@ -1065,6 +1047,26 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
     }
   }
   return MOE_LORA_ERR_INVALID_ARG;
+}
+
+int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
+                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl) {
+  if (a.S == 0 || al->T == 0) return MOE_LORA_OK;
+  AlignView v = align_view(al->buf, a);
+  const int sms = num_sms();
+  // tokens per CTA: as many as keep about four CTAs per SM busy (at most 8, and the CTA's
+  // slots within the 256-entry shared tables)
+  const int ncol = ceil_div(N, kExpandThreads);
+  int tpc = 1;
+  while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms &&
+         tpc * 2 * al->k <= kExpandThreads)
+    tpc *= 2;
+  if (tpc * al->k > kExpandThreads) return MOE_LORA_ERR_UNSUPPORTED;
+  const dim3 g2(ceil_div(al->T, tpc), ncol);
+  return y_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc)
+                : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc);
 }
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,

@@ -58,13 +58,55 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// z of (sorted row, rank) of pair (e, l) into the shifted buffer of the fused expand: the
+// bf16 rounding of v and the bf16 rounding of the remainder.
+__device__ __forceinline__ void zpad_put(const ZPadOut& o, int row, int e, int l, int rank, float v) {
+  const size_t at = ((size_t)row + ((size_t)e * o.L + l + 1) * o.gap) * o.zw;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  o.p[at + rank] = hi;
+  o.p[at + o.lo_off + rank] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// Run by the CTA of rank group 0 of a LoRA block: the zero columns [r, rp16) of its rows
+// in both halves and, for the first (last) block of its pair, the `gap` zero rows before
+// (after) the pair, which a fused-expand tile reads for its rows of other pairs.
+__device__ void zpad_extras(const ZPadOut& o, const int* hdr, int row0, int rows, int e, int l,
+                            int r) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const size_t shift = ((size_t)e * o.L + l + 1) * o.gap;
+  const __nv_bfloat16 zero = __ushort_as_bfloat16((unsigned short)0);
+  const int pad = o.rp16 - r;
+  for (int i = tid; i < rows * pad; i += nt) {
+    const int m = i / pad, c = r + (i - m * pad);
+    const size_t at = ((size_t)row0 + m + shift) * o.zw;
+    o.p[at + c] = zero;
+    o.p[at + o.lo_off + c] = zero;
+  }
+  const int n_valid = __ldcg(hdr + HDR_NVALID);
+  const int end = row0 + rows;
+  const bool first = row0 == 0 || __ldcg(o.row_expert + row0 - 1) != e ||
+                     __ldcg(o.row_adapter + row0 - 1) != l;
+  const bool last = end >= n_valid || __ldcg(o.row_expert + end) != e ||
+                    __ldcg(o.row_adapter + end) != l;
+  const int groups = o.gap * (o.zw / 8);  // 16-byte groups of `gap` rows
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  if (first) {
+    uint4* q = reinterpret_cast<uint4*>(o.p + ((size_t)row0 + shift - o.gap) * o.zw);
+    for (int i = tid; i < groups; i += nt) q[i] = z4;
+  }
+  if (last) {
+    uint4* q = reinterpret_cast<uint4*>(o.p + ((size_t)end + shift) * o.zw);
+    for (int i = tid; i < groups; i += nt) q[i] = z4;
+  }
+}
+
 template <int NT, int U, bool kVec, bool kEvenK, bool kSmallM>
 __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 : NT == 4 ? 2 : 1)
     lora_shrink_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
                        int K, int r, int E, float* __restrict__ Z, int ngroups, int early,
-                       const int* __restrict__ ranks, int rs) {
+                       const int* __restrict__ ranks, int rs, const ZPadOut zo) {
   constexpr int R = 8 * NT;  // ranks per CTA
   constexpr int XB = kSmallM ? 1 : U;  // kSmallM: blocks of at most 8 rows, no second row set
   __shared__ float red[kShrinkWarps][16][R + 1];
@@ -179,9 +221,14 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < kShrinkWarps; ++w) sum += red[w][m][c];
-    const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
-    Z[(size_t)slot * r + rank] = sum;
+    if (zo.p) {
+      zpad_put(zo, row0 + m, e, l, rank, sum);
+    } else {
+      const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
+      Z[(size_t)slot * r + rank] = sum;
+    }
   }
+  if (zo.p && g == 0) zpad_extras(zo, hdr, row0, rows, e, l, r);
 }
 
 // ----------------------------------------------------------------------------
@@ -216,7 +263,8 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
                             const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                             const int4* __restrict__ blocks, const int* __restrict__ sorted_slots,
                             int k, int K, int r, int E, float* __restrict__ Z, int ngroups,
-                            int early, int astride, const int* __restrict__ ranks, int rs) {
+                            int early, int astride, const int* __restrict__ ranks, int rs,
+                            unsigned long long wait_ns, const ZPadOut zo) {
   constexpr int R = 8 * NT;
   static_assert(R == 32, "one rank row per lane of warp 0");
   extern __shared__ __align__(16) uint8_t sA[];  // [R][astride] bytes; reused for the reduction
@@ -271,9 +319,11 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
     if (x0 && st < nsteps && (kEvenK || k0 < K)) xa[u] = __ldcg(reinterpret_cast<const uint4*>(x0 + k0));
   }
   __syncthreads();  // the barrier is initialised before any thread waits on it
-  if (!mbar_wait_bounded(&bar, 0)) {
-    set_dev_error(const_cast<int*>(hdr), MOE_LORA_DEVERR_TIMEOUT);
-    mbar_wait_bounded(&bar, 0);  // copies still in flight land before the slab is reused
+  const bool landed = mbar_wait_bounded(&bar, 0, wait_ns);
+  if (__syncthreads_or(!landed)) {  // a thread gave up: the CTA records it and writes nothing
+    if (threadIdx.x == 0) set_dev_error(const_cast<int*>(hdr), MOE_LORA_DEVERR_TIMEOUT);
+    mbar_wait_bounded(&bar, 0);  // the slab's copies land before the CTA exits
+    return;
   }
   float acc[NT][4];
 #pragma unroll
@@ -314,16 +364,21 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
     float sum = 0.f;
 #pragma unroll
     for (int w = 0; w < kShrinkWarps; ++w) sum += red[w][m][c];
-    const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
-    Z[(size_t)slot * r + rank] = sum;
+    if (zo.p) {
+      zpad_put(zo, row0 + m, e, l, rank, sum);
+    } else {
+      const int slot = idx == (int)threadIdx.x ? slot0 : __ldcg(sorted_slots + row0 + m);
+      Z[(size_t)slot * r + rank] = sum;
+    }
   }
+  if (zo.p && g == 0) zpad_extras(zo, hdr, row0, rows, e, l, r);
 }
 
 template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
                             float* Z, bool vec, cudaStream_t stream, bool pdl, int early,
-                            bool small_m, const int* ranks, int rs) {
+                            bool small_m, const int* ranks, int rs, const ZPadOut& zo) {
   const int ngroups = ceil_div(r, 8 * NT);
   const int64_t grid = (int64_t)max_blocks * ngroups;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
@@ -331,7 +386,7 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
   auto args = [&](auto kern) {
     return launch_pdl(kern, g, kShrinkWarps * 32, 0, stream, pdl, X, rows_are_slots, A,
                       (const int*)v.hdr, (const int4*)v.blocks, (const int*)v.sorted_slots, k, K,
-                      r, E, Z, ngroups, early, ranks, rs);
+                      r, E, Z, ngroups, early, ranks, rs, zo);
   };
   if (small_m) {
     if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true, true>);
@@ -345,9 +400,11 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
 
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
                        const moe_lora_align_t* al, const AlignLayout& a, int K, int r, int rs,
-                       float* Z, cudaStream_t stream, bool pdl, bool early) {
+                       float* Z, cudaStream_t stream, bool pdl, bool early,
+                       unsigned long long wait_ns, const ZPadOut* zpad) {
   const int* ranks = al->adapter_ranks;
   if (a.S == 0 || al->L == 0) return MOE_LORA_OK;
+  const ZPadOut zo = zpad ? *zpad : ZPadOut{};
   AlignView v = align_view(al->buf, a);
   const auto* Xp = static_cast<const __nv_bfloat16*>(X);
   const auto* Ap = static_cast<const __nv_bfloat16*>(A);
@@ -363,8 +420,8 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   else if (r <= 32) nt = 4;
   else nt = 8;
   switch (nt) {
-    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
-    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
+    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
+    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
     case 4:  // short blocks: two k-steps per batch, still two CTAs per SM
       if (al->bm_lora <= 8 && vec && K <= 32 * kShrinkWarps * kShortUMax &&
           32 * short_astride(K) <= 56 * 1024) {  // short K: the slab in shared memory
@@ -374,31 +431,30 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
         const int ngroups = ceil_div(r, 32);
         const int64_t grid = (int64_t)a.max_blocks * ngroups;
         if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
-        static std::atomic<int> configured[64];  // both instances at once, once per device
-        int dev = 0;
-        ML_CHECK_CUDA(cudaGetDevice(&dev));
-        if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+        static std::atomic<uint64_t> configured[kMaxDevices];  // every instance, once per context
+        const int cst = once_per_context(configured, [] {
           const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, false>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, false>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, true, true>, attr, 56 * 1024));
           ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_smem_kernel<4, false, true>, attr, 56 * 1024));
-          configured[dev].store(1, std::memory_order_release);
-        }
+          return MOE_LORA_OK;
+        });
+        if (cst != MOE_LORA_OK) return cst;
         auto go = [&](auto kern) -> int {
           return launch_pdl(kern, dim3((unsigned)grid), kShrinkWarps * 32, smem, stream, pdl, Xp,
                             rows_are_slots, Ap, (const int*)v.hdr, (const int4*)v.blocks,
                             (const int*)v.sorted_slots, al->k, K, r, al->E, Z, ngroups, ea, astride,
-                            ranks, rs);
+                            ranks, rs, wait_ns, zo);
         };
         if (ranks)
           return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true, true>) : go(lora_shrink_smem_kernel<4, false, true>);
         return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true, false>) : go(lora_shrink_smem_kernel<4, false, false>);
       }
       if (al->bm_lora <= 8)
-        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true, ranks, rs);
-      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false, ranks, rs);
-    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs);
+        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true, ranks, rs, zo);
+      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false, ranks, rs, zo);
+    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
   }
 }
 

@@ -144,7 +144,10 @@ MOE_LORA_API size_t moe_lora_align_buffer_size(int T, int k, int E, int L, int b
 /* Fills offsets[MOE_LORA_ALIGN_NFIELDS] (byte offsets; MAX_* fields hold counts). Host only. */
 MOE_LORA_API int moe_lora_align_layout(int T, int k, int E, int L, int bm_base, int bm_lora, int64_t* offsets);
 
-/* ids [T, k] int32; token_adapter [T] int32 or NULL (all -1). One CTA, deterministic. */
+/* ids [T, k] int32; token_adapter [T] int32 or NULL (all -1). Deterministic. Below 2048
+ * slots (or with more buckets E*(L+1)+1 than half the slots) one CTA sorts every slot;
+ * from 2048 slots three launches share the work: per-CTA stable sorts of 512-slot chunks,
+ * one scan over the (key, chunk) count table, and a placement pass. */
 MOE_LORA_API int moe_lora_align(const int32_t* ids, const int32_t* token_adapter, const moe_lora_align_t* al,
                    moe_lora_stream_t stream);
 
@@ -215,10 +218,14 @@ MOE_LORA_API int lora_expand_add(const float* Z, const void* B, const moe_lora_a
                     moe_lora_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * The whole layer:
+ * The whole layer, as one of two chains of launches (moe_lora_layer_plan says which):
  *   route (if logits != NULL) -> align -> gather -> gate_up grouped GEMM ->
  *   gate_up shrink -> gate_up expand + SwiGLU -> down grouped GEMM -> down shrink
- *   -> down expand + weighted top-k combine.
+ *   -> down expand + weighted top-k combine;
+ * or, with the expand fused into the grouped GEMMs by concatenation along K
+ * (y = xW + zB = [x | z][W | B]^T for the rows of each adapter):
+ *   route -> align -> gather -> gate_up shrink -> gate_up GEMM + expand + SwiGLU ->
+ *   down shrink -> down GEMM + expand -> weighted top-k combine.
  * x [T, H] bf16. Routing: either logits [T, E] fp32 (topk_ids/topk_w NULL) or
  * caller-provided topk_ids [T, k] int32 and topk_w [T, k] fp32 (logits NULL).
  * token_adapter [T] int32 or NULL. LoRA weights may be NULL with L = 0 (base MoE).
@@ -241,9 +248,13 @@ typedef struct moe_lora_layer_opts {
   int32_t disable_pdl;  /* 1: plain stream-ordered launches */
   int32_t num_events;   /* length of `events` (0: none) */
   void** events;        /* cudaEvent_t handles recorded on `stream` before each stage and
-                           after the last: [0] route, [1] align, [2] gather, [3] gate_up GEMM,
-                           [4] gate_up shrink, [5] gate_up expand+SwiGLU, [6] down GEMM,
-                           [7] down shrink, [8] down expand+combine, [9] end */
+                           after the last: [0] route, [1] align, [2] gather, then for the
+                           chain with a separate expand: [3] gate_up GEMM, [4] gate_up
+                           shrink, [5] gate_up expand+SwiGLU, [6] down GEMM, [7] down shrink,
+                           [8] down expand+combine; for the fused chain
+                           (moe_lora_layer_plan_t.fused_expand): [3] gate_up shrink, [4]
+                           gate_up GEMM with expand+SwiGLU, [5] empty, [6] down shrink, [7]
+                           down GEMM with expand, [8] combine; [9] end */
   const int32_t* adapter_ranks; /* optional device array [L] of per-adapter ranks (see
                            moe_lora_align_t.adapter_ranks); NULL: every adapter has rank r */
   int32_t gate_up_slices; /* 0 or 1: one adapter over the fused gate_up output (A1
@@ -252,6 +263,19 @@ typedef struct moe_lora_layer_opts {
                            [L,E,2I,r] unchanged: gate columns take the gate z, up columns
                            the up z (lora_expand_add epilogue 3). The pages describe one
                            adapter per projection and are silent on a split gate_up. */
+  int32_t expand_mode;  /* 0: the library picks; 1: the expand in kernels of its own (after
+                           each grouped GEMM); 2 is treated as 0. The fused chain (the expand
+                           as extra K-steps of the grouped GEMMs, SwiGLU in the gate_up GEMM's
+                           epilogue) is used where it applies: one adapter rank (no
+                           adapter_ranks), one gate_up slice, r % 8 == 0, and shapes whose
+                           shifted z buffers stay small (they grow with E * L). */
+  int64_t wait_limit_ns; /* for tests of the give-up path: the wall-time limit of the grouped
+                           GEMMs' main-loop mbarrier waits (and of the short-K shrink's slab
+                           wait). 0: the default, 4 s; < 0: give up at the first unsuccessful
+                           poll. A wait that gives up sets MOE_LORA_DEVERR_TIMEOUT; the CTA then
+                           drains its own copies and tensor-core work (those waits keep the 4 s
+                           limit), frees its tensor memory and exits, and that launch's
+                           results are invalid. */
 } moe_lora_layer_opts;
 
 #define MOE_LORA_LAYER_NUM_STAGES 9
@@ -304,6 +328,28 @@ MOE_LORA_API int moe_lora_layer_host(const void* in_host, void* y_host, void* st
 MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, int r, int32_t* bm_base,
                          int32_t* bm_lora);
 
+/* How moe_lora_layer_ex runs a shape with the given options (NULL: defaults); host only.
+ *   bm_base, bm_lora      the align's token tile and LoRA block rows
+ *   expert_major_rows     > 0: each grouped-GEMM CTA takes one (expert, 128-row weight block)
+ *                         and all of the expert's rows in chunks of this many (few rows per
+ *                         expert); 0: token tiles of bm_base rows
+ *   fused_expand          1: the LoRA expand runs as extra K-steps of the grouped GEMMs
+ *                         (y = [x | z][W | B]^T per adapter run of a tile; the gate_up GEMM
+ *                         writes the SwiGLU output directly, the down GEMM its rows, then a
+ *                         combine kernel); 0: the expand in kernels of its own
+ *   launches              kernels one call launches when routed from logits (one fewer with
+ *                         caller-provided ids) */
+typedef struct moe_lora_layer_plan_t {
+  int32_t bm_base;
+  int32_t bm_lora;
+  int32_t expert_major_rows;
+  int32_t fused_expand;
+  int32_t launches;
+} moe_lora_layer_plan_t;
+
+MOE_LORA_API int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int r,
+                                     const moe_lora_layer_opts* opts, moe_lora_layer_plan_t* plan);
+
 /* ---------------------------------------------------------------------------
  * moe_lora_layer_noalloc: the same layer as moe_lora_layer for callers that cannot
  * allocate device memory -- e.g. a serving engine that has reserved nearly all HBM
@@ -320,7 +366,9 @@ MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, 
  * The function allocates nothing. All calls on a device share the array and it
  * keeps the last call's contents: calls that overlap on the GPU race, so order
  * them on one stream. The first call on each device looks up the array's device
- * address; make that first call before any stream capture.
+ * address; make that first call before any stream capture. The address belongs to
+ * the device's current context: after that context is re-created (cudaDeviceReset)
+ * the next call looks it up again.
  * ------------------------------------------------------------------------- */
 MOE_LORA_API int moe_lora_layer_noalloc(const void* x, const float* logits,
                                         const int32_t* topk_ids, const float* topk_w,

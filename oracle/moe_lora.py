@@ -19,7 +19,7 @@ Sources (the pages describing vLLM's multi-LoRA serving for MoE models):
   select an (expert, adapter) pair ("compound sparsity"). Fig. 1: hidden 4096,
   intermediate 11008, r = 32.
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
 
 * Activation between the projections: SwiGLU, h = silu(gate) * up with
   silu(v) = v / (1 + exp(-v)); the gate_up output holds gate in columns
