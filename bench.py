@@ -496,10 +496,11 @@ def multi_layer(m, inp, W1, W2, lora, lg_d, ta_d, x_d, ws, n_layers, steps, warm
 class Layer:
     """One workload's inputs on the device and a layer call over them."""
 
-    def __init__(self, m, name):
+    def __init__(self, m, name, expand_mode=0):
         import torch
         from workloads import make_workload_inputs
         self.m = m
+        self.expand_mode = expand_mode
         self.inp = inp = make_workload_inputs(name)
         d = lambda t: None if t is None else t.to("cuda").contiguous()  # noqa: E731
         self.W1, self.W2 = d(inp.W1), d(inp.W2)
@@ -507,17 +508,18 @@ class Layer:
         self.x, self.lg, self.ta = d(inp.x), d(inp.logits), d(inp.token_adapter)
         self.y = torch.empty((inp.T, inp.H), dtype=torch.bfloat16, device="cuda")
         self.ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
-        self.plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+        self.plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r,
+                                          expand_mode=expand_mode)
 
     def __call__(self, events=None, adapters=True):
         inp = self.inp
         if adapters:
             self.m.moe_lora_layer(self.x, self.W1, self.W2, logits=self.lg, k=inp.k,
                                   token_adapter=self.ta, y=self.y, workspace=self.ws,
-                                  events=events, **self.lora)
+                                  events=events, expand_mode=self.expand_mode, **self.lora)
         else:  # the base MoE alone (L = 0): the same layer without adapters
             self.m.moe_lora_layer(self.x, self.W1, self.W2, logits=self.lg, k=inp.k, y=self.y,
-                                  workspace=self.ws, events=events)
+                                  workspace=self.ws, events=events, expand_mode=self.expand_mode)
 
 
 def timed_steps(fn, steps, stream):
@@ -572,6 +574,36 @@ def stage_table(layer, kernel_steps, stream, peaks):
     return kernels, sb
 
 
+def stream_floor(stream, sizes_mb=(29.7, 66.0, 300.0), reps=16):
+    """The time of one launch that reads and writes a given number of bytes, by CUDA events
+    over `reps` back-to-back device-to-device copies (torch's copy kernel) through rotating
+    buffers larger than L2. A short stream carries a fixed cost (launch, ramp-up of the
+    memory pipeline, drain) that no kernel design removes; these figures put the roofline
+    fractions of the decode LoRA kernels (30-66 MB each) in context."""
+    import torch
+    out = {}
+    for mb in sizes_mb:
+        n = int(mb * 1e6 / 2) // 2 * 2  # bf16 elements moved: half read, half written
+        half = n // 2
+        nbuf = max(2, int(512e6 // (n * 2)) + 1)  # > 512 MB in rotation: no L2 reuse
+        src = [torch.empty(half, dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+        dst = [torch.empty(half, dtype=torch.bfloat16, device="cuda") for _ in range(nbuf)]
+        for i in range(nbuf):
+            dst[i].copy_(src[i])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            dst[i % nbuf].copy_(src[i % nbuf])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        out[f"{mb:g}MB"] = {"us": round(us, 2), "GB_s": round(2 * half * 2 / (us * 1e-6) / 1e9, 1)}
+        del src, dst
+        torch.cuda.empty_cache()
+    return out
+
+
 def measure(layer, steps, warmup, kernel_steps, stream, peaks):
     """ms per step (CUDA events over exactly `steps` calls after `warmup`), the base MoE
     alone for the marginal cost of the adapters, and the per-stage table."""
@@ -605,7 +637,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     import expert_adapter_gemms_gb300 as m
 
-    layer = Layer(m, args.workload)
+    layer = Layer(m, args.workload, args.expand_mode)
     inp = layer.inp
     stream = torch.cuda.current_stream()
     peaks, peak_kind = measured_peaks()
@@ -642,7 +674,8 @@ def run_ours(args):
     d2h = io.y_host.numel() * io.y_host.element_size()
 
     def e2e_step():
-        m.moe_lora_layer_host(io, layer.W1, layer.W2, k=inp.k, workspace=layer.ws, **layer.lora)
+        m.moe_lora_layer_host(io, layer.W1, layer.W2, k=inp.k, workspace=layer.ws,
+                              expand_mode=args.expand_mode, **layer.lora)
 
     for _ in range(3):
         e2e_step()
@@ -680,6 +713,7 @@ def run_ours(args):
             "clocks": clk, "roofline": roof, "kernels": kernels,
             "base_moe_ms_per_step": head.get("base_moe_ms_per_step"),
             "lora_marginal_us": head.get("lora_marginal_us")}
+    line["stream_floor"] = stream_floor(stream)
     if args.layers > 1:
         line["multi_layer"] = multi_layer(m, inp, layer.W1, layer.W2, layer.lora, layer.lg,
                                           layer.ta, layer.x, layer.ws, args.layers,
@@ -702,7 +736,7 @@ def run_ours(args):
         for name in names:
             if name in wl:
                 continue
-            other = Layer(m, name)
+            other = Layer(m, name, args.expand_mode)
             wl[name] = measure(other, args.extra_steps, 5, max(5, args.kernel_steps // 5),
                                stream, peaks)
             wl[name]["l2"] = ("fits in L2: launch-bound" if name == "tiny"
@@ -734,6 +768,8 @@ def main(argv=None):
                     help="'all', 'none' or a comma list: other workloads measured after the "
                          "headline one (fewer steps, no CPU baseline)")
     ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--expand-mode", type=int, default=0, choices=[0, 1],
+                    help="0: the chain the library picks; 1: the expand in kernels of its own")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -319,7 +319,8 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r].
     adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r).
     wait_limit_ns (tests of the give-up path): 0 default 4 s, < 0 give up at once.
-    expand_mode: 0 the library picks, 1 the expand in kernels of its own."""
+    expand_mode: 0 the library picks, 1 the expand in kernels of its own, 2 the expand fused
+    into the grouped GEMMs wherever it applies."""
     _need(x, "x", torch.bfloat16, 2)
     T, H = x.shape
     E, I, Ln, r = _layer_weights(H, W1, W2, A1, B1, A2, B2, gate_up_slices)

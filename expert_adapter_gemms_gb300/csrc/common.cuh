@@ -271,6 +271,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Pulls `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 without
+// waiting for it (the bulk-copy engine's prefetch; a hint, nothing to complete).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ---- TMA (bulk tensor copies global -> shared, completion on an mbarrier) ----
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -368,6 +376,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024u >> 4) << 32;
   d |= (uint64_t)1u << 46;
   d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// The same descriptor for the other swizzle widths of a K-major bf16 tile: layout 2
+// (128-byte rows), 4 (64-byte rows) or 6 (32-byte rows); stride byte offset = 8 rows of
+// the tile (1024, 512 or 256 bytes); tile base aligned to 8 rows.
+__device__ __forceinline__ uint64_t smem_desc_swz(uint32_t saddr, uint32_t layout, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)(sbo >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)layout << 61;
   return d;
 }
 

@@ -9,14 +9,17 @@
 // so the expand is a few more K-steps of the same tcgen05 accumulation and the base
 // output never makes an fp32 round trip through HBM. Two epilogues:
 //
-// * gate_up (kGLU): a CTA holds a 128-row block of the gate rows of W1 and the
-//   matching 128-row block of the up rows in two TMEM accumulators and writes the
-//   SwiGLU output h = silu(gate) * up in bf16 directly.
-// * down: one accumulator, fp32 rows out (the weighted top-k combine follows).
+// * gate_up (kGLU): the 128 rows of a CTA's weight block are 64 rows of the gate half
+//   of W1 and the matching 64 rows of the up half, so one M = 128 accumulator holds
+//   gate (TMEM lanes 0..63) and up (lanes 64..127) of 64 output features for every
+//   token of the tile. The four epilogue warps pass their lanes through a small
+//   shared-memory tile so that one thread sees the gate and the up value of a feature,
+//   and write the SwiGLU output h = silu(gate) * up in bf16.
+// * down: 128 rows of W2, fp32 rows out (the weighted top-k combine follows).
 //
 // The z operand. The shrink writes z for sorted row j of pair (e, l) to row
 // j + (e L + l + 1) * gap of a "shifted" z buffer, and zero rows in the `gap` rows
-// before and after every pair it writes (gap = the GEMM's token tile). A tile's rows
+// before and after every pair it writes (gap >= the GEMM's token tile). A tile's rows
 // [r0, r0 + BN) all belong to one expert and are ordered by adapter, so the one TMA
 // box of BN rows at row r0 + (e L + l + 1) * gap returns z for exactly the tile's
 // rows of adapter l and zeros for its other rows: the rows of other pairs map into
@@ -26,12 +29,14 @@
 // of the remainder) that multiply the same bf16 B, which keeps the fp32 z to about
 // 2^-16 relative, as the unfused expand does.
 //
-// Stage ring: STAGES slots of [W (gate) | W (up, kGLU) | token rows]; a LoRA stage
-// uses the same slots for [B (gate) | B (up) | z rows]. Per job the producer issues the
-// K/64 base stages, then, for every run of rows with an adapter in the tile, the
-// stages of that adapter's B and z. Warp roles, TMEM double buffering, bounded waits
-// and the work decompositions (expert-major, per tile, persistent) follow the plain
-// grouped GEMM.
+// Stage ring: STAGES slots of [W block | token rows]; a LoRA stage uses the same slot for
+// [B block | z rows], its boxes only as wide as the rank (32-, 64- or 128-byte swizzled
+// rows). Per job the producer issues the K/64 base stages, then the stages of every run
+// of rows with an adapter in the tile; their MMAs stop at the run's last row. Warp roles
+// (a TMA producer, one MMA-issuing thread, four epilogue warps), TMEM double buffering,
+// bounded waits and the work decompositions (expert-major, per tile, persistent) follow
+// the plain grouped GEMM.
+#include <algorithm>
 #include <atomic>
 
 #include "internal.h"
@@ -42,19 +47,19 @@ constexpr int kFBM = 128;  // weight rows per block (MMA M)
 constexpr int kFBK = 64;   // K per stage
 constexpr int kFusedThreads = 192;
 constexpr int kFGroupTiles = 8;
+constexpr int kXStride = 17;  // floats per row of the gate/up exchange tile (conflict-free)
 enum { kFModeTile = 0, kFModeExpert = 1, kFModePersistent = 2 };
 
 template <int BN, int STAGES, bool kGLU>
 struct FusedCfg {
-  static constexpr int kNW = kGLU ? 2 : 1;  // weight tiles per stage (gate and up)
   static constexpr int kWBytes = kFBM * kFBK * 2;
   static constexpr int kABytes = BN * kFBK * 2;
-  static constexpr int kStageBytes = kNW * kWBytes + kABytes;
+  static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;   // one fp32 accumulator
-  static constexpr uint32_t kSetCols = kNW * kAccCols;      // gate (+ up) of one job
-  static constexpr uint32_t kTmemCols = 2 * kSetCols;       // two sets, used alternately
+  static constexpr int kXOff = kBarOff + 256;  // gate/up exchange tile [128][kXStride] fp32
+  static constexpr int kSmemBytes = kXOff + (kGLU ? kFBM * kXStride * 4 : 0) + 1024;
+  static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;  // one fp32 accumulator
+  static constexpr uint32_t kTmemCols = 2 * kAccCols;     // two, used alternately
   static_assert((2 * STAGES + 5) * 8 + 16 <= 256, "barrier area");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
@@ -72,42 +77,93 @@ struct FusedArgs {
   int up_off;       // kGLU: first row of the up half of W and B (= I)
   int K;            // reduction length of the base part
   int n_wblocks, max_tiles, mode, early;
+  int ksplit;       // expert-major, down form: CTAs per (expert, weight block), each a
+                    // contiguous share of the k-blocks writing its own partial output
+  size_t part_stride;  // elements between the partial outputs
   int E, L, gap;    // z of sorted row j of pair (e, l) sits at row j + (e L + l + 1) gap
   int lora;         // 0: no adapter term (B and z maps unused)
+  int lora_at;      // the adapter stages of a job follow its first lora_at base stages
   int zchunks;      // LoRA stages per run of an adapter in a tile
   int zk;           // > 0: one stage, z row = [high (zk K16 steps) | low (zk)]; 0: chunked
   int rp16;         // rank rounded up to a multiple of 16
+  // LoRA tiles: columns per box of B and of z, and their shared-memory swizzle (descriptor
+  // layout 2/4/6 for 128/64/32-byte rows, stride of 8 rows in bytes)
+  int b_cols, z_cols;
+  uint32_t b_layout, b_sbo, z_layout, z_sbo;
   unsigned long long wait_ns;
 };
 
-// Calls f(l) for every run of rows with an adapter (l >= 0) among sorted rows
-// [r0, r0 + rows), in order. Rows of one expert are ordered by adapter, so each adapter
-// present is one run. Warp-wide: every lane calls f with the same l.
-template <typename F>
-__device__ __forceinline__ void for_each_adapter_run(const int* row_adapter, int r0, int rows,
-                                                     F&& f) {
-  const int lane = threadIdx.x & 31;
-  int carry = -1;  // adapter of the last row of the previous 32-row group (-1 at r0)
-  for (int base = 0; base < rows; base += 32) {
-    const int i = base + lane;
-    const int l = i < rows ? __ldcg(row_adapter + r0 + i) : -1;
-    int prev = __shfl_up_sync(0xffffffffu, l, 1);
-    if (lane == 0) prev = carry;
-    unsigned m = __ballot_sync(0xffffffffu, l >= 0 && l != prev);
-    while (m) {
-      const int b = __ffs(m) - 1;
-      m &= m - 1;
-      f(__shfl_sync(0xffffffffu, l, b));
+// The adapters of a job's rows (sorted by (e, l), so each adapter present is one run),
+// loaded into registers when the job starts -- G groups of 32 rows, one value per lane --
+// and walked when its LoRA stages come, so no warp waits on these loads at that point.
+template <int G>
+struct AdapterRows {
+  int v[G];
+  int rows;
+  __device__ __forceinline__ void load(const int* row_adapter, int r0, int n) {
+    const int lane = threadIdx.x & 31;
+    rows = n;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int i = 32 * g + lane;
+      v[g] = i < n ? __ldcg(row_adapter + r0 + i) : -1;
     }
-    carry = __shfl_sync(0xffffffffu, l, 31);
   }
-}
+  // f(l, begin, end) for every run of rows [begin, end) with adapter l >= 0, in order.
+  // Warp-wide: every lane calls f with the same arguments.
+  template <typename F>
+  __device__ __forceinline__ void for_each_run(F&& f) const {
+    const int lane = threadIdx.x & 31;
+    unsigned m[G];
+    int carry = -1;  // adapter of the last row of the previous group (-1 before the first)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      int prev = __shfl_up_sync(0xffffffffu, v[g], 1);
+      if (lane == 0) prev = carry;
+      m[g] = __ballot_sync(0xffffffffu, v[g] >= 0 && v[g] != prev);
+      carry = __shfl_sync(0xffffffffu, v[g], 31);
+    }
+    // a run ends where the next one starts, or at the job's last row (rows without an
+    // adapter come first in an expert's order, never after a run)
+    int cur = -1, cur_l = -1;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      unsigned mm = m[g];
+      while (mm) {
+        const int b = __ffs(mm) - 1;
+        mm &= mm - 1;
+        const int l = __shfl_sync(0xffffffffu, v[g], b);
+        if (cur >= 0) f(cur_l, cur, 32 * g + b);
+        cur = 32 * g + b;
+        cur_l = l;
+      }
+    }
+    if (cur >= 0) f(cur_l, cur, rows);
+  }
+};
 
 // The CTA's abort flag as lane 0 of the warp reads it: every lane of a warp that loops
 // with warp-wide operations takes the same branch.
 __device__ __forceinline__ bool warp_aborted(volatile int* flag) {
   const int v = (threadIdx.x & 31) == 0 ? *flag : 0;
   return __shfl_sync(0xffffffffu, v, 0) != 0;
+}
+
+// AND of a predicate over the `n` threads that meet at named barrier `id`.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 template <int BN, int STAGES, bool kGLU>
@@ -117,24 +173,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_z, const FusedArgs p) {
   using C = FusedCfg<BN, STAGES, kGLU>;
+  // weight rows per output block: 64 gate + 64 up rows (kGLU) or 128 rows
+  constexpr int kWR = kGLU ? kFBM / 2 : kFBM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + STAGES;
-  uint64_t* tmem_full = empty + STAGES;  // [2]: one per accumulator set
+  uint64_t* tmem_full = empty + STAGES;  // [2]: one per accumulator
   uint64_t* tmem_empty = tmem_full + 2;  // [2]
   uint64_t* mma_done = tmem_empty + 2;   // after an abort: every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // expert-major: first row, row count
+  float* xt = reinterpret_cast<float*>(smem + C::kXOff);  // [128][kXStride] (kGLU)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool expert_major = p.mode == kFModeExpert;
   const bool persistent = p.mode == kFModePersistent;
   const int n_wblocks = p.n_wblocks;
-  // (tile, weight block) jobs in groups of kFGroupTiles tiles, so that CTAs sharing a
-  // weight block run together
+  // (token tile, weight block) jobs in groups of kFGroupTiles tiles, so that CTAs sharing
+  // a weight block run together
   auto tile_job = [&](int w, int n_tiles, int& e, int& wb, int& r0, int& rows) {
     const int per_group = kFGroupTiles * n_wblocks;
     const int grp = w / per_group;
@@ -176,11 +235,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // With `early`, everything but z was produced two or more launches back (the
   // predecessor, a shrink, triggers its dependents only after its own wait), so only
   // the first z copy waits for the predecessor; without it, every read waits.
-  int njobs, e0, wb0, r00 = 0, rows0 = 0, n_tiles = 0;
-  if (!p.early) pdl_wait();
+  // Expert-major CTAs know their weights from their index: they stream the first ring of
+  // weight stages before waiting in either case.
+  int njobs, e0, wb0, r00 = 0, rows0 = 0, n_tiles = 0, ks = 0;
+  if (!p.early && !expert_major) pdl_wait();
   if (expert_major) {
-    e0 = blockIdx.x / n_wblocks;
-    wb0 = blockIdx.x - e0 * n_wblocks;
+    const int jb = blockIdx.x / p.ksplit;
+    ks = blockIdx.x - jb * p.ksplit;
+    e0 = jb / n_wblocks;
+    wb0 = jb - e0 * n_wblocks;
     njobs = -1;  // known once the expert's rows are read
   } else {
     n_tiles = __ldcg(p.hdr + HDR_NTILES);
@@ -210,22 +273,35 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       return;
     }
   }
-  const int nk = (p.K + kFBK - 1) / kFBK;
+  // this CTA's k-blocks: [kb0, kb0 + nk) (all of them unless the K range is split)
+  const int nk_all = (p.K + kFBK - 1) / kFBK;
+  const int kper = (nk_all + p.ksplit - 1) / p.ksplit;
+  const int kb0 = ks * kper;
+  const int nk = max(0, min(nk_all, kb0 + kper) - kb0);
+  const bool lora = p.lora && ks == 0;  // the adapter term goes with the first K share
+  void* const out = static_cast<char*>(p.out) + (size_t)ks * p.part_stride * (kGLU ? 2 : 4);
   const int pre = nk < STAGES ? nk : STAGES;
 
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
+  // Weight block wb of expert e into a stage: rows [wb kWR, +kWR) of the gate half and,
+  // kGLU, of the up half (at up_off) below them -- one 128-row operand.
+  auto load_w = [&](uint8_t* sw, uint64_t* bar, int kb, int wb, int e, uint64_t pol) {
+    tma_load_3d(sw, &tm_w, bar, (kb0 + kb) * kFBK, wb * kWR, e, pol);
+    if (kGLU) tma_load_3d(sw + kWR * 128, &tm_w, bar, (kb0 + kb) * kFBK, p.up_off + wb * kWR, e, pol);
+  };
   // the first ring of weight stages of the first job (a weight never depends on a launch)
   if (threadIdx.x == 0) {
     const uint64_t pol_w = l2_policy_evict_first();
     for (int kb = 0; kb < pre; ++kb) {
-      uint8_t* sw = smem + kb * C::kStageBytes;
-      mbar_arrive_expect_tx(&full[kb], C::kNW * C::kWBytes);
-      tma_load_3d(sw, &tm_w, &full[kb], kb * kFBK, wb0 * kFBM, e0, pol_w);
-      if (kGLU) tma_load_3d(sw + C::kWBytes, &tm_w, &full[kb], kb * kFBK, p.up_off + wb0 * kFBM, e0, pol_w);
+      mbar_arrive_expect_tx(&full[kb], C::kWBytes);
+      load_w(smem + kb * C::kStageBytes, &full[kb], kb, wb0, e0, pol_w);
     }
+  }
+  if (!p.early && expert_major) pdl_wait();  // every thread, after the weights went out
+  if (threadIdx.x == 0) {
     if (!p.early) pdl_trigger();
     if (expert_major) {
       const int eb = __ldcg(p.expert_begin + e0), ee = __ldcg(p.expert_begin + e0 + 1);
@@ -252,14 +328,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
   };
   const int cph = p.zk ? 1 : p.zchunks / 2;  // chunked layout: stages per half (high, low)
+  // bytes of one B row and of one z row in shared memory (their boxes' widths)
+  const int b_row = p.b_cols * 2, z_row = p.z_cols * 2;
 
   bool waited0 = !p.early;  // thread 0 has passed griddepcontrol.wait
+  int issued = 0;           // producer: stages whose row (or z) copy went out
   if (warp == 0) {
     // producer: the whole warp walks the jobs (the adapter runs are found warp-wide);
     // lane 0 issues the copies
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_a = l2_policy_evict_last();
-    int g = 0, issued = 0;
+    int g = 0;
     if (njobs == 0 && lane == 0) {  // expert-major with no row: complete the prefetched stages
       for (int kb = 0; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
       for (int kb = 0; kb < pre; ++kb) mbar_wait_bounded(&full[kb], 0);
@@ -267,6 +346,49 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     for (int j = 0; j < njobs && !warp_aborted(s_abort); ++j) {
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
+      AdapterRows<(BN + 31) / 32> ar;
+      if (lora) ar.load(p.row_adapter, r0, rows);
+      // the adapter stages go after the first lora_at base stages (each accumulator is
+      // cleared by the job's first base stage), so their B loads overlap the base stream
+      auto adapter_stages = [&]() {
+        if (!lora || warp_aborted(s_abort)) return;
+        if (!waited0) {  // z comes from the predecessor
+          if (lane == 0) {
+            pdl_wait();
+            pdl_trigger();
+          }
+          waited0 = true;
+        }
+        ar.for_each_run([&](int l, int, int) {
+          for (int c = 0; c < p.zchunks; ++c, ++g) {
+            if (warp_aborted(s_abort)) return;
+            const int s = g % STAGES;
+            const uint32_t ph = (g / STAGES) & 1;
+            if (lane == 0) {
+              uint8_t* sw = smem + s * C::kStageBytes;
+              if (mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns)) {
+                const int bcol = 64 * (c % cph);
+                const int pair = l * p.E + e;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(kFBM * b_row));
+                tma_load_3d(sw, &tm_b, &full[s], bcol, wb * kWR, pair, pol_w);
+                if (kGLU)
+                  tma_load_3d(sw + kWR * b_row, &tm_b, &full[s], bcol, p.up_off + wb * kWR, pair,
+                              pol_w);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * z_row));
+                tma_load_2d(sw + C::kWBytes, &tm_z, &full[s], 64 * c,
+                            r0 + (e * p.L + l + 1) * p.gap, pol_a);
+                ++issued;
+              } else {
+                *s_abort = 1;
+              }
+            }
+            __syncwarp();
+          }
+        });
+      };
+      // (in the first job not before its stages whose weights were prefetched: those hold
+      // ring slots 0 .. pre - 1)
+      const int lora_at = min(max(j == 0 ? max(p.lora_at, pre) : p.lora_at, 1), nk);
       for (int kb = 0; kb < nk; ++kb, ++g) {
         const int s = g % STAGES;
         const uint32_t ph = (g / STAGES) & 1;
@@ -276,15 +398,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           if (ok && g >= pre) {
             ok = mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns);
             if (ok) {
-              mbar_arrive_expect_tx(&full[s], C::kNW * C::kWBytes);
-              tma_load_3d(sw, &tm_w, &full[s], kb * kFBK, wb * kFBM, e, pol_w);
-              if (kGLU)
-                tma_load_3d(sw + C::kWBytes, &tm_w, &full[s], kb * kFBK, p.up_off + wb * kFBM, e, pol_w);
+              mbar_arrive_expect_tx(&full[s], C::kWBytes);
+              load_w(sw, &full[s], kb, wb, e, pol_w);
             }
           }
           if (ok) {
             mbar_arrive_expect_tx(&full[s], C::kABytes);
-            tma_load_2d(sw + C::kNW * C::kWBytes, &tm_a, &full[s], kb * kFBK, r0, pol_a);
+            tma_load_2d(sw + C::kWBytes, &tm_a, &full[s], (kb0 + kb) * kFBK, r0, pol_a);
             ++issued;
           } else {
             *s_abort = 1;
@@ -292,45 +412,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
         __syncwarp();
         if (warp_aborted(s_abort)) break;
+        if (kb + 1 == lora_at) adapter_stages();
       }
-      if (!p.lora || warp_aborted(s_abort)) continue;
-      if (!waited0) {  // z comes from the predecessor
-        if (lane == 0) {
-          pdl_wait();
-          pdl_trigger();
-        }
-        waited0 = true;
-      }
-      for_each_adapter_run(p.row_adapter, r0, rows, [&](int l) {
-        for (int c = 0; c < p.zchunks; ++c, ++g) {
-          if (warp_aborted(s_abort)) return;
-          const int s = g % STAGES;
-          const uint32_t ph = (g / STAGES) & 1;
-          if (lane == 0) {
-            uint8_t* sw = smem + s * C::kStageBytes;
-            if (mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns)) {
-              const int bcol = 64 * (c % cph);
-              const int pair = l * p.E + e;
-              mbar_arrive_expect_tx(&full[s], C::kNW * C::kWBytes);
-              tma_load_3d(sw, &tm_b, &full[s], bcol, wb * kFBM, pair, pol_w);
-              if (kGLU) tma_load_3d(sw + C::kWBytes, &tm_b, &full[s], bcol, p.up_off + wb * kFBM, pair, pol_w);
-              mbar_arrive_expect_tx(&full[s], C::kABytes);
-              tma_load_2d(sw + C::kNW * C::kWBytes, &tm_z, &full[s], 64 * c,
-                          r0 + (e * p.L + l + 1) * p.gap, pol_a);
-              ++issued;
-            } else {
-              *s_abort = 1;
-            }
-          }
-          __syncwarp();
-        }
-      });
-    }
-    if (lane == 0 && *s_abort) {  // drain own copies in flight before the CTA may exit
-      // prefetched weight stages whose row copy was never issued miss one arrival
-      for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
-      for (int gg = (issued > pre ? issued : pre) - 1; gg >= 0 && gg >= issued - STAGES; --gg)
-        mbar_wait_bounded(&full[gg % STAGES], (gg / STAGES) & 1);
     }
   } else if (warp == 1) {
     // MMA issuer (lane 0); the warp walks the same jobs and adapter runs as the producer
@@ -339,43 +422,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
       const int a = j & 1;
-      const uint32_t acc = tmem + static_cast<uint32_t>(a * C::kSetCols);
+      const uint32_t acc = tmem + static_cast<uint32_t>(a * C::kAccCols);
       const uint32_t idesc = idesc_bf16_f32(kFBM, static_cast<uint32_t>((rows + 15) & ~15));
-      if (lane == 0 && j >= 2) {  // the epilogue must have read this set's previous job
+      AdapterRows<(BN + 31) / 32> ar;
+      if (lora) ar.load(p.row_adapter, r0, rows);
+      if (lane == 0 && j >= 2) {  // the epilogue must have read this accumulator's last job
         if (!mbar_wait_bounded(&tmem_empty[a], ((j >> 1) - 1) & 1, p.wait_ns)) *s_abort = 1;
         tc_fence_after();
       }
       __syncwarp();
       if (warp_aborted(s_abort)) break;
-      for (int kb = 0; kb < nk; ++kb, ++g) {
-        const int s = g % STAGES;
-        const uint32_t ph = (g / STAGES) & 1;
-        if (lane == 0) {
-          if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
-            *s_abort = 1;
-          } else {
-            tc_fence_after();
-            const uint8_t* sw = smem + s * C::kStageBytes;
-            const uint64_t dw = smem_desc_sw128(smem_u32(sw));
-            const uint64_t da = smem_desc_sw128(smem_u32(sw + C::kNW * C::kWBytes));
-#pragma unroll
-            for (int kk = 0; kk < kFBK / 16; ++kk) {
-              tc_mma_bf16(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
-              if (kGLU) {
-                const uint64_t du = smem_desc_sw128(smem_u32(sw + C::kWBytes));
-                tc_mma_bf16(acc + C::kAccCols, du + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
-              }
-            }
-            tc_commit(&empty[s]);
-          }
-        }
-        __syncwarp();
-        if (warp_aborted(s_abort)) break;
-      }
-      if (warp_aborted(s_abort)) break;
-      if (p.lora) {
-        for_each_adapter_run(p.row_adapter, r0, rows, [&](int l) {
-          (void)l;
+      auto adapter_stages = [&]() {
+        if (!lora || warp_aborted(s_abort)) return;
+        ar.for_each_run([&](int, int, int end) {
+          // the run's z rows are zero past its last row: the MMAs stop there (N = the run's
+          // end rounded up to 16), the accumulator columns beyond are left as they are
+          const uint32_t idr = idesc_bf16_f32(kFBM, static_cast<uint32_t>((end + 15) & ~15));
           for (int c = 0; c < p.zchunks; ++c, ++g) {
             if (warp_aborted(s_abort)) return;
             const int s = g % STAGES;
@@ -386,25 +448,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
               } else {
                 tc_fence_after();
                 const uint8_t* sw = smem + s * C::kStageBytes;
-                const uint64_t db = smem_desc_sw128(smem_u32(sw));
-                const uint64_t du = smem_desc_sw128(smem_u32(sw + C::kWBytes));
-                const uint64_t dz = smem_desc_sw128(smem_u32(sw + C::kNW * C::kWBytes));
+                const uint64_t db = smem_desc_swz(smem_u32(sw), p.b_layout, p.b_sbo);
+                const uint64_t dz = smem_desc_swz(smem_u32(sw + C::kWBytes), p.z_layout, p.z_sbo);
                 if (p.zk) {  // [high | low] in one row: both against the same B steps
                   for (int kk = 0; kk < p.zk; ++kk) {
-                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idesc, 1);
-                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * (p.zk + kk), idesc, 1);
-                    if (kGLU) {
-                      tc_mma_bf16(acc + C::kAccCols, du + 2 * kk, dz + 2 * kk, idesc, 1);
-                      tc_mma_bf16(acc + C::kAccCols, du + 2 * kk, dz + 2 * (p.zk + kk), idesc, 1);
-                    }
+                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
+                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * (p.zk + kk), idr, 1);
                   }
                 } else {  // chunk c of the high or the low half
                   const int rem = (p.rp16 - 64 * (c % cph)) / 16;
                   const int nm = rem < 4 ? rem : 4;
-                  for (int kk = 0; kk < nm; ++kk) {
-                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idesc, 1);
-                    if (kGLU) tc_mma_bf16(acc + C::kAccCols, du + 2 * kk, dz + 2 * kk, idesc, 1);
-                  }
+                  for (int kk = 0; kk < nm; ++kk) tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
                 }
                 tc_commit(&empty[s]);
               }
@@ -412,58 +466,90 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             __syncwarp();
           }
         });
+      };
+      // (in the first job not before its stages whose weights were prefetched: those hold
+      // ring slots 0 .. pre - 1)
+      const int lora_at = min(max(j == 0 ? max(p.lora_at, pre) : p.lora_at, 1), nk);
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        if (lane == 0) {
+          if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
+            *s_abort = 1;
+          } else {
+            tc_fence_after();
+            const uint8_t* sw = smem + s * C::kStageBytes;
+            const uint64_t dw = smem_desc_sw128(smem_u32(sw));
+            const uint64_t da = smem_desc_sw128(smem_u32(sw + C::kWBytes));
+#pragma unroll
+            for (int kk = 0; kk < kFBK / 16; ++kk)
+              tc_mma_bf16(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
+            tc_commit(&empty[s]);
+          }
+        }
+        __syncwarp();
+        if (warp_aborted(s_abort)) break;
+        if (kb + 1 == lora_at) adapter_stages();
       }
       if (warp_aborted(s_abort)) break;
       if (lane == 0) tc_commit(&tmem_full[a]);  // fires when every MMA issued above completes
       __syncwarp();
     }
-    if (lane == 0 && *s_abort) {  // MMAs still in flight read shared memory and write TMEM
-      tc_commit(mma_done);
-      mbar_wait_bounded(mma_done, 0);
-    }
   } else {
-    // epilogue: warp w reads TMEM lanes [32 (w % 4), 32 (w % 4) + 32), i.e. 32 output
-    // features, for every row of the job
+    // epilogue: warp w reads TMEM lanes [32 (w % 4), 32 (w % 4) + 32), i.e. 32 rows of the
+    // weight block, for every token of the job
     const int quad = warp & 3;
     bool waited = !p.early;
     for (int j = 0; j < njobs; ++j) {
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
       const int a = j & 1;
-      const bool ok =
-          __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1, p.wait_ns) ? 1 : 0);
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1, p.wait_ns) ? 1 : 0);
       if (!ok) *s_abort = 1;
-      if (!ok || warp_aborted(s_abort)) break;
+      ok = ok && !warp_aborted(s_abort);
+      if (kGLU) ok = bar_and(1, 128, ok);  // the four warps meet at the exchange below
+      if (!ok) break;
       tc_fence_after();
       if (!waited) {  // nothing is written before the predecessor has completed
         pdl_wait();
         waited = true;
       }
-      const int n = wb * kFBM + quad * 32 + lane;
-      const uint32_t taddr = tmem + static_cast<uint32_t>(a * C::kSetCols) +
+      const uint32_t taddr = tmem + static_cast<uint32_t>(a * C::kAccCols) +
                              (static_cast<uint32_t>(quad * 32) << 16);
       const uint32_t nmma = static_cast<uint32_t>((rows + 15) & ~15);
-      for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(taddr + c0, v);
-        if (kGLU) {
-          uint32_t u[16];
-          tmem_ld_x16(taddr + C::kAccCols + c0, u);
+      if (kGLU) {
+        // lanes 0..63 hold gate, 64..127 up of features f0 .. f0 + 63: every warp parks its
+        // 32 rows x 16 tokens in the exchange tile, then thread t takes feature t % 64 for
+        // 8 tokens (a warp stores 32 consecutive features of a token row)
+        const int t = (warp - 2) * 32 + lane;  // 0..127 over the epilogue warps
+        const int f = t & 63, tq = (t >> 6) * 8;
+        const int n = wb * kWR + f;
+        __nv_bfloat16* h = static_cast<__nv_bfloat16*>(out);
+        for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_x16(taddr + c0, v);
           tmem_ld_wait();
-          if (n < p.n_out) {
-            __nv_bfloat16* h = static_cast<__nv_bfloat16*>(p.out);
+          float* xr = xt + (quad * 32 + lane) * kXStride;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const int tok = static_cast<int>(c0) + q;
-              if (tok < rows)
-                h[(size_t)(r0 + tok) * p.n_out + n] =
-                    __float2bfloat16_rn(silu_fast(__uint_as_float(v[q])) * __uint_as_float(u[q]));
-            }
+          for (int q = 0; q < 16; ++q) xr[q] = __uint_as_float(v[q]);
+          bar_sync(1, 128);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int tok = static_cast<int>(c0) + tq + q;
+            const float gv = xt[f * kXStride + tq + q], uv = xt[(64 + f) * kXStride + tq + q];
+            if (tok < rows && n < p.n_out)
+              h[(size_t)(r0 + tok) * p.n_out + n] = __float2bfloat16_rn(silu_fast(gv) * uv);
           }
-        } else {
+          bar_sync(1, 128);  // the tile is read before the next chunk overwrites it
+        }
+      } else {
+        const int n = wb * kWR + quad * 32 + lane;
+        float* o = static_cast<float*>(out);
+        for (uint32_t c0 = 0; c0 < nmma; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_x16(taddr + c0, v);
           tmem_ld_wait();
           if (n < p.n_out) {
-            float* o = static_cast<float*>(p.out);
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const int tok = static_cast<int>(c0) + q;
@@ -479,11 +565,28 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // Past this barrier every role has stopped issuing and the abort flag is final. After a
+  // give-up -- by any warp, possibly after another role had already finished its loop --
+  // copies may still be landing in shared memory and MMAs still writing TMEM: both are
+  // drained before the CTA frees its tensor memory and exits (these waits keep the full
+  // limit).
+  const bool aborted = *s_abort != 0;
+  if (aborted && threadIdx.x == 0) {
+    // prefetched weight stages whose row copy was never issued miss one arrival
+    for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
+    for (int gg = (issued > pre ? issued : pre) - 1; gg >= 0 && gg >= issued - STAGES; --gg)
+      mbar_wait_bounded(&full[gg % STAGES], (gg / STAGES) & 1);
+  }
+  if (aborted && threadIdx.x == 32) {
+    tc_commit(mma_done);  // arrives once every MMA this thread issued has completed
+    mbar_wait_bounded(mma_done, 0);
+  }
   if (threadIdx.x == 0) {
-    if (*s_abort) set_dev_error(p.hdr, MOE_LORA_DEVERR_TIMEOUT);
+    if (aborted) set_dev_error(p.hdr, MOE_LORA_DEVERR_TIMEOUT);
     if (!waited0) pdl_wait();  // a CTA leaves only once its predecessor has completed
   }
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -504,7 +607,8 @@ static int launch_fused_t(const CUtensorMap& tw, const CUtensorMap& ta, const CU
     return MOE_LORA_OK;
   });
   if (st != MOE_LORA_OK) return st;
-  int64_t grid = (int64_t)(args.mode == kFModeExpert ? E : args.max_tiles) * args.n_wblocks;
+  int64_t grid = (int64_t)(args.mode == kFModeExpert ? E * args.ksplit : args.max_tiles) *
+                 args.n_wblocks;
   if (args.mode == kFModePersistent) {  // one resident CTA per SM slot, each looping over jobs
     int per_sm = 0;
     ML_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
@@ -541,18 +645,23 @@ ZPadLayout zpad_layout(int S, int E, int L, int r, int gap) {
 int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const void* zpad,
                       const ZPadLayout& zl, const moe_lora_align_t* al, const AlignLayout& a,
                       int N_w, int K, int r, bool glu, void* out, cudaStream_t stream, bool pdl,
-                      bool early, int expert_major_bn, unsigned long long wait_ns) {
+                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit) {
   if (a.S == 0) return MOE_LORA_OK;
+  // a split of the K range: expert-major down form only, at least two k-blocks a share
+  if (ksplit < 1 || (ksplit > 1 && (glu || expert_major_bn == 0 || ceil_div(K, kFBK) < 2 * ksplit)))
+    return MOE_LORA_ERR_UNSUPPORTED;
   AlignView v = align_view(al->buf, a);
+  // rows per job: the expert-major chunk, else the align's token tile
   const int bn = expert_major_bn > 0 ? expert_major_bn : al->bm_base;
   const int mode = expert_major_bn > 0 ? kFModeExpert : bn >= 128 ? kFModePersistent : kFModeTile;
   const bool lora = al->L > 0 && B != nullptr && zpad != nullptr;
   if (lora && (zl.gap < bn || r % 8 != 0 || zl.rows >= (1ll << 31))) return MOE_LORA_ERR_UNSUPPORTED;
+  const int wrows = glu ? kFBM / 2 : kFBM;  // weight rows per box (gate and up halves: 64 each)
   CUtensorMap tw, ta, tb, tz;
   {
     const uint64_t dims[3] = {(uint64_t)K, (uint64_t)N_w, (uint64_t)al->E};
     const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)N_w * K * 2};
-    const uint32_t box[3] = {kFBK, kFBM, 1};
+    const uint32_t box[3] = {kFBK, (uint32_t)wrows, 1};
     int st = make_tmap_bf16(&tw, W, 3, dims, strides, box);
     if (st != MOE_LORA_OK) return st;
   }
@@ -563,16 +672,27 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
     int st = make_tmap_bf16(&ta, a_sorted, 2, dims, strides, box);
     if (st != MOE_LORA_OK) return st;
   }
+  // LoRA tiles only as wide as the rank needs: B of rank 16 or 32 in 32- or 64-byte rows,
+  // z [high | low] of rank 16 or 32 in 64- or 128-byte rows; larger ranks in 64-column
+  // chunks of 128-byte rows. The TMA engine writes every byte of a box (its out-of-range
+  // part as zeros), so narrower boxes move less through shared memory.
+  const int b_cols = zl.zk ? zl.rp16 : kFBK;
+  const int z_cols = zl.zk ? 2 * zl.rp16 : kFBK;
+  auto swz = [](int cols) {
+    return cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                              : CU_TENSOR_MAP_SWIZZLE_128B;
+  };
+  auto layout = [](int cols) { return cols == 16 ? 6u : cols == 32 ? 4u : 2u; };
   if (lora) {
     const uint64_t dims[3] = {(uint64_t)r, (uint64_t)N_w, (uint64_t)al->L * al->E};
     const uint64_t strides[2] = {(uint64_t)r * 2, (uint64_t)N_w * r * 2};
-    const uint32_t box[3] = {kFBK, kFBM, 1};
-    int st = make_tmap_bf16(&tb, B, 3, dims, strides, box);
+    const uint32_t box[3] = {(uint32_t)b_cols, (uint32_t)wrows, 1};
+    int st = make_tmap_bf16(&tb, B, 3, dims, strides, box, swz(b_cols));
     if (st != MOE_LORA_OK) return st;
     const uint64_t zdims[2] = {(uint64_t)zl.zw, (uint64_t)zl.rows};
     const uint64_t zstrides[1] = {(uint64_t)zl.zw * 2};
-    const uint32_t zbox[2] = {kFBK, (uint32_t)bn};
-    st = make_tmap_bf16(&tz, zpad, 2, zdims, zstrides, zbox);
+    const uint32_t zbox[2] = {(uint32_t)z_cols, (uint32_t)bn};
+    st = make_tmap_bf16(&tz, zpad, 2, zdims, zstrides, zbox, swz(z_cols));
     if (st != MOE_LORA_OK) return st;
   } else {
     tb = tw;
@@ -587,32 +707,43 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
   args.n_out = glu ? N_w / 2 : N_w;
   args.up_off = glu ? N_w / 2 : 0;
   args.K = K;
-  args.n_wblocks = ceil_div(args.n_out, kFBM);
+  args.n_wblocks = ceil_div(args.n_out, wrows);
   args.max_tiles = a.max_tiles;
   args.mode = mode;
+  args.ksplit = ksplit;
+  args.part_stride = (size_t)a.S * (size_t)args.n_out;
   args.early = early ? 1 : 0;
   args.E = al->E;
   args.L = al->L;
   args.gap = zl.gap;
   args.lora = lora ? 1 : 0;
+  // the gate_up form's z is ready as the GEMM starts (its shrink computed before waiting):
+  // the adapter stages follow the first base stage; the down form's shrink starts when
+  // the gate_up GEMM ends: the stages wait until half the K range has streamed
+  args.lora_at = glu ? 1 : std::max(1, ceil_div(K, kFBK) / (2 * ksplit));
   args.zchunks = lora ? zl.zchunks : 0;
   args.zk = zl.zk;
   args.rp16 = zl.rp16;
+  args.b_cols = b_cols;
+  args.z_cols = z_cols;
+  args.b_layout = layout(b_cols);
+  args.b_sbo = 8u * (uint32_t)b_cols * 2u;
+  args.z_layout = layout(z_cols);
+  args.z_sbo = 8u * (uint32_t)z_cols * 2u;
   args.wait_ns = wait_ns;
-  if (glu) {
-    switch (bn) {
-      case 16: return launch_fused_t<16, 5, true>(tw, ta, tb, tz, args, al->E, stream, pdl);
-      case 32: return launch_fused_t<32, 5, true>(tw, ta, tb, tz, args, al->E, stream, pdl);
-      case 64: return launch_fused_t<64, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl);
-      case 128: return launch_fused_t<128, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl);
-      default: return MOE_LORA_ERR_UNSUPPORTED;
-    }
-  }
+  // stages: 192-200 KB of ring with one CTA per SM (128 and 256 rows), about 100 KB with
+  // two (16 to 64 rows, the decode shapes)
   switch (bn) {
-    case 16: return launch_fused_t<16, 6, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
-    case 32: return launch_fused_t<32, 5, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
-    case 64: return launch_fused_t<64, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
-    case 128: return launch_fused_t<128, 6, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 16: return glu ? launch_fused_t<16, 6, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                        : launch_fused_t<16, 6, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 32: return glu ? launch_fused_t<32, 5, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                        : launch_fused_t<32, 5, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 64: return glu ? launch_fused_t<64, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                        : launch_fused_t<64, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 128: return glu ? launch_fused_t<128, 6, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                         : launch_fused_t<128, 6, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 256: return glu ? launch_fused_t<256, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                         : launch_fused_t<256, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
 }

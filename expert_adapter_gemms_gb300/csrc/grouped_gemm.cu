@@ -40,7 +40,7 @@ struct GemmCfg {
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-  static_assert((2 * STAGES + 5) * 8 + 16 <= 256, "barrier area");
+  static_assert((2 * STAGES + 5) * 8 + 24 <= 256, "barrier area");
   static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;  // one fp32 accumulator
   static constexpr uint32_t kTmemCols = 2 * kAccCols;     // two, used alternately
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
@@ -137,6 +137,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_job = reinterpret_cast<int*>(tmem_slot + 2);  // expert-major: first row, row count
+  int* s_issued = s_job + 2;  // the producer's count of stages whose token copy went out
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -299,12 +300,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++issued;
         }
       }
-      if (*s_abort) {  // drain own copies in flight before the CTA may exit
-        // prefetched weight stages whose token copy was never issued miss one arrival
-        for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
-        for (int g = (issued > pre ? issued : pre) - 1; g >= 0 && g >= issued - STAGES; --g)
-          mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1);
-      }
+      s_issued[0] = issued;  // for the drain after the final barrier
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -341,10 +337,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_commit(&tmem_full[a]);  // fires when every MMA issued above has completed
       }
-      if (*s_abort) {  // MMAs still in flight read shared memory and write TMEM: drain them
-        tc_commit(mma_done);
-        mbar_wait_bounded(mma_done, 0);
-      }
     }
   } else {
     // epilogue: warp w may read TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
@@ -380,8 +372,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0 && *s_abort) set_dev_error(hdr, MOE_LORA_DEVERR_TIMEOUT);
+  // Past this barrier every role has stopped issuing and the abort flag is final. After a
+  // give-up -- by any warp, possibly after another role had already finished its loop --
+  // copies may still be landing in shared memory and MMAs still writing TMEM: both are
+  // drained before the CTA frees its tensor memory and exits (these waits keep the full
+  // limit).
+  const bool aborted = *s_abort != 0;
+  if (aborted && threadIdx.x == 0) {
+    const int issued = s_issued[0];
+    // prefetched weight stages whose token copy was never issued miss one arrival
+    for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
+    for (int g = (issued > pre ? issued : pre) - 1; g >= 0 && g >= issued - STAGES; --g)
+      mbar_wait_bounded(&full[g % STAGES], (g / STAGES) & 1);
+  }
+  if (aborted && threadIdx.x == 32) {
+    tc_commit(mma_done);  // arrives once every MMA this thread issued has completed
+    mbar_wait_bounded(mma_done, 0);
+  }
+  if (threadIdx.x == 0 && aborted) set_dev_error(hdr, MOE_LORA_DEVERR_TIMEOUT);
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -411,7 +421,7 @@ static EncodeTiledFn get_encode_fn() {
 
 // bf16 tensor map, innermost dimension K (contiguous), 128-byte swizzle, box {64, box_rows[, 1]}.
 int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                          const uint64_t* strides_bytes, const uint32_t* box) {
+                   const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return MOE_LORA_ERR_CUDA;
   cuuint64_t gd[3], gs[2];
@@ -422,7 +432,7 @@ int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* d
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bd,
-                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_LORA_OK : MOE_LORA_ERR_CUDA;
 }

@@ -16,10 +16,11 @@ int launch_gather(const void* x, const moe_lora_align_t* al, const AlignLayout& 
                   void* xs, cudaStream_t stream, bool pdl, bool trigger_first);
 
 // bf16 tensor map over `rank` (2 or 3) dimensions, innermost first (dims[0] contiguous),
-// byte strides of dimensions 1.. in strides_bytes, box `box`, 128-byte swizzle, zero fill
-// out of bounds. Host only; no device work.
+// byte strides of dimensions 1.. in strides_bytes, box `box` (box[0] x 2 bytes equal to the
+// swizzle width), zero fill out of bounds. Host only; no device work.
 int make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                   const uint64_t* strides_bytes, const uint32_t* box);
+                   const uint64_t* strides_bytes, const uint32_t* box,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // silu(v) = v / (1 + exp(-v)) with the hardware exponential and a reciprocal-based
 // divide (CUDA's __expf, __fdividef): a few fp32 ulps, far below the bf16 rounding of the
@@ -63,14 +64,18 @@ struct ZPadOut {
 // [L, E, N_w, r]. glu: N_w = 2I and out is h [S, I] bf16 = silu(gate) * up; else out is
 // [S, N_w] fp32. B or zpad null (or L = 0): the base GEMM only. `early`: everything but z
 // may be read before griddepcontrol.wait.
+// ksplit > 1 (expert-major down form): the K range in ksplit shares, each CTA writing its
+// own partial output at out + share * S * N (the combine sums them).
 int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const void* zpad,
                       const ZPadLayout& zl, const moe_lora_align_t* al, const AlignLayout& a,
                       int N_w, int K, int r, bool glu, void* out, cudaStream_t stream, bool pdl,
-                      bool early, int expert_major_bn, unsigned long long wait_ns);
+                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit = 1);
 
-// y[t] = sum_j w[t, j] O[row(t, j)] (j ascending) over O [S, N] fp32 by sorted row.
+// y[t] = sum_j w[t, j] O[row(t, j)] (j ascending) over O [S, N] fp32 by sorted row; with
+// nparts > 1, O holds nparts partial outputs part_stride elements apart, summed in order.
 int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
-                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl);
+                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl,
+                   int nparts = 1, size_t part_stride = 0);
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,
                   int N, int r, int epilogue, float* base, void* out, int out_fp32,
@@ -84,7 +89,12 @@ int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, con
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
                        const moe_lora_align_t* al, const AlignLayout& a, int K, int r, int rs,
                        float* Z, cudaStream_t stream, bool pdl, bool early,
-                       unsigned long long wait_ns = kWaitLimitNs, const ZPadOut* zpad = nullptr);
+                       unsigned long long wait_ns = kWaitLimitNs, const ZPadOut* zpad = nullptr,
+                       int flags = 0);
+// flags of launch_shrink_impl: every CTA resident at once; the block table is two or more
+// launches old, so each CTA reads its block and prefetches its rows of A into L2 before its
+// wait (for a shrink whose activations come from its immediate predecessor)
+enum { kShrinkOneWave = 1, kShrinkPrefetchA = 2 };
 // expert_major_bn > 0: one CTA per (expert, weight block) taking the expert's rows in
 // chunks of that many rows (16..256), which lets the weights stream before the align
 // tables exist; 0: one CTA per (token tile of bm_base rows, weight block).

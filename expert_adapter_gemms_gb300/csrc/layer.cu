@@ -109,14 +109,13 @@ static int expert_major_rows(int T, int k, int E) {
 }
 
 // The fused expand's token tile (and so the zero gap of its shifted z buffers) that the
-// heuristics give a shape: the expert-major chunk, else the token tile capped at 128 rows
-// (the gate and up accumulators of two jobs fill TMEM at 128).
+// heuristics give a shape: the expert-major chunk, else the align's token tile.
 static int fused_gap(int T, int k, int E, int L) {
   const int em = expert_major_rows(T, k, E);
   if (em) return em;
   int32_t hb, hl;
   pick_tiles(T, k, E, L, &hb, &hl);
-  return hb < 128 ? hb : 128;
+  return hb;
 }
 
 struct LayerPlan {
@@ -124,7 +123,7 @@ struct LayerPlan {
   int bm_base, bm_lora, em_bn;
   bool fused;    // expand (and SwiGLU) inside the grouped GEMMs
   ZPadLayout z;  // the shifted z buffers of the fused chain (both the same shape)
-  int launches;  // kernels of one call routed from logits
+  int ksplit;    // fused, expert-major: CTAs per down weight block (partial outputs)
   int64_t off_align, off_ids, off_w, off_xs, off_G, off_Z1, off_h, off_Z2, off_O, off_Z1p,
       off_Z2p, total;
   bool valid;
@@ -150,13 +149,24 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r,
   const int64_t zbytes = L > 0 ? (int64_t)round_up((size_t)(p.z.rows * p.z.zw * 2), 256) : 0;
   const int64_t g_bytes = S * 2 * (int64_t)I * 4;
   const bool shape_ok = L == 0 || (r % 8 == 0 && 2 * zbytes <= std::max<int64_t>(g_bytes, 64ll << 20));
-  const bool want = shape_ok && opt.expand_mode != 1 &&
+  // ... where it pays: with adapters at few rows per expert (the grouped GEMMs then stream
+  // weights, and the adapter stages add bytes, not time) or where the (expert, adapter) runs
+  // are long (each run's stages multiply a whole token tile, so short runs waste tensor
+  // work); without adapters where token tiles, not expert-major chunks, are used
+  const int em_shape = expert_major_rows(T, k, E);
+  const bool long_runs = L > 0 && S >= 16 * std::min<int64_t>((int64_t)E * L, S);
+  const bool pays = L == 0 ? em_shape == 0 : (em_shape > 0 || long_runs);
+  const bool want = shape_ok && opt.expand_mode != 1 && (pays || opt.expand_mode == 2) &&
                     (L == 0 || (opt.adapter_ranks == nullptr && slices == 1));
-  p.em_bn = pdl ? expert_major_rows(T, k, E) : 0;
-  p.bm_base = opt.bm_base > 0 ? opt.bm_base : (want && hb > 128 ? 128 : hb);
+  p.em_bn = pdl ? em_shape : 0;
+  p.bm_base = opt.bm_base > 0 ? opt.bm_base : hb;
   p.bm_lora = opt.bm_lora > 0 ? opt.bm_lora : hl;
   const int chunk = p.em_bn > 0 ? p.em_bn : p.bm_base;
-  p.fused = want && chunk <= gap && chunk <= 128;
+  p.fused = want && chunk <= gap;
+  // few rows per expert: the down GEMM's (expert, weight block) CTAs are few against the
+  // SMs' slots (2.4 waves at the GPT-OSS decode shape), so each block's K range is split in
+  // two and the combine sums both partial outputs (4.8 waves)
+  p.ksplit = p.fused && p.em_bn > 0 && (I + 63) / 64 >= 4 ? 2 : 1;
   p.al = align_layout(T, k, E, L, p.bm_base, p.bm_lora);
   // the align region is sized for the smallest tiles so any tile choice fits
   AlignLayout worst = align_layout(T, k, E, L, 16, 1);
@@ -173,18 +183,113 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r,
   p.off_Z1 = take(S * 2 * rr * 4);  // two z slices with separate gate and up adapters
   p.off_h = take(S * (int64_t)I * 2);
   p.off_Z2 = take(S * rr * 4);
-  p.off_O = take(S * (int64_t)H * 4);
+  p.off_O = take(S * (int64_t)H * 4 * (em_shape > 0 ? 2 : 1));  // room for two partial outputs
   p.total = o;
-  // launches of one call routed from logits
-  const int align_n = p.al.ctas > 0 ? 3 : 1;
-  if (p.fused) {
-    p.launches = 1 + align_n + 1 + 2 + 1 + (L > 0 ? 2 : 0);
-  } else {
-    const bool add_then_combine = L > 0 && S >= 2 * (int64_t)E * L;
-    p.launches = 1 + align_n + 1 + 2 + 2 + (L > 0 ? 2 : 0) + (add_then_combine ? 1 : 0);
-  }
   p.valid = true;
   return p;
+}
+
+// ---------------------------------------------------------------------------
+// The chain of launches and the reads made before a kernel's wait
+// ---------------------------------------------------------------------------
+// Under programmatic dependent launch a kernel starts once every CTA of its predecessor
+// has triggered its dependents (or exited), and no kernel of the layer completes before
+// its own griddepcontrol.wait has returned, i.e. before its predecessor completed. So
+// when launch c starts, an earlier launch p has completed if p <= c - 2 and launch c - 1
+// triggers only after its own wait. Reads a kernel makes before its wait ("early" reads:
+// weights, older activations, the align tables) rely on exactly that. The chain records,
+// per step, its launches, whether they trigger only after waiting, and the steps whose
+// outputs the step reads early; the layer refuses a chain that breaks the rule, and every
+// launch takes its early flag from here.
+enum Step { kRoute, kAlign, kGather, kShrink1, kGemm1, kExpand1, kShrink2, kGemm2, kExpand2,
+            kCombine, kNumSteps };
+struct Chain {
+  int first[kNumSteps], last[kNumSteps];  // launch indices of each step (-1: not launched)
+  int src[kNumSteps][3];                  // steps read before the wait (-1: none)
+  bool after_wait[24];                    // per launch: triggers only after its wait
+  int n;                                  // launches
+  bool early(Step s) const { return src[s][0] >= 0; }
+  int early_reads() const {
+    int c = 0;
+    for (int s = 0; s < kNumSteps; ++s)
+      for (int i = 0; i < 3; ++i) c += src[s][i] >= 0 && last[src[s][i]] >= 0;
+    return c;
+  }
+  // every early read comes from a launch that has completed when the reader starts
+  bool ok() const {
+    for (int s = 0; s < kNumSteps; ++s) {
+      for (int i = 0; i < 3; ++i) {
+        const int t = src[s][i];
+        if (t < 0 || last[t] < 0) continue;  // a caller input (e.g. routing given by the caller)
+        const int c = first[s];
+        if (c < 0 || c - last[t] < 2 || !after_wait[c - 1]) return false;
+      }
+    }
+    return true;
+  }
+};
+
+static Chain layer_chain(const LayerPlan& p, int T, int k, int E, int L, bool have_logits,
+                         bool pdl) {
+  Chain c;
+  for (int s = 0; s < kNumSteps; ++s) {
+    c.first[s] = c.last[s] = -1;
+    c.src[s][0] = c.src[s][1] = c.src[s][2] = -1;
+  }
+  c.n = 0;
+  auto add = [&](Step s, int kernels, bool after_wait) {
+    c.first[s] = c.n;
+    for (int i = 0; i < kernels; ++i) c.after_wait[c.n++] = after_wait;
+    c.last[s] = c.n - 1;
+  };
+  auto reads = [&](Step s, int a, int b = -1, int d = -1) {
+    if (!pdl) return;  // plain stream order: every read follows its producer's completion
+    c.src[s][0] = a;
+    c.src[s][1] = b;
+    c.src[s][2] = d;
+  };
+  const bool lora = L > 0;
+  if (have_logits) add(kRoute, 1, false);       // triggers at its start
+  add(kAlign, p.al.ctas > 0 ? 3 : 1, false);    // each align kernel triggers at its start
+  if (p.fused) {
+    add(kGather, 1, lora || p.em_bn == 0);  // base only, expert-major: triggers at its start
+    if (lora) {
+      add(kShrink1, 1, true);
+      reads(kShrink1, kAlign);                  // x by token (a caller input), the tables
+    }
+    add(kGemm1, 1, true);
+    if (lora) reads(kGemm1, kGather, kAlign);   // gathered rows, tables; z only after the wait
+    if (lora) {                                 // h is its predecessor's: waits for it, but
+      add(kShrink2, 1, true);                   // reads its block and prefetches A first
+      reads(kShrink2, kAlign);
+    }
+    add(kGemm2, 1, true);
+    if (lora) reads(kGemm2, kGemm1, kAlign);    // h, tables; z only after the wait
+    add(kCombine, 1, true);
+    return c;
+  }
+  const bool em = p.em_bn > 0;
+  add(kGather, 1, !em);  // expert-major: the gate_up GEMM reads nothing of it early
+  add(kGemm1, 1, true);
+  if (!em) reads(kGemm1, kAlign);  // the token tiles
+  if (lora) {
+    add(kShrink1, 1, true);
+    if (p.bm_lora <= 8) reads(kShrink1, kGather, kAlign);  // gathered rows
+    else reads(kShrink1, kAlign);                          // x by token
+  }
+  add(kExpand1, 1, true);
+  if (lora) reads(kExpand1, kGemm1, kAlign);  // G, B, tables; z after the wait
+  add(kGemm2, 1, true);
+  if (!em) reads(kGemm2, kAlign);
+  if (lora) {
+    add(kShrink2, 1, true);
+    reads(kShrink2, kExpand1, kAlign);  // h
+  }
+  // the down expand: a token walk, or (several rows per pair) an in-place add and a combine
+  const bool add_then_combine = lora && (int64_t)T * k >= 2 * (int64_t)E * L;
+  add(kExpand2, add_then_combine ? 2 : 1, true);
+  if (lora) reads(kExpand2, kGemm2, kAlign, kRoute);  // O, tables, routing weights
+  return c;
 }
 
 }  // namespace moe_lora
@@ -242,11 +347,15 @@ extern "C" int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int
   if (opts) o = *opts;
   LayerPlan p = plan_layer(T, k, E, L, H, I, r, o);
   if (!p.valid) return MOE_LORA_ERR_UNSUPPORTED;
+  const bool pdl = !o.disable_pdl;
+  const Chain c = layer_chain(p, T, k, E, L, true, pdl);
+  if (!c.ok() || !layer_chain(p, T, k, E, L, false, pdl).ok()) return MOE_LORA_ERR_UNSUPPORTED;
   out->bm_base = p.bm_base;
   out->bm_lora = p.bm_lora;
   out->expert_major_rows = p.em_bn;
   out->fused_expand = p.fused ? 1 : 0;
-  out->launches = T > 0 ? p.launches : 0;
+  out->launches = T > 0 ? c.n : 0;
+  out->early_reads = c.early_reads();
   return MOE_LORA_OK;
 }
 
@@ -304,6 +413,8 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool pdl = !o.disable_pdl;
+  const Chain ch = layer_chain(p, T, k, E, L, have_logits, pdl);
+  if (!ch.ok()) return MOE_LORA_ERR_UNSUPPORTED;
   char* ws = static_cast<char*>(workspace);
   moe_lora_align_t al;
   al.buf = ws + p.off_align;
@@ -367,26 +478,31 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
     zo.row_expert = av.row_expert;
     zo.row_adapter = av.row_adapter;
     const bool lora = L > 0;
-    ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, false));
+    // without adapters the gate_up GEMM follows the gather and reads nothing of it early:
+    // the gather then triggers at its start so that the (expert-major) GEMM streams weights
+    ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, !lora && em_bn > 0));
     ML_STEP(mark(3));
     if (lora) {  // by token: x is a caller input, the align tables two launches back
       zo.p = Z1p;
-      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, r, nullptr, stream, pdl, pdl, wait_ns, &zo));
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, r, r, nullptr, stream, pdl,
+                                 ch.early(kShrink1), wait_ns, &zo, kShrinkOneWave));
     }
     ML_STEP(mark(4));
     ML_STEP(launch_fused_gemm(xs, W1, lora ? B1 : nullptr, Z1p, p.z, &al, p.al, 2 * I, H, r, true, h,
-                              stream, pdl, pdl && lora, em_bn, wait_ns));
+                              stream, pdl, ch.early(kGemm1), em_bn, wait_ns));
     ML_STEP(mark(5));
     ML_STEP(mark(6));
-    if (lora) {  // h comes from the predecessor: the shrink waits first
+    if (lora) {  // h comes from the predecessor: the shrink waits for it, A streams first
       zo.p = Z2p;
-      ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, nullptr, stream, pdl, false, wait_ns, &zo));
+      ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, nullptr, stream, pdl, false, wait_ns,
+                                 &zo, kShrinkOneWave | (ch.early(kShrink2) ? kShrinkPrefetchA : 0)));
     }
     ML_STEP(mark(7));
     ML_STEP(launch_fused_gemm(h, W2, lora ? B2 : nullptr, Z2p, p.z, &al, p.al, H, I, r, false, O,
-                              stream, pdl, pdl && lora, em_bn, wait_ns));
+                              stream, pdl, ch.early(kGemm2), em_bn, wait_ns, p.ksplit));
     ML_STEP(mark(8));
-    ML_STEP(launch_combine(O, w, &al, p.al, H, y, y_fp32, stream, pdl));
+    ML_STEP(launch_combine(O, w, &al, p.al, H, y, y_fp32, stream, pdl, p.ksplit,
+                           (size_t)T * k * H));
     ML_STEP(mark(9));
     return MOE_LORA_OK;
   }
@@ -394,29 +510,35 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   // stream from the start of the layer while routing, align and gather finish.
   ML_STEP(launch_gather(x, &al, p.al, H, xs, stream, pdl, em_bn > 0));
   ML_STEP(mark(3));
-  ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, pdl, em_bn, wait_ns));
+  ML_STEP(launch_grouped_gemm_impl(xs, W1, &al, p.al, 2 * I, H, G, stream, pdl, ch.early(kGemm1),
+                                   em_bn, wait_ns));
   ML_STEP(mark(4));
   // Short LoRA blocks (decode-like) read the gathered rows: addressed by sorted row, they
   // need no slot lookup before the load (and are recent in L2).
   if (L > 0) {
     // with separate gate and up adapters the gate_up shrink is one of rank 2r
     if (p.bm_lora <= 8)
-      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl, wait_ns));
+      ML_STEP(launch_shrink_impl(xs, 1, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl,
+                                 ch.early(kShrink1), wait_ns));
     else
-      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl, pdl, wait_ns));
+      ML_STEP(launch_shrink_impl(x, 0, A1, &al, p.al, H, slices * r, r, Z1, stream, pdl,
+                                 ch.early(kShrink1), wait_ns));
   }
   ML_STEP(mark(5));
   ML_STEP(launch_expand_impl(Z1, L > 0 ? B1 : nullptr, &al, p.al, 2 * I, rr, L > 0 && slices == 2 ? 3 : 1, G, h, 0,
-                             nullptr, stream, pdl, pdl && L > 0));
+                             nullptr, stream, pdl, ch.early(kExpand1)));
   ML_STEP(mark(6));
   // the down GEMM likewise runs expert-major when experts hold few rows: its weights stream
   // while the SwiGLU expand drains
-  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, pdl, em_bn, wait_ns));
+  ML_STEP(launch_grouped_gemm_impl(h, W2, &al, p.al, H, I, O, stream, pdl, ch.early(kGemm2), em_bn,
+                                   wait_ns));
   ML_STEP(mark(7));
-  if (L > 0) ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, pdl, wait_ns));
+  if (L > 0)
+    ML_STEP(launch_shrink_impl(h, 1, A2, &al, p.al, I, r, r, Z2, stream, pdl, ch.early(kShrink2),
+                               wait_ns));
   ML_STEP(mark(8));
   ML_STEP(launch_expand_impl(Z2, L > 0 ? B2 : nullptr, &al, p.al, H, rr, 2, O, y, y_fp32, w,
-                             stream, pdl, pdl && L > 0));
+                             stream, pdl, ch.early(kExpand2)));
   ML_STEP(mark(9));
 #undef ML_STEP
   return MOE_LORA_OK;

@@ -782,7 +782,7 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(kExpandThreads)
     combine_kernel(const float* __restrict__ O, const float* __restrict__ w,
                    const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
-                   int tokens_per_cta) {
+                   int tokens_per_cta, int nparts, size_t part_stride) {
   constexpr int KM = 8;
   __shared__ int s_row[kExpandThreads];
   __shared__ float s_w[kExpandThreads];
@@ -808,7 +808,11 @@ __global__ void __launch_bounds__(kExpandThreads)
         o[j] = 0.f;
         if (j0 + j < k) {
           const int row = s_row[q0 + j0 + j];
-          if (row >= 0) o[j] = __ldcg(O + (size_t)row * N + n);
+          if (row >= 0) {
+            o[j] = __ldcg(O + (size_t)row * N + n);
+            for (int pp = 1; pp < nparts; ++pp)  // partial outputs of a split K range
+              o[j] += __ldcg(O + pp * part_stride + (size_t)row * N + n);
+          }
         }
       }
 #pragma unroll
@@ -1050,7 +1054,8 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
 }
 
 int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
-                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl) {
+                   const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl,
+                   int nparts, size_t part_stride) {
   if (a.S == 0 || al->T == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   const int sms = num_sms();
@@ -1064,9 +1069,9 @@ int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* 
   if (tpc * al->k > kExpandThreads) return MOE_LORA_ERR_UNSUPPORTED;
   const dim3 g2(ceil_div(al->T, tpc), ncol);
   return y_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                             (const int*)v.slot_row, al->T, al->k, N, y, tpc)
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride)
                 : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                             (const int*)v.slot_row, al->T, al->k, N, y, tpc);
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride);
 }
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,

@@ -106,14 +106,18 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
                        const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
                        const int4* __restrict__ blocks, const int* __restrict__ sorted_slots, int k,
                        int K, int r, int E, float* __restrict__ Z, int ngroups, int early,
-                       const int* __restrict__ ranks, int rs, const ZPadOut zo) {
+                       const int* __restrict__ ranks, int rs, const ZPadOut zo, int prefetch) {
   constexpr int R = 8 * NT;  // ranks per CTA
   constexpr int XB = kSmallM ? 1 : U;  // kSmallM: blocks of at most 8 rows, no second row set
-  __shared__ float red[kShrinkWarps][16][R + 1];
+  constexpr int RM = kSmallM ? 8 : 16;  // rows of the reduction buffer
+  __shared__ float red[kShrinkWarps][RM][R + 1];
 
   // With `early` every input was produced two or more launches back (see
   // lora_expand.cu on launch ordering): compute first, wait only before publishing.
-  if (!early) pdl_wait();
+  // With `prefetch` only the block table is that old: the CTA reads its block and pulls
+  // its rows of A into L2 before waiting for the activations.
+  const bool tables_early = early || prefetch;
+  if (!tables_early) pdl_wait();
   // The block count and this CTA's descriptor are read together: the grid covers the
   // host's bound on the block count, so blocks + b is in bounds either way.
   const int b = blockIdx.x / ngroups;
@@ -121,8 +125,16 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
   const int nb = __ldcg(hdr + HDR_NBLOCKS);
   const int4 blk = __ldcg(blocks + b);
   if (b >= nb) {
-    if (early) pdl_wait();
+    if (tables_early) pdl_wait();
     return;
+  }
+  if (prefetch && !early) {
+    // weights never depend on a launch: this CTA's rows of A head for L2 while the
+    // predecessor drains (rank rows g R .. g R + R - 1, one bulk prefetch per row)
+    if (kVec && threadIdx.x < R && g * R + (int)threadIdx.x < r)
+      bulk_prefetch_l2(A + (((size_t)blk.w * E + blk.z) * r + g * R + threadIdx.x) * K,
+                       (uint32_t)K * 2u);
+    pdl_wait();
   }
   if (!early) pdl_trigger();
   const int row0 = blk.x, rows = blk.y, e = blk.z, l = blk.w;
@@ -206,8 +218,10 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, !kSmallM ? 1 : NT == 1 ? 5 
   for (int nt = 0; nt < NT; ++nt) {
     red[warp][gid][nt * 8 + 2 * q] = acc[nt][0];
     red[warp][gid][nt * 8 + 2 * q + 1] = acc[nt][1];
-    red[warp][gid + 8][nt * 8 + 2 * q] = acc[nt][2];
-    red[warp][gid + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+    if (!kSmallM) {  // rows 8..15 (empty with blocks of at most 8 rows)
+      red[warp][(gid + 8) % RM][nt * 8 + 2 * q] = acc[nt][2];
+      red[warp][(gid + 8) % RM][nt * 8 + 2 * q + 1] = acc[nt][3];
+    }
   }
   __syncthreads();
   if (early) {
@@ -378,7 +392,8 @@ template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
                             float* Z, bool vec, cudaStream_t stream, bool pdl, int early,
-                            bool small_m, const int* ranks, int rs, const ZPadOut& zo) {
+                            bool small_m, const int* ranks, int rs, const ZPadOut& zo,
+                            int prefetch) {
   const int ngroups = ceil_div(r, 8 * NT);
   const int64_t grid = (int64_t)max_blocks * ngroups;
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
@@ -386,7 +401,7 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
   auto args = [&](auto kern) {
     return launch_pdl(kern, g, kShrinkWarps * 32, 0, stream, pdl, X, rows_are_slots, A,
                       (const int*)v.hdr, (const int4*)v.blocks, (const int*)v.sorted_slots, k, K,
-                      r, E, Z, ngroups, early, ranks, rs, zo);
+                      r, E, Z, ngroups, early, ranks, rs, zo, prefetch);
   };
   if (small_m) {
     if (vec && K % 32 == 0) return args(lora_shrink_kernel<NT, U, true, true, true>);
@@ -401,10 +416,11 @@ static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __
 int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
                        const moe_lora_align_t* al, const AlignLayout& a, int K, int r, int rs,
                        float* Z, cudaStream_t stream, bool pdl, bool early,
-                       unsigned long long wait_ns, const ZPadOut* zpad) {
+                       unsigned long long wait_ns, const ZPadOut* zpad, int flags) {
   const int* ranks = al->adapter_ranks;
   if (a.S == 0 || al->L == 0) return MOE_LORA_OK;
   const ZPadOut zo = zpad ? *zpad : ZPadOut{};
+  const int pf = (flags & kShrinkPrefetchA) ? 1 : 0;
   AlignView v = align_view(al->buf, a);
   const auto* Xp = static_cast<const __nv_bfloat16*>(X);
   const auto* Ap = static_cast<const __nv_bfloat16*>(A);
@@ -419,9 +435,23 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   else if (r <= 16) nt = 2;
   else if (r <= 32) nt = 4;
   else nt = 8;
+  if (flags & kShrinkOneWave) {
+    // every CTA resident at once (the launch bounds' CTAs per SM), so that the next kernel
+    // of the chain launches as soon as these have passed their wait -- where some choice
+    // of ranks per CTA (at most the adapter's) allows it; else the choice above stands
+    const bool sm8 = al->bm_lora <= 8;
+    for (int c : {1, 2, 4, 8}) {
+      const int per_sm = !sm8 ? 1 : c == 1 ? 5 : c == 4 ? 2 : 1;
+      if (8 * c > ((r + 7) & ~7) * 2) break;
+      if ((int64_t)blocks_est * ceil_div(r, 8 * c) <= (int64_t)sms * per_sm) {
+        nt = c;
+        break;
+      }
+    }
+  }
   switch (nt) {
-    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
-    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
+    case 1: return launch_shrink_nt<1, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo, pf);
+    case 2: return launch_shrink_nt<2, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo, pf);
     case 4:  // short blocks: two k-steps per batch, still two CTAs per SM
       if (al->bm_lora <= 8 && vec && K <= 32 * kShrinkWarps * kShortUMax &&
           32 * short_astride(K) <= 56 * 1024) {  // short K: the slab in shared memory
@@ -452,9 +482,9 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
         return K % 32 == 0 ? go(lora_shrink_smem_kernel<4, true, false>) : go(lora_shrink_smem_kernel<4, false, false>);
       }
       if (al->bm_lora <= 8)
-        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true, ranks, rs, zo);
-      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false, ranks, rs, zo);
-    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo);
+        return launch_shrink_nt<4, 2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, true, ranks, rs, zo, pf);
+      return launch_shrink_nt<4, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, false, ranks, rs, zo, pf);
+    default: return launch_shrink_nt<8, 1>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z, vec, stream, pdl, ea, al->bm_lora <= 8, ranks, rs, zo, pf);
   }
 }
 

@@ -264,11 +264,15 @@ typedef struct moe_lora_layer_opts {
                            the up z (lora_expand_add epilogue 3). The pages describe one
                            adapter per projection and are silent on a split gate_up. */
   int32_t expand_mode;  /* 0: the library picks; 1: the expand in kernels of its own (after
-                           each grouped GEMM); 2 is treated as 0. The fused chain (the expand
-                           as extra K-steps of the grouped GEMMs, SwiGLU in the gate_up GEMM's
-                           epilogue) is used where it applies: one adapter rank (no
-                           adapter_ranks), one gate_up slice, r % 8 == 0, and shapes whose
-                           shifted z buffers stay small (they grow with E * L). */
+                           each grouped GEMM); 2: the fused chain (the expand as extra K-steps
+                           of the grouped GEMMs, SwiGLU in the gate_up GEMM's epilogue)
+                           wherever it applies: one adapter rank (no adapter_ranks), one
+                           gate_up slice, r % 8 == 0, and shapes whose shifted z buffers stay
+                           small (they grow with E * L). The library picks the fused chain
+                           where it applies and pays: with adapters, at few rows per expert or
+                           at (expert, adapter) runs of 16 rows or more on average; without,
+                           with token tiles. Both chains compute the same function; their
+                           results differ in fp32 summation order only. */
   int64_t wait_limit_ns; /* for tests of the give-up path: the wall-time limit of the grouped
                            GEMMs' main-loop mbarrier waits (and of the short-K shrink's slab
                            wait). 0: the default, 4 s; < 0: give up at the first unsuccessful
@@ -338,13 +342,20 @@ MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, 
  *                         writes the SwiGLU output directly, the down GEMM its rows, then a
  *                         combine kernel); 0: the expand in kernels of its own
  *   launches              kernels one call launches when routed from logits (one fewer with
- *                         caller-provided ids) */
+ *                         caller-provided ids)
+ *   early_reads           (kernel, earlier step) pairs where a kernel reads that step's
+ *                         output before its own griddepcontrol.wait (programmatic dependent
+ *                         launch). The plan checks each: the producer is at least two launches
+ *                         back and the launch in between triggers its dependents only after its
+ *                         own wait, so the producer has completed when the reader starts; a
+ *                         chain that broke this would be refused (MOE_LORA_ERR_UNSUPPORTED). */
 typedef struct moe_lora_layer_plan_t {
   int32_t bm_base;
   int32_t bm_lora;
   int32_t expert_major_rows;
   int32_t fused_expand;
   int32_t launches;
+  int32_t early_reads;
 } moe_lora_layer_plan_t;
 
 MOE_LORA_API int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int r,

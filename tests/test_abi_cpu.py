@@ -211,3 +211,40 @@ def test_product_path_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
+
+
+def test_chain_early_reads_come_from_completed_launches(L):
+    """Under programmatic dependent launch some kernels read before their own wait: the
+    shrinks read x or the gathered rows and the align tables, the grouped GEMMs the token
+    tiles (and, fused, the gathered rows or h), the expand kernels G or O, B and the
+    tables. The library checks each such read when it plans the chain (the producer at
+    least two launches back, the launch in between triggering only after its own wait)
+    and refuses a chain that breaks the rule; here every shape and option combination is
+    planned and the number of checked reads is pinned per chain:
+      fused, adapters: shrink1 <- align; GEMM1 <- gather, align; shrink2 <- align (its
+        block, before prefetching A); GEMM2 <- GEMM1, align = 6
+      separate expand, expert-major: shrink1 <- gather, align; expand1 <- GEMM1, align;
+        shrink2 <- expand1, align; expand2 <- GEMM2, align, route = 9
+      separate expand, token tiles: + GEMM1 <- align, GEMM2 <- align, shrink1 by token
+        (no gather) = 10
+      no adapters: the GEMMs read token tiles early only in tile mode."""
+    import itertools
+    import expert_adapter_gemms_gb300 as m
+    shapes = [(8, 2, 4, 2, 256, 512, 8), (64, 4, 32, 8, 2880, 2880, 32),
+              (4096, 4, 32, 16, 2880, 2880, 16), (512, 2, 8, 32, 4096, 11008, 64),
+              (256, 8, 128, 128, 2048, 768, 32), (300, 2, 4, 0, 256, 192, 16)]
+    for (T, k, E, Ln, H, I, r), mode, pdl, slices in itertools.product(
+            shapes, (0, 1), (True, False), (1, 2)):
+        p = m.moe_lora_layer_plan(T, k, E, Ln, H, I, r, expand_mode=mode, disable_pdl=not pdl,
+                                  gate_up_slices=slices)
+        if not pdl:
+            assert p["early_reads"] == 0
+            continue
+        if Ln == 0:
+            assert p["early_reads"] == (0 if p["fused_expand"] or p["expert_major_rows"] else 2)
+        elif p["fused_expand"]:
+            assert p["early_reads"] == 6, (T, mode, p)
+        elif p["expert_major_rows"]:
+            assert p["early_reads"] == 9, (T, mode, p)
+        else:
+            assert p["early_reads"] == 10, (T, mode, p)

@@ -1,4 +1,6 @@
 """The whole fused MoE-LoRA layer on the GPU against the fp64 oracle."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -34,19 +36,95 @@ def oracle_layer(inp, tokens=None, adapters=True, token_adapter=None):
     return oracle.moe_lora_layer(inp.x[sel], inp.W1, inp.W2, ids[sel], w[sel], ta[sel], *lora)
 
 
-@pytest.mark.parametrize("name", WORKLOAD_NAMES)
-def test_layer_workloads(name):
-    """All five workloads; the oracle runs on every token of the small ones and on a
-    sample of 48 tokens of the large ones (tokens are independent of each other)."""
+_GPU_Y = {}
+_REF_Y = {}
+
+
+@functools.lru_cache(maxsize=1)
+def _inputs(name):
+    """A workload's inputs, drawn once for the consecutive tests that use them."""
+    return make_workload_inputs(name)
+
+
+def _workload_y(m, name, expand_mode):
+    """The layer's y (bf16) on a workload, computed once per (workload, chain)."""
+    key = (name, expand_mode)
+    if key not in _GPU_Y:
+        inp = _inputs(name)
+        plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r,
+                                     expand_mode=expand_mode)
+        if expand_mode == 1:
+            assert plan["fused_expand"] == 0
+        _GPU_Y[key] = (run_layer(m, inp, expand_mode=expand_mode).cpu(), plan)
+        torch.cuda.empty_cache()
+    return _GPU_Y[key]
+
+
+@pytest.mark.parametrize("expand_mode", [0, 1])
+@pytest.mark.parametrize("name,chunk", [(n, c) for n in WORKLOAD_NAMES for c in
+                                        (range(4) if n == "gptoss20b_prefill" else range(1))])
+def test_layer_workloads(name, chunk, expand_mode):
+    """All five workloads through the chain the library picks (expand fused into the grouped
+    GEMMs where it applies) and through the chain with separate expand kernels, compared
+    with the oracle on every token (the prefill workload's 4096 tokens in four chunks)."""
     m = need_gpu()
-    inp = make_workload_inputs(name)
-    y = run_layer(m, inp).cpu()
-    if inp.T <= 256:
-        tokens = np.arange(inp.T)
-    else:
-        tokens = np.sort(np.random.default_rng(WORKLOAD_NAMES.index(name)).choice(inp.T, size=48, replace=False))
+    inp = _inputs(name)
+    y, plan = _workload_y(m, name, expand_mode)
+    n_chunks = 4 if name == "gptoss20b_prefill" else 1
+    per = (inp.T + n_chunks - 1) // n_chunks
+    tokens = np.arange(chunk * per, min(inp.T, (chunk + 1) * per))
+    key = (name, chunk)
+    if key not in _REF_Y:
+        _REF_Y[key] = oracle_layer(inp, tokens)
+    assert_close(y[tokens], _REF_Y[key], LAYER_RTOL, f"{name} chunk {chunk} plan {plan}")
+
+
+def test_fused_chain_is_picked_where_it_applies():
+    """The plan fuses the expand into the grouped GEMMs for the decode and prefill workloads
+    (few rows per expert, or long (expert, adapter) runs), not for the 4096/11008 example
+    (runs of about four rows: each run's adapter stages multiply a whole token tile) nor for
+    separate gate and up adapters or per-adapter ranks, and never when asked for the
+    separate kernels."""
+    m = need_gpu()
+    c = make_workload_inputs("paper_example_4096_11008")
+    assert m.moe_lora_layer_plan(c.T, c.k, c.E, c.L, c.H, c.I, c.r)["fused_expand"] == 0
+    for name in ("tiny", "gptoss20b_decode", "gptoss20b_prefill"):
+        c = make_workload_inputs(name)
+        args = (c.T, c.k, c.E, c.L, c.H, c.I, c.r)
+        assert m.moe_lora_layer_plan(*args)["fused_expand"] == 1, name
+        assert m.moe_lora_layer_plan(*args, expand_mode=1)["fused_expand"] == 0, name
+        assert m.moe_lora_layer_plan(*args, gate_up_slices=2)["fused_expand"] == 0, name
+        assert m.moe_lora_layer_plan(*args, adapter_ranks=True)["fused_expand"] == 0, name
+
+
+@pytest.mark.parametrize("shape", ["r8_expert_major", "r24_expert_major", "r64_chunked",
+                                   "r128_chunked", "tiles_many_runs", "persistent_r32",
+                                   "base_only_tiles"])
+def test_fused_expand_shapes(shape):
+    """The fused chain on shapes that exercise its cases: ranks that need zero padding to a
+    multiple of 16 (8, 24), ranks whose high and low z parts take separate 64-column chunks
+    (64, 128), expert-major chunks, token tiles holding many adapter runs (one adapter per
+    request of 64 tokens), persistent 128-row tiles, and no adapters at all. Every token is
+    compared with the oracle and with the chain of separate expand kernels."""
+    m = need_gpu()
+    kw = {"r8_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=8),
+          "r24_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=24),
+          "r64_chunked": dict(T=60, H=256, I=192, E=5, k=2, L=4, r=64),
+          "r128_chunked": dict(T=48, H=256, I=128, E=4, k=2, L=2, r=128),
+          "tiles_many_runs": dict(T=1024, H=256, I=256, E=8, k=2, L=16, r=16,
+                                  adapters="one_per_request16"),
+          "persistent_r32": dict(T=700, H=128, I=256, E=4, k=2, L=3, r=32),
+          "base_only_tiles": dict(T=300, H=256, I=192, E=4, k=2, L=0, r=16)}[shape]
+    inp = make_layer_inputs(seed=120 + len(shape), lora_std=None, **kw)
+    plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    assert plan["fused_expand"] == 1, plan
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    y_sep = run_layer(m, inp, y_fp32=True, expand_mode=1).cpu()
+    tokens = np.arange(inp.T) if inp.T <= 300 else np.arange(0, inp.T, 3)
     ref = oracle_layer(inp, tokens)
-    assert_close(y[tokens], ref, LAYER_RTOL, name)
+    assert_close(y[tokens], ref, LAYER_RTOL, f"fused {shape} {plan}")
+    # the two chains differ only in fp32 summation order and where z is rounded
+    assert_close(y, f64(y_sep), 1e-3, f"fused vs separate expand, {shape}")
 
 
 def test_layer_error_word_clean_on_workload():
@@ -85,15 +163,18 @@ def test_layer_lora_delta_matches_oracle():
     assert np.abs(d_gpu - d_ref).max() <= 0.1 * np.abs(d_ref).max()
 
 
-def test_layer_base_reductions_bitwise():
-    """Adapter -1 everywhere, or B = 0, give exactly the base-only output."""
+@pytest.mark.parametrize("expand_mode", [1, 2])
+def test_layer_base_reductions_bitwise(expand_mode):
+    """Adapter -1 everywhere, or B = 0, give exactly the base-only output of the same chain
+    (the separate expand kernels, or the expand fused into the grouped GEMMs)."""
     m = need_gpu()
     inp = make_workload_inputs("tiny")
-    y_base = run_layer(m, inp, y_fp32=True, adapters=False)
+    kw = dict(y_fp32=True, expand_mode=expand_mode)
+    y_base = run_layer(m, inp, adapters=False, **kw)
     none = torch.full((inp.T,), -1, dtype=torch.int32)
-    y_none = run_layer(m, inp, y_fp32=True, token_adapter=none)
+    y_none = run_layer(m, inp, token_adapter=none, **kw)
     assert torch.equal(y_none, y_base)
-    y_zero = run_layer(m, inp, y_fp32=True, B_zero=True)
+    y_zero = run_layer(m, inp, B_zero=True, **kw)
     assert torch.equal(y_zero, y_base)
 
 
@@ -329,7 +410,7 @@ def test_layer_host_staged(name, with_adapter, y_fp32):
     y_dev = m.moe_lora_layer(dev(inp.x), W1, W2, logits=dev(inp.logits), k=inp.k,
                              token_adapter=ta, y_fp32=y_fp32, **lora).cpu()
     assert torch.equal(y_host, y_dev)
-    tokens = np.arange(inp.T) if inp.T <= 16 else np.arange(0, inp.T, 4)
+    tokens = np.arange(inp.T)
     no_adapter = np.full(inp.T, -1, dtype=np.int32)
     ref = oracle_layer(inp, tokens, token_adapter=None if with_adapter else no_adapter)
     assert_close(y_host[tokens], ref, LAYER_RTOL, f"host-staged {name}")
