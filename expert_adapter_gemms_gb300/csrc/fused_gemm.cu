@@ -82,7 +82,6 @@ struct FusedArgs {
   size_t part_stride;  // elements between the partial outputs
   int E, L, gap;    // z of sorted row j of pair (e, l) sits at row j + (e L + l + 1) gap
   int lora;         // 0: no adapter term (B and z maps unused)
-  int lora_at;      // the adapter stages of a job follow its first lora_at base stages
   int zchunks;      // LoRA stages per run of an adapter in a tile
   int zk;           // > 0: one stage, z row = [high (zk K16 steps) | low (zk)]; 0: chunked
   int rp16;         // rank rounded up to a multiple of 16
@@ -348,48 +347,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       job(j, e, wb, r0, rows);
       AdapterRows<(BN + 31) / 32> ar;
       if (lora) ar.load(p.row_adapter, r0, rows);
-      // the adapter stages go after the first lora_at base stages (each accumulator is
-      // cleared by the job's first base stage), so their B loads overlap the base stream
-      auto adapter_stages = [&]() {
-        if (!lora || warp_aborted(s_abort)) return;
-        if (!waited0) {  // z comes from the predecessor
-          if (lane == 0) {
-            pdl_wait();
-            pdl_trigger();
-          }
-          waited0 = true;
-        }
-        ar.for_each_run([&](int l, int, int) {
-          for (int c = 0; c < p.zchunks; ++c, ++g) {
-            if (warp_aborted(s_abort)) return;
-            const int s = g % STAGES;
-            const uint32_t ph = (g / STAGES) & 1;
-            if (lane == 0) {
-              uint8_t* sw = smem + s * C::kStageBytes;
-              if (mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns)) {
-                const int bcol = 64 * (c % cph);
-                const int pair = l * p.E + e;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(kFBM * b_row));
-                tma_load_3d(sw, &tm_b, &full[s], bcol, wb * kWR, pair, pol_w);
-                if (kGLU)
-                  tma_load_3d(sw + kWR * b_row, &tm_b, &full[s], bcol, p.up_off + wb * kWR, pair,
-                              pol_w);
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * z_row));
-                tma_load_2d(sw + C::kWBytes, &tm_z, &full[s], 64 * c,
-                            r0 + (e * p.L + l + 1) * p.gap, pol_a);
-                ++issued;
-              } else {
-                *s_abort = 1;
-              }
-            }
-            __syncwarp();
-          }
-        });
-      };
-      // (in the first job not before its stages whose weights were prefetched: those hold
-      // ring slots 0 .. pre - 1)
-      const int lora_at = min(max(j == 0 ? max(p.lora_at, pre) : p.lora_at, 1), nk);
-      for (int kb = 0; kb < nk; ++kb, ++g) {
+      // Every stage, base or adapter, takes the next ring index g: the job's K/64 base
+      // stages, then its adapter stages (the accumulator was cleared by the first base
+      // stage; placed last, they also give the predecessor that writes z the most time).
+      for (int kb = 0; kb < nk; ++kb) {
         const int s = g % STAGES;
         const uint32_t ph = (g / STAGES) & 1;
         if (lane == 0) {
@@ -410,10 +371,45 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             *s_abort = 1;
           }
         }
+        ++g;
         __syncwarp();
         if (warp_aborted(s_abort)) break;
-        if (kb + 1 == lora_at) adapter_stages();
       }
+      if (!lora || warp_aborted(s_abort)) continue;
+      if (!waited0) {  // z comes from the predecessor
+        if (lane == 0) {
+          pdl_wait();
+          pdl_trigger();
+        }
+        waited0 = true;
+      }
+      ar.for_each_run([&](int l, int, int) {
+        for (int c = 0; c < p.zchunks; ++c) {
+          if (warp_aborted(s_abort)) return;
+          const int s = g % STAGES;
+          const uint32_t ph = (g / STAGES) & 1;
+          if (lane == 0) {
+            uint8_t* sw = smem + s * C::kStageBytes;
+            if (mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns)) {
+              const int bcol = 64 * (c % cph);
+              const int pair = l * p.E + e;
+              mbar_arrive_expect_tx(&full[s], (uint32_t)(kFBM * b_row));
+              tma_load_3d(sw, &tm_b, &full[s], bcol, wb * kWR, pair, pol_w);
+              if (kGLU)
+                tma_load_3d(sw + kWR * b_row, &tm_b, &full[s], bcol, p.up_off + wb * kWR, pair,
+                            pol_w);
+              mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * z_row));
+              tma_load_2d(sw + C::kWBytes, &tm_z, &full[s], 64 * c,
+                          r0 + (e * p.L + l + 1) * p.gap, pol_a);
+              ++issued;
+            } else {
+              *s_abort = 1;
+            }
+          }
+          ++g;
+          __syncwarp();
+        }
+      });
     }
   } else if (warp == 1) {
     // MMA issuer (lane 0); the warp walks the same jobs and adapter runs as the producer
@@ -432,13 +428,33 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
       __syncwarp();
       if (warp_aborted(s_abort)) break;
-      auto adapter_stages = [&]() {
-        if (!lora || warp_aborted(s_abort)) return;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = g % STAGES;
+        const uint32_t ph = (g / STAGES) & 1;
+        if (lane == 0) {
+          if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
+            *s_abort = 1;
+          } else {
+            tc_fence_after();
+            const uint8_t* sw = smem + s * C::kStageBytes;
+            const uint64_t dw = smem_desc_sw128(smem_u32(sw));
+            const uint64_t da = smem_desc_sw128(smem_u32(sw + C::kWBytes));
+#pragma unroll
+            for (int kk = 0; kk < kFBK / 16; ++kk)
+              tc_mma_bf16(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
+            tc_commit(&empty[s]);
+          }
+        }
+        ++g;
+        __syncwarp();
+        if (warp_aborted(s_abort)) break;
+      }
+      if (lora && !warp_aborted(s_abort)) {
         ar.for_each_run([&](int, int, int end) {
           // the run's z rows are zero past its last row: the MMAs stop there (N = the run's
           // end rounded up to 16), the accumulator columns beyond are left as they are
           const uint32_t idr = idesc_bf16_f32(kFBM, static_cast<uint32_t>((end + 15) & ~15));
-          for (int c = 0; c < p.zchunks; ++c, ++g) {
+          for (int c = 0; c < p.zchunks; ++c) {
             if (warp_aborted(s_abort)) return;
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1;
@@ -463,33 +479,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 tc_commit(&empty[s]);
               }
             }
+            ++g;
             __syncwarp();
           }
         });
-      };
-      // (in the first job not before its stages whose weights were prefetched: those hold
-      // ring slots 0 .. pre - 1)
-      const int lora_at = min(max(j == 0 ? max(p.lora_at, pre) : p.lora_at, 1), nk);
-      for (int kb = 0; kb < nk; ++kb, ++g) {
-        const int s = g % STAGES;
-        const uint32_t ph = (g / STAGES) & 1;
-        if (lane == 0) {
-          if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
-            *s_abort = 1;
-          } else {
-            tc_fence_after();
-            const uint8_t* sw = smem + s * C::kStageBytes;
-            const uint64_t dw = smem_desc_sw128(smem_u32(sw));
-            const uint64_t da = smem_desc_sw128(smem_u32(sw + C::kWBytes));
-#pragma unroll
-            for (int kk = 0; kk < kFBK / 16; ++kk)
-              tc_mma_bf16(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
-            tc_commit(&empty[s]);
-          }
-        }
-        __syncwarp();
-        if (warp_aborted(s_abort)) break;
-        if (kb + 1 == lora_at) adapter_stages();
       }
       if (warp_aborted(s_abort)) break;
       if (lane == 0) tc_commit(&tmem_full[a]);  // fires when every MMA issued above completes
@@ -720,7 +713,6 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
   // the gate_up form's z is ready as the GEMM starts (its shrink computed before waiting):
   // the adapter stages follow the first base stage; the down form's shrink starts when
   // the gate_up GEMM ends: the stages wait until half the K range has streamed
-  args.lora_at = glu ? 1 : std::max(1, ceil_div(K, kFBK) / (2 * ksplit));
   args.zchunks = lora ? zl.zchunks : 0;
   args.zk = zl.zk;
   args.rp16 = zl.rp16;
