@@ -47,7 +47,7 @@ class LayerOpts(ctypes.Structure):
                 ("disable_pdl", ctypes.c_int32), ("num_events", ctypes.c_int32),
                 ("events", ctypes.POINTER(ctypes.c_void_p)), ("adapter_ranks", ctypes.c_void_p),
                 ("gate_up_slices", ctypes.c_int32), ("expand_mode", ctypes.c_int32),
-                ("wait_limit_ns", ctypes.c_int64)]
+                ("wait_limit_ns", ctypes.c_int64), ("mma_pairs", ctypes.c_int32)]
 
 
 class LayerPlan(ctypes.Structure):

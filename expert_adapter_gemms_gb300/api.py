@@ -287,13 +287,14 @@ def _layer_weights(H: int, W1, W2, A1, B1, A2, B2, gate_up_slices: int):
 
 def _layer_opts(Ln: int, bm_base: int, bm_lora: int, disable_pdl: bool, events,
                 gate_up_slices: int, adapter_ranks, wait_limit_ns: int = 0,
-                expand_mode: int = 0):
+                expand_mode: int = 0, mma_pairs: int = 0):
     """The layer options struct, and the event array it points to (keep it alive)."""
     opts = LayerOpts()
     opts.bm_base, opts.bm_lora, opts.disable_pdl = bm_base, bm_lora, int(disable_pdl)
     opts.gate_up_slices = gate_up_slices
     opts.wait_limit_ns = int(wait_limit_ns)
     opts.expand_mode = int(expand_mode)
+    opts.mma_pairs = int(mma_pairs)
     if adapter_ranks is not None:
         _need(adapter_ranks, "adapter_ranks", torch.int32, 1, (Ln,))
         opts.adapter_ranks = ptr(adapter_ranks)
@@ -314,13 +315,15 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
                    bm_base: int = 0, bm_lora: int = 0, disable_pdl: bool = False,
                    events: Optional[Sequence] = None, gate_up_slices: int = 1,
                    adapter_ranks: Optional[torch.Tensor] = None,
-                   wait_limit_ns: int = 0, expand_mode: int = 0) -> torch.Tensor:
+                   wait_limit_ns: int = 0, expand_mode: int = 0,
+                   mma_pairs: int = 0) -> torch.Tensor:
     """The whole fused MoE-LoRA layer; returns y [T, H]. gate_up_slices=2: separate gate
     and up adapters, A1 [L, E, 2r, H] (gate A rows first), B1 [L, E, 2I, r].
     adapter_ranks [L] int32 (device): adapter l has rank r_l <= r (weights padded to r).
     wait_limit_ns (tests of the give-up path): 0 default 4 s, < 0 give up at once.
     expand_mode: 0 the library picks, 1 the expand in kernels of its own, 2 the expand fused
-    into the grouped GEMMs wherever it applies."""
+    into the grouped GEMMs wherever it applies. mma_pairs: 0 the library picks (CTA pairs
+    for the fused chain's 256-row token tiles), -1 one CTA per MMA."""
     _need(x, "x", torch.bfloat16, 2)
     T, H = x.shape
     E, I, Ln, r = _layer_weights(H, W1, W2, A1, B1, A2, B2, gate_up_slices)
@@ -341,7 +344,7 @@ def moe_lora_layer(x: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, *,
     if workspace is None:
         workspace = new_workspace(T, k, E, Ln, H, I, r, x.device)
     opts, _ev = _layer_opts(Ln, bm_base, bm_lora, disable_pdl, events, gate_up_slices,
-                            adapter_ranks, wait_limit_ns, expand_mode)
+                            adapter_ranks, wait_limit_ns, expand_mode, mma_pairs)
     check(lib().moe_lora_layer_ex(
         ptr(x), ptr(logits), ptr(topk_ids), ptr(topk_w), ptr(token_adapter), T, H, I, E, k,
         ptr(W1), ptr(W2), ptr(A1), ptr(B1), ptr(A2), ptr(B2), Ln, r, ptr(y), int(y_fp32),

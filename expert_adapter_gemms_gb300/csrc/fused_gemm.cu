@@ -50,10 +50,13 @@ constexpr int kFGroupTiles = 8;
 constexpr int kXStride = 17;  // floats per row of the gate/up exchange tile (conflict-free)
 enum { kFModeTile = 0, kFModeExpert = 1, kFModePersistent = 2 };
 
-template <int BN, int STAGES, bool kGLU>
+// kPair: a cluster of two CTAs computes each job as one M = 256 tcgen05.mma.cta_group::2
+// (CTA c: weight block 2 wbp + c, and half of the tile's token rows).
+template <int BN, int STAGES, bool kGLU, bool kPair = false>
 struct FusedCfg {
+  static constexpr int kRowsPerCta = kPair ? BN / 2 : BN;  // token rows a CTA stages
   static constexpr int kWBytes = kFBM * kFBK * 2;
-  static constexpr int kABytes = BN * kFBK * 2;
+  static constexpr int kABytes = kRowsPerCta * kFBK * 2;
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kXOff = kBarOff + 256;  // gate/up exchange tile [128][kXStride] fp32
@@ -65,6 +68,7 @@ struct FusedCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kABytes % 1024 == 0, "stage alignment");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(!kPair || BN == 256, "CTA pairs take 256-row token tiles");
 };
 
 struct FusedArgs {
@@ -165,13 +169,13 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int BN, int STAGES, bool kGLU>
+template <int BN, int STAGES, bool kGLU, bool kPair>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_a,
                       const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_z, const FusedArgs p) {
-  using C = FusedCfg<BN, STAGES, kGLU>;
+  using C = FusedCfg<BN, STAGES, kGLU, kPair>;
   // weight rows per output block: 64 gate + 64 up rows (kGLU) or 128 rows
   constexpr int kWR = kGLU ? kFBM / 2 : kFBM;
   extern __shared__ uint8_t smem_raw[];
@@ -190,7 +194,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool expert_major = p.mode == kFModeExpert;
   const bool persistent = p.mode == kFModePersistent;
-  const int n_wblocks = p.n_wblocks;
+  // A CTA pair (persistent mode only) walks its jobs as one unit: CTA c takes weight block
+  // 2 wbp + c of job wbp, the leader (c = 0) issues the MMAs of both.
+  const uint32_t crank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int unit = kPair ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int nunits = kPair ? (int)gridDim.x / 2 : (int)gridDim.x;
+  const int n_wblocks = kPair ? (p.n_wblocks + 1) / 2 : p.n_wblocks;  // weight jobs per tile
   // (token tile, weight block) jobs in groups of kFGroupTiles tiles, so that CTAs sharing
   // a weight block run together
   auto tile_job = [&](int w, int n_tiles, int& e, int& wb, int& r0, int& rows) {
@@ -200,6 +210,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int gsz = min(kFGroupTiles, n_tiles - first);
     const int within = w - grp * per_group;
     wb = within / gsz;
+    if (kPair) wb = 2 * wb + (int)crank;
     const int4 tile = __ldcg(p.tiles + first + within % gsz);
     e = tile.x;
     r0 = tile.y;
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tmem_empty[a], kPair ? 8 : 4);  // one arrival per epilogue warp (of both)
     }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -229,7 +240,35 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       tma_prefetch_desc(&tm_z);
     }
   }
-  __syncthreads();
+  // the pair: each CTA's barriers are initialised before the other arrives on them
+  if constexpr (kPair) cluster_sync();
+  else __syncthreads();
+
+  // Pair-aware pieces. Copies complete on the leader's full barrier (which the leader arms
+  // for the bytes of both CTAs); waits acquire at cluster scope; an abort is mirrored into
+  // the other CTA of the pair.
+  auto full_bar = [&](int s) -> uint32_t {
+    return kPair ? smem_in_cta(&full[s], 0) : smem_u32(&full[s]);
+  };
+  auto copy2d = [&](void* dst, const CUtensorMap* m, int s, int c0, int c1, uint64_t pol) {
+    if constexpr (kPair) tma_load_2d_pair(dst, m, full_bar(s), c0, c1, pol);
+    else tma_load_2d(dst, m, &full[s], c0, c1, pol);
+  };
+  auto copy3d = [&](void* dst, const CUtensorMap* m, int s, int c0, int c1, int c2, uint64_t pol) {
+    if constexpr (kPair) tma_load_3d_pair(dst, m, full_bar(s), c0, c1, c2, pol);
+    else tma_load_3d(dst, m, &full[s], c0, c1, c2, pol);
+  };
+  auto arm = [&](int s, uint32_t bytes_per_cta) {  // the leader arms for the whole pair
+    if (leader) mbar_arrive_expect_tx(&full[s], kPair ? 2 * bytes_per_cta : bytes_per_cta);
+  };
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if constexpr (kPair) return mbar_wait_cluster(bar, parity, p.wait_ns);
+    else return mbar_wait_bounded(bar, parity, p.wait_ns);
+  };
+  auto set_abort = [&]() {
+    *s_abort = 1;
+    if constexpr (kPair) st_cluster_u32(smem_in_cta((const void*)s_abort, crank ^ 1u), 1u);
+  };
 
   // With `early`, everything but z was produced two or more launches back (the
   // predecessor, a shrink, triggers its dependents only after its own wait), so only
@@ -248,8 +287,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     n_tiles = __ldcg(p.hdr + HDR_NTILES);
     const int total = n_tiles * n_wblocks;
     if (persistent) {
-      njobs = blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-      if (njobs > 0) tile_job(blockIdx.x, n_tiles, e0, wb0, r00, rows0);
+      njobs = unit < total ? (total - 1 - unit) / nunits + 1 : 0;
+      if (njobs > 0) tile_job(unit, n_tiles, e0, wb0, r00, rows0);
     } else {
       const int lin = blockIdx.x;
       const int per_group = kFGroupTiles * n_wblocks;
@@ -282,21 +321,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int pre = nk < STAGES ? nk : STAGES;
 
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {  // one warp of each CTA of the pair
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
-  // Weight block wb of expert e into a stage: rows [wb kWR, +kWR) of the gate half and,
+  // Weight block wb of expert e into stage s: rows [wb kWR, +kWR) of the gate half and,
   // kGLU, of the up half (at up_off) below them -- one 128-row operand.
-  auto load_w = [&](uint8_t* sw, uint64_t* bar, int kb, int wb, int e, uint64_t pol) {
-    tma_load_3d(sw, &tm_w, bar, (kb0 + kb) * kFBK, wb * kWR, e, pol);
-    if (kGLU) tma_load_3d(sw + kWR * 128, &tm_w, bar, (kb0 + kb) * kFBK, p.up_off + wb * kWR, e, pol);
+  auto load_w = [&](uint8_t* sw, int s, int kb, int wb, int e, uint64_t pol) {
+    copy3d(sw, &tm_w, s, (kb0 + kb) * kFBK, wb * kWR, e, pol);
+    if (kGLU) copy3d(sw + kWR * 128, &tm_w, s, (kb0 + kb) * kFBK, p.up_off + wb * kWR, e, pol);
   };
   // the first ring of weight stages of the first job (a weight never depends on a launch)
   if (threadIdx.x == 0) {
     const uint64_t pol_w = l2_policy_evict_first();
     for (int kb = 0; kb < pre; ++kb) {
-      mbar_arrive_expect_tx(&full[kb], C::kWBytes);
-      load_w(smem + kb * C::kStageBytes, &full[kb], kb, wb0, e0, pol_w);
+      arm(kb, C::kWBytes);
+      load_w(smem + kb * C::kStageBytes, kb, kb, wb0, e0, pol_w);
     }
   }
   if (!p.early && expert_major) pdl_wait();  // every thread, after the weights went out
@@ -321,11 +365,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       r0 = s_job[0] + j * BN;
       rows = min(BN, s_job[1] - j * BN);
     } else if (persistent && j > 0) {
-      tile_job(blockIdx.x + j * gridDim.x, n_tiles, e, wb, r0, rows);
+      tile_job(unit + j * nunits, n_tiles, e, wb, r0, rows);
     } else {
       e = e0; wb = wb0; r0 = r00; rows = rows0;
     }
   };
+  // A pair splits a job's token rows at half its MMA width nj (rows rounded up to 32):
+  // CTA c stages rows [c nj / 2, c nj / 2 + 128) of the tile, and the MMA reads nj / 2 of
+  // them from each CTA. One CTA: the MMA width follows the rows (16-row steps).
+  auto job_n = [&](int rows) -> int { return kPair ? (rows + 31) & ~31 : (rows + 15) & ~15; };
+  auto row_off = [&](int rows) -> int { return kPair ? (int)crank * (job_n(rows) / 2) : 0; };
   const int cph = p.zk ? 1 : p.zchunks / 2;  // chunked layout: stages per half (high, low)
   // bytes of one B row and of one z row in shared memory (their boxes' widths)
   const int b_row = p.b_cols * 2, z_row = p.z_cols * 2;
@@ -341,7 +390,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (njobs == 0 && lane == 0) {  // expert-major with no row: complete the prefetched stages
       for (int kb = 0; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
       for (int kb = 0; kb < pre; ++kb) mbar_wait_bounded(&full[kb], 0);
-    }
+    }  // (a pair always has jobs: persistent CTAs without one have left)
     for (int j = 0; j < njobs && !warp_aborted(s_abort); ++j) {
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
@@ -357,18 +406,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           uint8_t* sw = smem + s * C::kStageBytes;
           bool ok = !*s_abort;
           if (ok && g >= pre) {
-            ok = mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns);
+            ok = wait_bar(&empty[s], ph ^ 1);
             if (ok) {
-              mbar_arrive_expect_tx(&full[s], C::kWBytes);
-              load_w(sw, &full[s], kb, wb, e, pol_w);
+              arm(s, C::kWBytes);
+              load_w(sw, s, kb, wb, e, pol_w);
             }
           }
           if (ok) {
-            mbar_arrive_expect_tx(&full[s], C::kABytes);
-            tma_load_2d(sw + C::kWBytes, &tm_a, &full[s], (kb0 + kb) * kFBK, r0, pol_a);
+            arm(s, C::kABytes);
+            copy2d(sw + C::kWBytes, &tm_a, s, (kb0 + kb) * kFBK, r0 + row_off(rows), pol_a);
             ++issued;
           } else {
-            *s_abort = 1;
+            set_abort();
           }
         }
         ++g;
@@ -390,20 +439,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const uint32_t ph = (g / STAGES) & 1;
           if (lane == 0) {
             uint8_t* sw = smem + s * C::kStageBytes;
-            if (mbar_wait_bounded(&empty[s], ph ^ 1, p.wait_ns)) {
+            if (wait_bar(&empty[s], ph ^ 1)) {
               const int bcol = 64 * (c % cph);
               const int pair = l * p.E + e;
-              mbar_arrive_expect_tx(&full[s], (uint32_t)(kFBM * b_row));
-              tma_load_3d(sw, &tm_b, &full[s], bcol, wb * kWR, pair, pol_w);
-              if (kGLU)
-                tma_load_3d(sw + kWR * b_row, &tm_b, &full[s], bcol, p.up_off + wb * kWR, pair,
-                            pol_w);
-              mbar_arrive_expect_tx(&full[s], (uint32_t)(BN * z_row));
-              tma_load_2d(sw + C::kWBytes, &tm_z, &full[s], 64 * c,
-                          r0 + (e * p.L + l + 1) * p.gap, pol_a);
+              arm(s, (uint32_t)(kFBM * b_row));
+              copy3d(sw, &tm_b, s, bcol, wb * kWR, pair, pol_w);
+              if (kGLU) copy3d(sw + kWR * b_row, &tm_b, s, bcol, p.up_off + wb * kWR, pair, pol_w);
+              arm(s, (uint32_t)(C::kRowsPerCta * z_row));
+              copy2d(sw + C::kWBytes, &tm_z, s, 64 * c,
+                     r0 + row_off(rows) + (e * p.L + l + 1) * p.gap, pol_a);
               ++issued;
             } else {
-              *s_abort = 1;
+              set_abort();
             }
           }
           ++g;
@@ -411,19 +458,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
       });
     }
-  } else if (warp == 1) {
-    // MMA issuer (lane 0); the warp walks the same jobs and adapter runs as the producer
+  } else if (warp == 1 && leader) {
+    // MMA issuer (lane 0); the warp walks the same jobs and adapter runs as the producer.
+    // A pair's MMAs (M = 256 over both CTAs) and commits (to the barriers of both) are
+    // issued by the leader alone.
+    constexpr uint32_t kM = kPair ? 2 * kFBM : kFBM;
+    auto mma = [&](uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc_in) {
+      if constexpr (kPair) tc_mma_bf16_pair(d, a_desc, b_desc, idesc, acc_in);
+      else tc_mma_bf16(d, a_desc, b_desc, idesc, acc_in);
+    };
+    auto commit = [&](uint64_t* bar) {
+      if constexpr (kPair) tc_commit_pair_mc(bar);
+      else tc_commit(bar);
+    };
     int g = 0;
     for (int j = 0; j < njobs && !warp_aborted(s_abort); ++j) {
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
       const int a = j & 1;
       const uint32_t acc = tmem + static_cast<uint32_t>(a * C::kAccCols);
-      const uint32_t idesc = idesc_bf16_f32(kFBM, static_cast<uint32_t>((rows + 15) & ~15));
+      const uint32_t idesc = idesc_bf16_f32(kM, static_cast<uint32_t>(job_n(rows)));
       AdapterRows<(BN + 31) / 32> ar;
       if (lora) ar.load(p.row_adapter, r0, rows);
       if (lane == 0 && j >= 2) {  // the epilogue must have read this accumulator's last job
-        if (!mbar_wait_bounded(&tmem_empty[a], ((j >> 1) - 1) & 1, p.wait_ns)) *s_abort = 1;
+        if (!wait_bar(&tmem_empty[a], ((j >> 1) - 1) & 1)) set_abort();
         tc_fence_after();
       }
       __syncwarp();
@@ -432,8 +490,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const int s = g % STAGES;
         const uint32_t ph = (g / STAGES) & 1;
         if (lane == 0) {
-          if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
-            *s_abort = 1;
+          if (!wait_bar(&full[s], ph)) {
+            set_abort();
           } else {
             tc_fence_after();
             const uint8_t* sw = smem + s * C::kStageBytes;
@@ -441,8 +499,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint64_t da = smem_desc_sw128(smem_u32(sw + C::kWBytes));
 #pragma unroll
             for (int kk = 0; kk < kFBK / 16; ++kk)
-              tc_mma_bf16(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
-            tc_commit(&empty[s]);
+              mma(acc, dw + 2 * kk, da + 2 * kk, idesc, (kb | kk) != 0);
+            commit(&empty[s]);
           }
         }
         ++g;
@@ -452,15 +510,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       if (lora && !warp_aborted(s_abort)) {
         ar.for_each_run([&](int, int, int end) {
           // the run's z rows are zero past its last row: the MMAs stop there (N = the run's
-          // end rounded up to 16), the accumulator columns beyond are left as they are
-          const uint32_t idr = idesc_bf16_f32(kFBM, static_cast<uint32_t>((end + 15) & ~15));
+          // end rounded up to 16), the accumulator columns beyond are left as they are (a
+          // pair keeps the job's width: its split of the rows between the CTAs follows it)
+          const uint32_t idr =
+              idesc_bf16_f32(kM, static_cast<uint32_t>(kPair ? job_n(rows) : (end + 15) & ~15));
           for (int c = 0; c < p.zchunks; ++c) {
             if (warp_aborted(s_abort)) return;
             const int s = g % STAGES;
             const uint32_t ph = (g / STAGES) & 1;
             if (lane == 0) {
-              if (!mbar_wait_bounded(&full[s], ph, p.wait_ns)) {
-                *s_abort = 1;
+              if (!wait_bar(&full[s], ph)) {
+                set_abort();
               } else {
                 tc_fence_after();
                 const uint8_t* sw = smem + s * C::kStageBytes;
@@ -468,15 +528,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 const uint64_t dz = smem_desc_swz(smem_u32(sw + C::kWBytes), p.z_layout, p.z_sbo);
                 if (p.zk) {  // [high | low] in one row: both against the same B steps
                   for (int kk = 0; kk < p.zk; ++kk) {
-                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
-                    tc_mma_bf16(acc, db + 2 * kk, dz + 2 * (p.zk + kk), idr, 1);
+                    mma(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
+                    mma(acc, db + 2 * kk, dz + 2 * (p.zk + kk), idr, 1);
                   }
                 } else {  // chunk c of the high or the low half
                   const int rem = (p.rp16 - 64 * (c % cph)) / 16;
                   const int nm = rem < 4 ? rem : 4;
-                  for (int kk = 0; kk < nm; ++kk) tc_mma_bf16(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
+                  for (int kk = 0; kk < nm; ++kk) mma(acc, db + 2 * kk, dz + 2 * kk, idr, 1);
                 }
-                tc_commit(&empty[s]);
+                commit(&empty[s]);
               }
             }
             ++g;
@@ -485,10 +545,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         });
       }
       if (warp_aborted(s_abort)) break;
-      if (lane == 0) tc_commit(&tmem_full[a]);  // fires when every MMA issued above completes
+      if (lane == 0) commit(&tmem_full[a]);  // fires when every MMA issued above completes
       __syncwarp();
     }
-  } else {
+  } else if (warp >= 2) {
     // epilogue: warp w reads TMEM lanes [32 (w % 4), 32 (w % 4) + 32), i.e. 32 rows of the
     // weight block, for every token of the job
     const int quad = warp & 3;
@@ -497,8 +557,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       int e, wb, r0, rows;
       job(j, e, wb, r0, rows);
       const int a = j & 1;
-      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tmem_full[a], (j >> 1) & 1, p.wait_ns) ? 1 : 0);
-      if (!ok) *s_abort = 1;
+      bool ok = __all_sync(0xffffffffu, wait_bar(&tmem_full[a], (j >> 1) & 1) ? 1 : 0);
+      if (!ok && lane == 0) set_abort();
       ok = ok && !warp_aborted(s_abort);
       if (kGLU) ok = bar_and(1, 128, ok);  // the four warps meet at the exchange below
       if (!ok) break;
@@ -553,65 +613,105 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[a]);
+      if (lane == 0) {
+        if (kPair && !leader) mbar_arrive_remote(smem_in_cta(&tmem_empty[a], 0));
+        else mbar_arrive(&tmem_empty[a]);
+      }
     }
   }
   tc_fence_before();
-  __syncthreads();
-  // Past this barrier every role has stopped issuing and the abort flag is final. After a
-  // give-up -- by any warp, possibly after another role had already finished its loop --
-  // copies may still be landing in shared memory and MMAs still writing TMEM: both are
-  // drained before the CTA frees its tensor memory and exits (these waits keep the full
-  // limit).
+  if constexpr (kPair) cluster_sync();
+  else __syncthreads();
+  // Past this barrier every role (of both CTAs of a pair) has stopped issuing and the
+  // abort flag is final. After a give-up -- by any warp, possibly after another role had
+  // already finished its loop -- copies may still be landing in shared memory and MMAs
+  // still writing TMEM: both are drained before the CTA frees its tensor memory and exits
+  // (these waits keep the full limit).
   const bool aborted = *s_abort != 0;
-  if (aborted && threadIdx.x == 0) {
+  if (!kPair && aborted && threadIdx.x == 0) {
     // prefetched weight stages whose row copy was never issued miss one arrival
     for (int kb = issued; kb < pre; ++kb) mbar_arrive_expect_tx(&full[kb], 0);
     for (int gg = (issued > pre ? issued : pre) - 1; gg >= 0 && gg >= issued - STAGES; --gg)
       mbar_wait_bounded(&full[gg % STAGES], (gg / STAGES) & 1);
   }
-  if (aborted && threadIdx.x == 32) {
-    tc_commit(mma_done);  // arrives once every MMA this thread issued has completed
+  if (kPair && aborted && threadIdx.x == 0) {
+    // A pair's copies complete on the leader's barriers, armed for both CTAs' bytes: once
+    // the two CTAs stopped at different stages no phase can be awaited exactly. Each
+    // copy is at most a 32 KB box; 100 us is far beyond its flight time.
+    const unsigned long long t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 100000ull) {
+    }
+  }
+  if (aborted && threadIdx.x == 32 && leader) {
+    if constexpr (kPair) tc_commit_pair(mma_done);  // once every MMA issued has completed
+    else tc_commit(mma_done);
     mbar_wait_bounded(mma_done, 0);
   }
   if (threadIdx.x == 0) {
     if (aborted) set_dev_error(p.hdr, MOE_LORA_DEVERR_TIMEOUT);
     if (!waited0) pdl_wait();  // a CTA leaves only once its predecessor has completed
   }
+  // a pair: the leader's MMAs into this CTA's TMEM and the other CTA's arrivals on this
+  // CTA's barriers are over before either frees anything
+  if constexpr (kPair) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, C::kTmemCols);
+    else tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
-template <int BN, int STAGES, bool kGLU>
+template <int BN, int STAGES, bool kGLU, bool kPair = false>
 static int launch_fused_t(const CUtensorMap& tw, const CUtensorMap& ta, const CUtensorMap& tb,
                           const CUtensorMap& tz, const FusedArgs& args, int E,
                           cudaStream_t stream, bool pdl) {
-  using C = FusedCfg<BN, STAGES, kGLU>;
+  using C = FusedCfg<BN, STAGES, kGLU, kPair>;
+  auto kernel = fused_gemm_kernel<BN, STAGES, kGLU, kPair>;
   static std::atomic<uint64_t> configured[kMaxDevices];
   int st = once_per_context(configured, [] {
-    ML_CHECK_CUDA(cudaFuncSetAttribute(fused_gemm_kernel<BN, STAGES, kGLU>,
+    ML_CHECK_CUDA(cudaFuncSetAttribute(fused_gemm_kernel<BN, STAGES, kGLU, kPair>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     return MOE_LORA_OK;
   });
   if (st != MOE_LORA_OK) return st;
+  if (kPair) {  // persistent CTA pairs: as many as can be resident at once
+    if (args.mode != kFModePersistent) return MOE_LORA_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)num_sms());
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    ML_CHECK_CUDA(cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg));
+    if (clusters < 1) return MOE_LORA_ERR_UNSUPPORTED;
+    int64_t units = (int64_t)args.max_tiles * ((args.n_wblocks + 1) / 2);
+    if (units > clusters) units = clusters;
+    if (units < 1) units = 1;
+    return launch_pdl_cluster(kernel, dim3(2 * (unsigned)units), kFusedThreads, C::kSmemBytes,
+                              stream, pdl, 2, tw, ta, tb, tz, args);
+  }
   int64_t grid = (int64_t)(args.mode == kFModeExpert ? E * args.ksplit : args.max_tiles) *
                  args.n_wblocks;
   if (args.mode == kFModePersistent) {  // one resident CTA per SM slot, each looping over jobs
     int per_sm = 0;
-    ML_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, fused_gemm_kernel<BN, STAGES, kGLU>, kFusedThreads, C::kSmemBytes));
+    ML_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFusedThreads,
+                                                                C::kSmemBytes));
     const int64_t slots = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
     if (grid > slots) grid = slots;
   }
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
-  return launch_pdl(fused_gemm_kernel<BN, STAGES, kGLU>, dim3((unsigned)grid), kFusedThreads,
-                    C::kSmemBytes, stream, pdl, tw, ta, tb, tz, args);
+  return launch_pdl(kernel, dim3((unsigned)grid), kFusedThreads, C::kSmemBytes, stream, pdl, tw,
+                    ta, tb, tz, args);
 }
 
 ZPadLayout zpad_layout(int S, int E, int L, int r, int gap) {
@@ -638,7 +738,8 @@ ZPadLayout zpad_layout(int S, int E, int L, int r, int gap) {
 int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const void* zpad,
                       const ZPadLayout& zl, const moe_lora_align_t* al, const AlignLayout& a,
                       int N_w, int K, int r, bool glu, void* out, cudaStream_t stream, bool pdl,
-                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit) {
+                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit,
+                      bool pairs) {
   if (a.S == 0) return MOE_LORA_OK;
   // a split of the K range: expert-major down form only, at least two k-blocks a share
   if (ksplit < 1 || (ksplit > 1 && (glu || expert_major_bn == 0 || ceil_div(K, kFBK) < 2 * ksplit)))
@@ -649,6 +750,9 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
   const int mode = expert_major_bn > 0 ? kFModeExpert : bn >= 128 ? kFModePersistent : kFModeTile;
   const bool lora = al->L > 0 && B != nullptr && zpad != nullptr;
   if (lora && (zl.gap < bn || r % 8 != 0 || zl.rows >= (1ll << 31))) return MOE_LORA_ERR_UNSUPPORTED;
+  // 256-row token tiles: CTA pairs, each CTA staging 128 of the tile's rows
+  const bool pair = pairs && mode == kFModePersistent && bn == 256;
+  const uint32_t rows_per_cta = pair ? (uint32_t)bn / 2 : (uint32_t)bn;
   const int wrows = glu ? kFBM / 2 : kFBM;  // weight rows per box (gate and up halves: 64 each)
   CUtensorMap tw, ta, tb, tz;
   {
@@ -658,10 +762,10 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
     int st = make_tmap_bf16(&tw, W, 3, dims, strides, box);
     if (st != MOE_LORA_OK) return st;
   }
-  {
+  {  // the token rows in sorted order (a CTA of a pair stages half the tile's rows)
     const uint64_t dims[2] = {(uint64_t)K, (uint64_t)a.S};
     const uint64_t strides[1] = {(uint64_t)K * 2};
-    const uint32_t box[2] = {kFBK, (uint32_t)bn};
+    const uint32_t box[2] = {kFBK, rows_per_cta};
     int st = make_tmap_bf16(&ta, a_sorted, 2, dims, strides, box);
     if (st != MOE_LORA_OK) return st;
   }
@@ -684,7 +788,7 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
     if (st != MOE_LORA_OK) return st;
     const uint64_t zdims[2] = {(uint64_t)zl.zw, (uint64_t)zl.rows};
     const uint64_t zstrides[1] = {(uint64_t)zl.zw * 2};
-    const uint32_t zbox[2] = {(uint32_t)z_cols, (uint32_t)bn};
+    const uint32_t zbox[2] = {(uint32_t)z_cols, rows_per_cta};
     st = make_tmap_bf16(&tz, zpad, 2, zdims, zstrides, zbox, swz(z_cols));
     if (st != MOE_LORA_OK) return st;
   } else {
@@ -710,9 +814,6 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
   args.L = al->L;
   args.gap = zl.gap;
   args.lora = lora ? 1 : 0;
-  // the gate_up form's z is ready as the GEMM starts (its shrink computed before waiting):
-  // the adapter stages follow the first base stage; the down form's shrink starts when
-  // the gate_up GEMM ends: the stages wait until half the K range has streamed
   args.zchunks = lora ? zl.zchunks : 0;
   args.zk = zl.zk;
   args.rp16 = zl.rp16;
@@ -734,8 +835,12 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
                         : launch_fused_t<64, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
     case 128: return glu ? launch_fused_t<128, 6, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
                          : launch_fused_t<128, 6, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
-    case 256: return glu ? launch_fused_t<256, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
-                         : launch_fused_t<256, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
+    case 256:
+      if (pair)  // 32 KB stages: six in the ring
+        return glu ? launch_fused_t<256, 6, true, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                   : launch_fused_t<256, 6, false, true>(tw, ta, tb, tz, args, al->E, stream, pdl);
+      return glu ? launch_fused_t<256, 4, true>(tw, ta, tb, tz, args, al->E, stream, pdl)
+                 : launch_fused_t<256, 4, false>(tw, ta, tb, tz, args, al->E, stream, pdl);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
 }

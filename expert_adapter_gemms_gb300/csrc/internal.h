@@ -66,10 +66,13 @@ struct ZPadOut {
 // may be read before griddepcontrol.wait.
 // ksplit > 1 (expert-major down form): the K range in ksplit shares, each CTA writing its
 // own partial output at out + share * S * N (the combine sums them).
+// pairs: 256-row token tiles run on CTA pairs (tcgen05.mma.cta_group::2, M = 256 over two
+// weight blocks).
 int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const void* zpad,
                       const ZPadLayout& zl, const moe_lora_align_t* al, const AlignLayout& a,
                       int N_w, int K, int r, bool glu, void* out, cudaStream_t stream, bool pdl,
-                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit = 1);
+                      bool early, int expert_major_bn, unsigned long long wait_ns, int ksplit = 1,
+                      bool pairs = true);
 
 // y[t] = sum_j w[t, j] O[row(t, j)] (j ascending) over O [S, N] fp32 by sorted row; with
 // nparts > 1, O holds nparts partial outputs part_stride elements apart, summed in order.

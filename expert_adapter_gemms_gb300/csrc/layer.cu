@@ -489,7 +489,8 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
     }
     ML_STEP(mark(4));
     ML_STEP(launch_fused_gemm(xs, W1, lora ? B1 : nullptr, Z1p, p.z, &al, p.al, 2 * I, H, r, true, h,
-                              stream, pdl, ch.early(kGemm1), em_bn, wait_ns));
+                              stream, pdl, ch.early(kGemm1), em_bn, wait_ns, 1,
+                              o.mma_pairs >= 0));
     ML_STEP(mark(5));
     ML_STEP(mark(6));
     if (lora) {  // h comes from the predecessor: the shrink waits for it, A streams first
@@ -499,7 +500,8 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
     }
     ML_STEP(mark(7));
     ML_STEP(launch_fused_gemm(h, W2, lora ? B2 : nullptr, Z2p, p.z, &al, p.al, H, I, r, false, O,
-                              stream, pdl, ch.early(kGemm2), em_bn, wait_ns, p.ksplit));
+                              stream, pdl, ch.early(kGemm2), em_bn, wait_ns, p.ksplit,
+                              o.mma_pairs >= 0));
     ML_STEP(mark(8));
     ML_STEP(launch_combine(O, w, &al, p.al, H, y, y_fp32, stream, pdl, p.ksplit,
                            (size_t)T * k * H));

@@ -824,6 +824,77 @@ __global__ void __launch_bounds__(kExpandThreads)
   }
 }
 
+// The same combine, four columns per thread: 16-byte loads of O, and the loads of eight
+// consecutive slots (two tokens at k = 4) in flight before they are summed -- per element
+// the same products in the same order as above, so the same bits. N % 4 == 0 and y
+// aligned for 16-byte (fp32) or 8-byte (bf16) stores.
+template <bool kOutF32>
+__global__ void __launch_bounds__(kExpandThreads)
+    combine4_kernel(const float* __restrict__ O, const float* __restrict__ w,
+                    const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
+                    int tokens_per_cta, int nparts, size_t part_stride) {
+  constexpr int KM = 8;
+  __shared__ int s_row[kExpandThreads];
+  __shared__ float s_w[kExpandThreads];
+  pdl_wait();
+  pdl_trigger();
+  const int t0 = blockIdx.x * tokens_per_cta;
+  const int t1 = min(T, t0 + tokens_per_cta);
+  const int ns = (t1 - t0) * k;  // the host keeps tokens_per_cta * k <= 256
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    s_row[i] = __ldcg(slot_row + (size_t)t0 * k + i);
+    s_w[i] = __ldcg(w + (size_t)t0 * k + i);
+  }
+  __syncthreads();
+  const int n = 4 * (blockIdx.y * kExpandThreads + threadIdx.x);
+  if (n >= N) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 < ns; q0 += KM) {
+    float4 o[KM];
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+      o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int row = q0 + i < ns ? s_row[q0 + i] : -1;
+      if (row >= 0) {
+        o[i] = __ldcg(reinterpret_cast<const float4*>(O + (size_t)row * N + n));
+        for (int pp = 1; pp < nparts; ++pp) {  // partial outputs of a split K range
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(O + pp * part_stride + (size_t)row * N + n));
+          o[i].x += v.x;
+          o[i].y += v.y;
+          o[i].z += v.z;
+          o[i].w += v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+      const int q = q0 + i;
+      if (q >= ns) break;
+      if (s_row[q] >= 0) {
+        const float wq = s_w[q];
+        acc.x = fmaf(wq, o[i].x, acc.x);
+        acc.y = fmaf(wq, o[i].y, acc.y);
+        acc.z = fmaf(wq, o[i].z, acc.z);
+        acc.w = fmaf(wq, o[i].w, acc.w);
+      }
+      if ((q + 1) % k == 0) {  // the token's last slot
+        const size_t at = (size_t)(t0 + q / k) * N + n;
+        if (kOutF32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(y) + at) = acc;
+        } else {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 u;
+          u.x = *reinterpret_cast<const uint32_t*>(&lo);
+          u.y = *reinterpret_cast<const uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(y) + at) = u;
+        }
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
@@ -1059,15 +1130,24 @@ int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* 
   if (a.S == 0 || al->T == 0) return MOE_LORA_OK;
   AlignView v = align_view(al->buf, a);
   const int sms = num_sms();
+  // four columns a thread where the row width and y's address allow 16-byte (8-byte) access
+  const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
+  const bool vec = N % 4 == 0 && (ya % (y_fp32 ? 16 : 8)) == 0 &&
+                   reinterpret_cast<uintptr_t>(O) % 16 == 0 && part_stride % 4 == 0;
   // tokens per CTA: as many as keep about four CTAs per SM busy (at most 8, and the CTA's
   // slots within the 256-entry shared tables)
-  const int ncol = ceil_div(N, kExpandThreads);
+  const int ncol = ceil_div(N, kExpandThreads * (vec ? 4 : 1));
   int tpc = 1;
   while (tpc < 8 && (int64_t)ceil_div(al->T, tpc * 2) * ncol >= 4 * sms &&
          tpc * 2 * al->k <= kExpandThreads)
     tpc *= 2;
   if (tpc * al->k > kExpandThreads) return MOE_LORA_ERR_UNSUPPORTED;
   const dim3 g2(ceil_div(al->T, tpc), ncol);
+  if (vec)
+    return y_fp32 ? launch_pdl(combine4_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
+                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride)
+                  : launch_pdl(combine4_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
+                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride);
   return y_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
                              (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride)
                 : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,

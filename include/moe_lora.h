@@ -280,6 +280,11 @@ typedef struct moe_lora_layer_opts {
                            drains its own copies and tensor-core work (those waits keep the 4 s
                            limit), frees its tensor memory and exits, and that launch's
                            results are invalid. */
+  int32_t mma_pairs;    /* fused chain with 256-row token tiles: 0 = the library's choice
+                           (pairs of CTAs, each job one tcgen05.mma.cta_group::2 of M = 256
+                           over two 128-row weight blocks, each CTA staging half the token
+                           rows); -1 = one CTA per 128-row weight block. Same results up to
+                           fp32 summation order. */
 } moe_lora_layer_opts;
 
 #define MOE_LORA_LAYER_NUM_STAGES 9

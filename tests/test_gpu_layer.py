@@ -127,6 +127,35 @@ def test_fused_expand_shapes(shape):
     assert_close(y, f64(y_sep), 1e-3, f"fused vs separate expand, {shape}")
 
 
+@pytest.mark.parametrize("shape", ["odd_blocks_many_runs", "ragged_tiles_r32",
+                                   "base_only", "r64_chunked_pairs", "one_tile"])
+def test_fused_cta_pairs(shape):
+    """256-row token tiles of the fused chain run on CTA pairs: one
+    tcgen05.mma.cta_group::2 of M = 256 over two weight blocks, each CTA staging half of
+    the tile's rows (split at half the MMA width, which follows the tile's rows). Shapes:
+    an odd number of 64-feature gate_up blocks and of 128-row down blocks (the last
+    pair's second CTA has no block), ragged last tiles of every expert, chunked rank-64
+    z, no adapters, and a single tile shorter than the split. Every token against the
+    oracle, and against the one-CTA MMAs."""
+    m = need_gpu()
+    kw = {"odd_blocks_many_runs": dict(T=1104, H=320, I=320, E=6, k=2, L=16, r=16,
+                                       adapters="one_per_request16"),
+          "ragged_tiles_r32": dict(T=900, H=384, I=224, E=5, k=3, L=5, r=32),
+          "base_only": dict(T=700, H=256, I=192, E=4, k=2, L=0, r=16),
+          "r64_chunked_pairs": dict(T=640, H=256, I=192, E=4, k=2, L=3, r=64),
+          "one_tile": dict(T=300, H=128, I=64, E=2, k=1, L=2, r=16)}[shape]
+    inp = make_layer_inputs(seed=300 + len(shape), lora_std=None, **kw)
+    plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    assert plan["fused_expand"] == 1 and plan["bm_base"] == 256, plan
+    y = run_layer(m, inp, y_fp32=True).cpu()
+    y1 = run_layer(m, inp, y_fp32=True, mma_pairs=-1).cpu()
+    ref = oracle_layer(inp)
+    assert_close(y, ref, LAYER_RTOL, f"pairs {shape} {plan}")
+    assert_close(y1, ref, LAYER_RTOL, f"one CTA {shape} {plan}")
+    # the same products in the same K order: only the accumulation hardware differs
+    assert_close(y, f64(y1), 1e-4, f"pairs vs one CTA, {shape}")
+
+
 def test_layer_error_word_clean_on_workload():
     m = need_gpu()
     inp = make_workload_inputs("gptoss20b_decode")
