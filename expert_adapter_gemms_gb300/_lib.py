@@ -53,7 +53,8 @@ class LayerOpts(ctypes.Structure):
 class LayerPlan(ctypes.Structure):
     _fields_ = [("bm_base", ctypes.c_int32), ("bm_lora", ctypes.c_int32),
                 ("expert_major_rows", ctypes.c_int32), ("fused_expand", ctypes.c_int32),
-                ("launches", ctypes.c_int32), ("early_reads", ctypes.c_int32)]
+                ("launches", ctypes.c_int32), ("early_reads", ctypes.c_int32),
+                ("route_in_align", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p

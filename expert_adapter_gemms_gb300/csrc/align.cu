@@ -12,13 +12,18 @@
 // keys, give the expert and (expert, adapter) segment boundaries, from which the
 // grouped-GEMM token tiles and the LoRA blocks are cut. Working state (bucket counts and starts, the
 // sort buffers) stays in shared memory whenever it fits; only results go out.
+// Up to kRankSortMaxSlots slots the words are placed by rank instead of the radix sort, and
+// a layer at few tokens has this CTA route the tokens first (one launch fewer).
 #include <atomic>
-#include "common.cuh"
+
+#include "internal.h"
+#include "route.cuh"
 
 namespace moe_lora {
 
 constexpr int kSmemSortMaxSlots = 16384;
 constexpr size_t kAlignSmemBudget = 200 * 1024;
+constexpr int kRankSortMaxSlots = 512;
 
 // Exclusive scan of one int per thread across the CTA; returns the prefix and
 // writes the total to *total. `tmp` holds NW + 1 ints.
@@ -138,6 +143,23 @@ __device__ uint32_t* block_radix_sort(uint32_t* a, uint32_t* b, int n, int lo, i
   return src;
 }
 
+// The words are unique ((key, slot) with distinct slots), so the stable key order of the
+// radix sort is their ascending order, and a word's place is the number of smaller words:
+// for a few hundred words one pass of broadcast shared-memory reads per thread, without
+// the radix sort's barriers. The same result, bit for bit.
+template <int NT>
+__device__ uint32_t* block_rank_sort(const uint32_t* a, uint32_t* b, int n) {
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t x = a[i];
+    int pos = 0;
+#pragma unroll 8
+    for (int j = 0; j < n; ++j) pos += a[j] < x ? 1 : 0;
+    b[pos] = x;
+  }
+  __syncthreads();
+  return b;
+}
+
 // Shared-memory plan of one align launch (host and device agree through this).
 struct AlignSmem {
   int hist_off, tmp_off, bcount_off, bstart_off, sort_off;  // in ints
@@ -164,11 +186,14 @@ __host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nt
   return p;
 }
 
-template <int NT>
+// V > 0: route first (logits [T, E], V experts a lane): ids and w are written here and
+// the keys read the ids back (ids then points at that buffer).
+template <int NT, int V>
 __global__ void __launch_bounds__(NT, 1)
     align_kernel(const int* __restrict__ ids, const int* __restrict__ token_adapter, AlignView v,
                  int T, int k, int E, int L, int bm_base, int bm_lora, int S, int nbuckets,
-                 int key_bits, int slot_bits) {
+                 int key_bits, int slot_bits, const float* __restrict__ logits,
+                 float* __restrict__ w_out) {
   constexpr int NW = NT / 32;
   extern __shared__ __align__(16) int smem[];
   const AlignSmem plan = align_smem_plan(S, nbuckets, NT);
@@ -188,6 +213,26 @@ __global__ void __launch_bounds__(NT, 1)
   pdl_trigger();
   pdl_wait();
   if (tid == 0) s_err = 0u;
+  if constexpr (V > 0) {  // 0. routing, one warp per token (its ids are read back below):
+    // eight of a warp's tokens at once, their logits in flight and their selections side
+    // by side
+    constexpr int TB = 8;
+    int* ids_out = const_cast<int*>(ids);
+    for (int t0 = warp; t0 < T; t0 += NW * TB) {
+      float lv[TB][V];
+      int tok[TB];
+#pragma unroll
+      for (int b = 0; b < TB; ++b) {
+        const int t = t0 + b * NW;
+        tok[b] = t < T ? t : -1;
+        if (t < T) topk_softmax_load<V>(logits + (size_t)t * E, E, lv[b]);
+        else
+#pragma unroll
+          for (int i = 0; i < V; ++i) lv[b][i] = -INFINITY;
+      }
+      topk_softmax_select<V, TB>(lv, tok, E, k, ids_out, w_out);
+    }
+  }
   __syncthreads();
 
   // 1. keys (the loads of four slots go out together)
@@ -220,7 +265,9 @@ __global__ void __launch_bounds__(NT, 1)
   __syncthreads();
 
   // 2. stable LSD radix sort on the key bits (8-bit digits)
-  uint32_t* src = block_radix_sort<NT>(bufA, bufB, S, slot_bits, key_bits, hist, tmp);
+  uint32_t* src = plan.smem_sort && S <= kRankSortMaxSlots
+                      ? block_rank_sort<NT>(bufA, bufB, S)
+                      : block_radix_sort<NT>(bufA, bufB, S, slot_bits, key_bits, hist, tmp);
   uint32_t* dst = src == bufA ? bufB : bufA;
   const unsigned lt = (1u << lane) - 1u;
 
@@ -532,21 +579,35 @@ __global__ void __launch_bounds__(NT)
   }
 }
 
-template <int NT>
+template <int NT, int V>
 static int launch_align_t(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
-                          const AlignLayout& a, cudaStream_t stream, bool pdl) {
+                          const AlignLayout& a, cudaStream_t stream, bool pdl,
+                          const float* logits = nullptr, float* w = nullptr) {
   AlignView v = align_view(al->buf, a);
   const AlignSmem plan = align_smem_plan(a.S, a.nbuckets, NT);
   static std::atomic<uint64_t> configured[kMaxDevices];
   int st = once_per_context(configured, [] {
-    ML_CHECK_CUDA(cudaFuncSetAttribute(align_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ML_CHECK_CUDA(cudaFuncSetAttribute(align_kernel<NT, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)(kAlignSmemBudget + 16 * 1024)));
     return MOE_LORA_OK;
   });
   if (st != MOE_LORA_OK) return st;
-  return launch_pdl(align_kernel<NT>, 1, NT, plan.bytes, stream, pdl, ids, token_adapter, v,
+  return launch_pdl(align_kernel<NT, V>, 1, NT, plan.bytes, stream, pdl, ids, token_adapter, v,
                     al->T, al->k, al->E, al->L, al->bm_base, al->bm_lora, a.S, a.nbuckets,
-                    a.key_bits, a.slot_bits);
+                    a.key_bits, a.slot_bits, logits, w);
+}
+
+bool align_can_route(const AlignLayout& a, int T, int E) {
+  return a.ctas == 0 && a.S <= 4096 && T <= kAlignRouteMaxTokens && E <= 128;
+}
+
+int launch_route_align(const float* logits, int* ids, float* w, const int* token_adapter,
+                       const moe_lora_align_t* al, const AlignLayout& a, cudaStream_t stream,
+                       bool pdl) {
+  if (!align_can_route(a, al->T, al->E)) return MOE_LORA_ERR_UNSUPPORTED;
+  if (al->E <= 32) return launch_align_t<256, 1>(ids, token_adapter, al, a, stream, pdl, logits, w);
+  if (al->E <= 64) return launch_align_t<256, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
+  return launch_align_t<256, 4>(ids, token_adapter, al, a, stream, pdl, logits, w);
 }
 
 int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
@@ -563,8 +624,8 @@ int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_
                       a.nbuckets, a.slot_bits, a.ctas);
   }
   // few slots: a small CTA keeps the many barriers of the sort cheap
-  if (a.S <= 4096) return launch_align_t<256>(ids, token_adapter, al, a, stream, pdl);
-  return launch_align_t<1024>(ids, token_adapter, al, a, stream, pdl);
+  if (a.S <= 4096) return launch_align_t<256, 0>(ids, token_adapter, al, a, stream, pdl);
+  return launch_align_t<1024, 0>(ids, token_adapter, al, a, stream, pdl);
 }
 
 }  // namespace moe_lora

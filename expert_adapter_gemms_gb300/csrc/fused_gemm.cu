@@ -46,7 +46,8 @@ namespace moe_lora {
 constexpr int kFBM = 128;  // weight rows per block (MMA M)
 constexpr int kFBK = 64;   // K per stage
 constexpr int kFusedThreads = 192;
-constexpr int kFGroupTiles = 8;
+constexpr int kFGroupTiles = 16;  // token tiles that share their weight blocks (<= 24 MB of rows)
+constexpr int kFMaxExperts = 1024;
 constexpr int kXStride = 17;  // floats per row of the gate/up exchange tile (conflict-free)
 enum { kFModeTile = 0, kFModeExpert = 1, kFModePersistent = 2 };
 
@@ -60,14 +61,18 @@ struct FusedCfg {
   static constexpr int kStageBytes = kWBytes + kABytes;
   static constexpr int kBarOff = STAGES * kStageBytes;
   static constexpr int kXOff = kBarOff + 256;  // gate/up exchange tile [128][kXStride] fp32
-  static constexpr int kSmemBytes = kXOff + (kGLU ? kFBM * kXStride * 4 : 0) + 1024;
+  static constexpr int kT0Off = kXOff + (kGLU ? kFBM * kXStride * 4 : 0);  // first tile per expert
+  // expert-major launches take kSmemBytes (two CTAs an SM at the decode shapes); the token
+  // tile modes add the first-tile table
+  static constexpr int kSmemBytes = kT0Off + 1024;
+  static constexpr int kSmemTiles = kSmemBytes + 4 * (kFMaxExperts + 8);
   static constexpr uint32_t kAccCols = BN < 32 ? 32 : BN;  // one fp32 accumulator
   static constexpr uint32_t kTmemCols = 2 * kAccCols;     // two, used alternately
   static_assert((2 * STAGES + 5) * 8 + 16 <= 256, "barrier area");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kABytes % 1024 == 0, "stage alignment");
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kSmemTiles <= 227 * 1024, "shared memory");
   static_assert(!kPair || BN == 256, "CTA pairs take 256-row token tiles");
 };
 
@@ -201,17 +206,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int unit = kPair ? (int)blockIdx.x / 2 : (int)blockIdx.x;
   const int nunits = kPair ? (int)gridDim.x / 2 : (int)gridDim.x;
   const int n_wblocks = kPair ? (p.n_wblocks + 1) / 2 : p.n_wblocks;  // weight jobs per tile
-  // (token tile, weight block) jobs in groups of kFGroupTiles tiles, so that CTAs sharing
-  // a weight block run together
-  auto tile_job = [&](int w, int n_tiles, int& e, int& wb, int& r0, int& rows) {
+  // (token tile, weight block) jobs expert by expert, in groups of up to kFGroupTiles of the
+  // expert's tiles taken weight block by weight block: the CTAs that share a weight block
+  // run together and the group's token rows stay in L2, so each weight block is read from
+  // memory about once. s_t0[e] = the first tile of expert e (the align cuts every expert's
+  // rows into tiles of BN rows, in expert order); expert e's jobs are [s_t0[e] nwb,
+  // s_t0[e + 1] nwb), so tile w / nwb is one of e's own.
+  int* s_t0 = reinterpret_cast<int*>(smem + C::kT0Off);
+  auto tile_job = [&](int w, int& e, int& wb, int& r0, int& rows) {
+    const int ew = __ldcg(p.tiles + w / n_wblocks).x;
+    const int t0 = s_t0[ew], nt = s_t0[ew + 1] - t0;
+    const int u = w - t0 * n_wblocks;
     const int per_group = kFGroupTiles * n_wblocks;
-    const int grp = w / per_group;
+    const int grp = u / per_group;
     const int first = grp * kFGroupTiles;
-    const int gsz = min(kFGroupTiles, n_tiles - first);
-    const int within = w - grp * per_group;
+    const int gsz = min(kFGroupTiles, nt - first);
+    const int within = u - grp * per_group;
     wb = within / gsz;
     if (kPair) wb = 2 * wb + (int)crank;
-    const int4 tile = __ldcg(p.tiles + first + within % gsz);
+    const int4 tile = __ldcg(p.tiles + t0 + first + within % gsz);
     e = tile.x;
     r0 = tile.y;
     rows = tile.z;
@@ -285,26 +298,30 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     njobs = -1;  // known once the expert's rows are read
   } else {
     n_tiles = __ldcg(p.hdr + HDR_NTILES);
+    if (warp == 0) {  // s_t0: exclusive prefix of the experts' tile counts
+      int carry = 0;
+      for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        const int c = e < p.E ? (__ldcg(p.expert_begin + e + 1) - __ldcg(p.expert_begin + e) + BN - 1) / BN : 0;
+        int v = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, v, off);
+          if (lane >= off) v += y;
+        }
+        if (e < p.E) s_t0[e] = carry + v - c;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      if (lane == 0) s_t0[p.E] = carry;
+    }
+    __syncthreads();
     const int total = n_tiles * n_wblocks;
     if (persistent) {
       njobs = unit < total ? (total - 1 - unit) / nunits + 1 : 0;
-      if (njobs > 0) tile_job(unit, n_tiles, e0, wb0, r00, rows0);
+      if (njobs > 0) tile_job(unit, e0, wb0, r00, rows0);
     } else {
-      const int lin = blockIdx.x;
-      const int per_group = kFGroupTiles * n_wblocks;
-      const int grp = lin / per_group;
-      const int first = grp * kFGroupTiles;
-      const int gsz = min(kFGroupTiles, p.max_tiles - first);
-      const int within = lin - grp * per_group;
-      wb0 = within / gsz;
-      const int ti = first + within % gsz;
-      njobs = ti < n_tiles ? 1 : 0;
-      if (njobs) {
-        const int4 tile = __ldcg(p.tiles + ti);
-        e0 = tile.x;
-        r00 = tile.y;
-        rows0 = tile.z;
-      }
+      njobs = (int)blockIdx.x < total ? 1 : 0;
+      if (njobs) tile_job(blockIdx.x, e0, wb0, r00, rows0);
     }
     if (njobs == 0) {
       if (p.early) pdl_wait();  // a CTA leaves only once its predecessor has completed
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
   // the first ring of weight stages of the first job (a weight never depends on a launch)
   if (threadIdx.x == 0) {
-    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_w = expert_major ? l2_policy_evict_first() : l2_policy_evict_normal();
     for (int kb = 0; kb < pre; ++kb) {
       arm(kb, C::kWBytes);
       load_w(smem + kb * C::kStageBytes, kb, kb, wb0, e0, pol_w);
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       r0 = s_job[0] + j * BN;
       rows = min(BN, s_job[1] - j * BN);
     } else if (persistent && j > 0) {
-      tile_job(unit + j * nunits, n_tiles, e, wb, r0, rows);
+      tile_job(unit + j * nunits, e, wb, r0, rows);
     } else {
       e = e0; wb = wb0; r0 = r00; rows = rows0;
     }
@@ -383,8 +400,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   int issued = 0;           // producer: stages whose row (or z) copy went out
   if (warp == 0) {
     // producer: the whole warp walks the jobs (the adapter runs are found warp-wide);
-    // lane 0 issues the copies
-    const uint64_t pol_w = l2_policy_evict_first();
+    // lane 0 issues the copies. Expert-major, a weight block is read by one CTA: it streams
+    // through L2 marked to go first; token tiles share each weight block with the other
+    // tiles of their group, which read it moments later.
+    const uint64_t pol_w = expert_major ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint64_t pol_a = l2_policy_evict_last();
     int g = 0;
     if (njobs == 0 && lane == 0) {  // expert-major with no row: complete the prefetched stages
@@ -674,16 +693,17 @@ static int launch_fused_t(const CUtensorMap& tw, const CUtensorMap& ta, const CU
   static std::atomic<uint64_t> configured[kMaxDevices];
   int st = once_per_context(configured, [] {
     ML_CHECK_CUDA(cudaFuncSetAttribute(fused_gemm_kernel<BN, STAGES, kGLU, kPair>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemTiles));
     return MOE_LORA_OK;
   });
   if (st != MOE_LORA_OK) return st;
+  const int smem = args.mode == kFModeExpert ? C::kSmemBytes : C::kSmemTiles;
   if (kPair) {  // persistent CTA pairs: as many as can be resident at once
     if (args.mode != kFModePersistent) return MOE_LORA_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)num_sms());
     cfg.blockDim = dim3(kFusedThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -697,7 +717,7 @@ static int launch_fused_t(const CUtensorMap& tw, const CUtensorMap& ta, const CU
     int64_t units = (int64_t)args.max_tiles * ((args.n_wblocks + 1) / 2);
     if (units > clusters) units = clusters;
     if (units < 1) units = 1;
-    return launch_pdl_cluster(kernel, dim3(2 * (unsigned)units), kFusedThreads, C::kSmemBytes,
+    return launch_pdl_cluster(kernel, dim3(2 * (unsigned)units), kFusedThreads, smem,
                               stream, pdl, 2, tw, ta, tb, tz, args);
   }
   int64_t grid = (int64_t)(args.mode == kFModeExpert ? E * args.ksplit : args.max_tiles) *
@@ -705,12 +725,12 @@ static int launch_fused_t(const CUtensorMap& tw, const CUtensorMap& ta, const CU
   if (args.mode == kFModePersistent) {  // one resident CTA per SM slot, each looping over jobs
     int per_sm = 0;
     ML_CHECK_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kFusedThreads,
-                                                                C::kSmemBytes));
+                                                                smem));
     const int64_t slots = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 1);
     if (grid > slots) grid = slots;
   }
   if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
-  return launch_pdl(kernel, dim3((unsigned)grid), kFusedThreads, C::kSmemBytes, stream, pdl, tw,
+  return launch_pdl(kernel, dim3((unsigned)grid), kFusedThreads, smem, stream, pdl, tw,
                     ta, tb, tz, args);
 }
 
@@ -750,6 +770,7 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
   const int mode = expert_major_bn > 0 ? kFModeExpert : bn >= 128 ? kFModePersistent : kFModeTile;
   const bool lora = al->L > 0 && B != nullptr && zpad != nullptr;
   if (lora && (zl.gap < bn || r % 8 != 0 || zl.rows >= (1ll << 31))) return MOE_LORA_ERR_UNSUPPORTED;
+  if (mode != kFModeExpert && al->E > kFMaxExperts) return MOE_LORA_ERR_UNSUPPORTED;
   // 256-row token tiles: CTA pairs, each CTA staging 128 of the tile's rows
   const bool pair = pairs && mode == kFModePersistent && bn == 256;
   const uint32_t rows_per_cta = pair ? (uint32_t)bn / 2 : (uint32_t)bn;

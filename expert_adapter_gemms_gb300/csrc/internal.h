@@ -9,6 +9,13 @@ int check_route_args(const float* logits, int T, int E, int k, const int32_t* id
 int launch_topk_softmax(const float* logits, int T, int E, int k, int* ids, float* w,
                         cudaStream_t stream, bool pdl);
 
+// The one-CTA align routing the tokens itself (few tokens): ids and w are written by the
+// same launch. align_can_route tells where it applies.
+constexpr int kAlignRouteMaxTokens = 256;
+bool align_can_route(const AlignLayout& a, int T, int E);
+int launch_route_align(const float* logits, int* ids, float* w, const int* token_adapter,
+                       const moe_lora_align_t* al, const AlignLayout& a, cudaStream_t stream,
+                       bool pdl);
 int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
                  const AlignLayout& a, cudaStream_t stream, bool pdl);
 

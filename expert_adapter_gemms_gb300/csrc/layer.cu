@@ -249,7 +249,8 @@ static Chain layer_chain(const LayerPlan& p, int T, int k, int E, int L, bool ha
     c.src[s][2] = d;
   };
   const bool lora = L > 0;
-  if (have_logits) add(kRoute, 1, false);       // triggers at its start
+  // few tokens: the one-CTA align routes them itself (no route launch)
+  if (have_logits && !align_can_route(p.al, T, E)) add(kRoute, 1, false);  // triggers at its start
   add(kAlign, p.al.ctas > 0 ? 3 : 1, false);    // each align kernel triggers at its start
   if (p.fused) {
     add(kGather, 1, lora || p.em_bn == 0);  // base only, expert-major: triggers at its start
@@ -356,6 +357,7 @@ extern "C" int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int
   out->fused_expand = p.fused ? 1 : 0;
   out->launches = T > 0 ? c.n : 0;
   out->early_reads = c.early_reads();
+  out->route_in_align = T > 0 && align_can_route(p.al, T, E) ? 1 : 0;
   return MOE_LORA_OK;
 }
 
@@ -451,14 +453,19 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
   } while (0)
 
   ML_STEP(mark(0));
-  if (have_logits) {
+  const bool route_in_align = have_logits && align_can_route(p.al, T, E);
+  if (have_logits && !route_in_align) {
     ML_STEP(launch_topk_softmax(logits, T, E, k, ids, w, stream, pdl));
-  } else {
+  } else if (!have_logits) {
     ids = const_cast<int32_t*>(topk_ids);
     w = const_cast<float*>(topk_w);
   }
   ML_STEP(mark(1));
-  ML_STEP(launch_align(ids, L > 0 ? token_adapter : nullptr, &al, p.al, stream, pdl));
+  if (route_in_align)  // few tokens: the align's one CTA routes them first
+    ML_STEP(launch_route_align(logits, ids, w, L > 0 ? token_adapter : nullptr, &al, p.al, stream,
+                               pdl));
+  else
+    ML_STEP(launch_align(ids, L > 0 ? token_adapter : nullptr, &al, p.al, stream, pdl));
   ML_STEP(mark(2));
   const int em_bn = p.em_bn;
   if (p.fused) {

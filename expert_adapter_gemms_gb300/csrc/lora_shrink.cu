@@ -388,6 +388,192 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
   if (zo.p && g == 0) zpad_extras(zo, hdr, row0, rows, e, l, r);
 }
 
+// ----------------------------------------------------------------------------
+// Long K, blocks of up to 16 rows, many blocks (prefill): the register kernel above keeps
+// about 128 bytes a thread in flight, too little to cover the latency of a K = 2880 sum.
+// Here the block's rank rows of A and its x rows go through a ring of shared-memory
+// stages (256 columns, 512 bytes a row) filled by 16-byte asynchronous copies
+// (cp.async: the load path, no registers held while in flight; the bulk-copy engine
+// was measured slower for these 512-byte pieces), three stages ahead; four warps form the
+// same mma.sync products from shared memory (warp w takes k-steps w and w + 4 of each
+// stage) and the partials are reduced in warp order. Rows past the block and rank rows
+// past the adapter's rank are not copied: their stale stage contents only reach outputs
+// that are not stored (masked ranks are written as zero).
+// ----------------------------------------------------------------------------
+constexpr int kPipeKC = 256;                  // columns per stage
+constexpr int kPipeRow = kPipeKC * 2 + 64;    // bytes per stage row: == 64 (mod 128)
+constexpr int kPipeWarps = 4;
+constexpr int kPipeStages = 4;
+__host__ __device__ constexpr size_t pipe_smem(int R) {
+  return (size_t)kPipeStages * (R + 16) * kPipeRow + (R + 16) * sizeof(void*);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int NT, bool kRanked>
+__global__ void __launch_bounds__(kPipeWarps * 32, NT <= 2 ? 3 : 2)
+    lora_shrink_pipe_kernel(const __nv_bfloat16* __restrict__ X, int rows_are_slots,
+                            const __nv_bfloat16* __restrict__ A, const int* __restrict__ hdr,
+                            const int4* __restrict__ blocks, const int* __restrict__ sorted_slots,
+                            int k, int K, int r, int E, float* __restrict__ Z, int ngroups,
+                            int early, const int* __restrict__ ranks, int rs, const ZPadOut zo,
+                            int prefetch) {
+  constexpr int R = 8 * NT;
+  constexpr int NS = kPipeStages;
+  constexpr int ROWS = R + 16;  // stage rows: R rank rows of A, then 16 x rows
+  constexpr int GROUPS = kPipeKC / 8;  // 16-byte pieces per stage row
+  extern __shared__ __align__(128) uint8_t smem[];
+  const __nv_bfloat16** s_src =
+      reinterpret_cast<const __nv_bfloat16**>(smem + (size_t)NS * ROWS * kPipeRow);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, q = lane & 3;
+
+  const bool tables_early = early || prefetch;
+  if (!tables_early) pdl_wait();
+  const int b = blockIdx.x / ngroups;
+  const int g = blockIdx.x - b * ngroups;
+  const int nb = __ldcg(hdr + HDR_NBLOCKS);
+  const int4 blk = __ldcg(blocks + b);  // in bounds: the grid covers the host's block bound
+  if (b >= nb) {
+    if (tables_early) pdl_wait();
+    return;
+  }
+  const int row0 = blk.x, rows = min(blk.y, 16), e = blk.z, l = blk.w;
+  const __nv_bfloat16* Ab = A + (((size_t)l * E + e) * r + (size_t)g * R) * K;
+  const int nr = min(R, r - g * R);  // rank rows of this group
+  const unsigned long long vmask =
+      kRanked ? rank_row_mask(g * R, rs, adapter_rank(ranks, l, rs, hdr)) : ~0ull;
+  if (prefetch && !early) {  // weights never depend on a launch: A heads for L2 first
+    if (threadIdx.x < nr && ((vmask >> threadIdx.x) & 1ull))
+      bulk_prefetch_l2(Ab + (size_t)threadIdx.x * K, (uint32_t)K * 2u);
+    pdl_wait();
+  }
+  if (!early) pdl_trigger();
+  // each stage row's source (null: not copied)
+  for (int i = threadIdx.x; i < ROWS; i += blockDim.x) {
+    const __nv_bfloat16* src = nullptr;
+    if (i < R) {
+      if (i < nr && ((vmask >> i) & 1ull)) src = Ab + (size_t)i * K;
+    } else if (i - R < rows) {
+      const int row = row0 + i - R;
+      src = X + (size_t)(rows_are_slots ? row : __ldcg(sorted_slots + row) / k) * K;
+    }
+    s_src[i] = src;
+  }
+  __syncthreads();
+
+  const int nchunks = (K + kPipeKC - 1) / kPipeKC;
+  auto issue = [&](int c) {  // chunk c into its stage (an empty group past the last chunk)
+    if (c < nchunks) {
+      uint8_t* st = smem + (size_t)(c % NS) * ROWS * kPipeRow;
+      for (int it = threadIdx.x; it < ROWS * GROUPS; it += blockDim.x) {
+        const int i = it / GROUPS, grp = it - i * GROUPS;
+        const int col = c * kPipeKC + grp * 8;
+        const __nv_bfloat16* src = s_src[i];
+        if (src && col < K) cp_async16(st + (size_t)i * kPipeRow + grp * 16, src + col);
+      }
+    }
+    cp_async_commit();
+  };
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+  for (int c = 0; c < NS - 1; ++c) issue(c);
+  for (int c = 0; c < nchunks; ++c) {
+    cp_async_wait<NS - 2>();  // this thread's copies of chunk c have landed
+    __syncthreads();          // everyone's have; and every warp is done with chunk c - 1
+    issue(c + NS - 1);        // into chunk c - 1's stage
+    const uint8_t* st = smem + (size_t)(c % NS) * ROWS * kPipeRow;
+    const int cols = min(kPipeKC, K - c * kPipeKC);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s0 = (warp + kPipeWarps * h) * 32;  // the warp's k-step in the stage
+      if (s0 >= cols) continue;  // the whole warp: mma.sync needs all of its lanes
+      // K % 8 == 0: a lane's 16-byte group is wholly in or out; out, it feeds zeros
+      const int k0 = s0 + q * 8;
+      const bool kin = k0 < cols;
+      const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 xa = kin ? *reinterpret_cast<const uint4*>(st + (size_t)(R + gid) * kPipeRow + k0 * 2) : z4;
+      const uint4 xb = kin ? *reinterpret_cast<const uint4*>(st + (size_t)(R + gid + 8) * kPipeRow + k0 * 2) : z4;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 av = kin ? *reinterpret_cast<const uint4*>(st + (size_t)(nt * 8 + gid) * kPipeRow + k0 * 2) : z4;
+        mma_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, av.x, av.y);
+        mma_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, av.z, av.w);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // every warp is done with the stages
+  // reduce the four warps' partials in warp order, in the first stage
+  float (*red)[16][R + 1] = reinterpret_cast<float (*)[16][R + 1]>(smem);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    red[warp][gid][nt * 8 + 2 * q] = acc[nt][0];
+    red[warp][gid][nt * 8 + 2 * q + 1] = acc[nt][1];
+    red[warp][gid + 8][nt * 8 + 2 * q] = acc[nt][2];
+    red[warp][gid + 8][nt * 8 + 2 * q + 1] = acc[nt][3];
+  }
+  __syncthreads();
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
+  }
+  for (int idx = threadIdx.x; idx < rows * R; idx += blockDim.x) {
+    const int m = idx / R, c = idx - m * R;
+    const int rank = g * R + c;
+    if (rank >= r) continue;
+    float sum = 0.f;
+    if ((vmask >> c) & 1ull) {
+#pragma unroll
+      for (int w = 0; w < kPipeWarps; ++w) sum += red[w][m][c];
+    }
+    if (zo.p) {
+      zpad_put(zo, row0 + m, e, l, rank, sum);
+    } else {
+      Z[(size_t)__ldcg(sorted_slots + row0 + m) * r + rank] = sum;
+    }
+  }
+  if (zo.p && g == 0) zpad_extras(zo, hdr, row0, rows, e, l, r);
+}
+
+template <int NT>
+static int launch_shrink_pipe(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
+                              const AlignView& v, int max_blocks, int k, int K, int r, int E,
+                              float* Z, cudaStream_t stream, bool pdl, int early,
+                              const int* ranks, int rs, const ZPadOut& zo, int prefetch) {
+  constexpr int R = 8 * NT;
+  const int ngroups = ceil_div(r, R);
+  const int64_t grid = (int64_t)max_blocks * ngroups;
+  if (grid > 0x7fffffff) return MOE_LORA_ERR_UNSUPPORTED;
+  const size_t smem = pipe_smem(R);
+  static std::atomic<uint64_t> configured[kMaxDevices];
+  const int cst = once_per_context(configured, [smem] {
+    const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_pipe_kernel<NT, false>, attr, (int)smem));
+    ML_CHECK_CUDA(cudaFuncSetAttribute(lora_shrink_pipe_kernel<NT, true>, attr, (int)smem));
+    return MOE_LORA_OK;
+  });
+  if (cst != MOE_LORA_OK) return cst;
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, dim3((unsigned)grid), kPipeWarps * 32, smem, stream, pdl, X,
+                      rows_are_slots, A, (const int*)v.hdr, (const int4*)v.blocks,
+                      (const int*)v.sorted_slots, k, K, r, E, Z, ngroups, early, ranks, rs, zo,
+                      prefetch);
+  };
+  return ranks ? go(lora_shrink_pipe_kernel<NT, true>) : go(lora_shrink_pipe_kernel<NT, false>);
+}
+
 template <int NT, int U>
 static int launch_shrink_nt(const __nv_bfloat16* X, int rows_are_slots, const __nv_bfloat16* A,
                             const AlignView& v, int max_blocks, int k, int K, int r, int E,
@@ -430,6 +616,15 @@ int launch_shrink_impl(const void* X, int rows_are_slots, const void* A,
   // many CTAs. Many blocks (prefill): all ranks in one CTA so that X is read once.
   const int blocks_est = a.max_blocks;
   const int sms = num_sms();
+  // long sums over many blocks of up to 16 rows (prefill): the pipelined kernel
+  if (vec && al->bm_lora > 8 && K >= 1024 && r <= 32 &&
+      (int64_t)blocks_est * ceil_div(r, 16) > 4 * (int64_t)sms) {
+    if (r <= 16)
+      return launch_shrink_pipe<2>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z,
+                                   stream, pdl, ea, ranks, rs, zo, pf);
+    return launch_shrink_pipe<4>(Xp, rows_are_slots, Ap, v, a.max_blocks, al->k, K, r, al->E, Z,
+                                 stream, pdl, ea, ranks, rs, zo, pf);
+  }
   int nt;
   if ((int64_t)blocks_est * ceil_div(r, 8) <= 8 * sms) nt = 1;
   else if (r <= 16) nt = 2;

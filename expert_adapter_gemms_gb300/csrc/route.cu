@@ -1,13 +1,11 @@
-// Router top-k + softmax over the chosen logits (the router "sends each token to
-// its most relevant experts"; vllm.com.cn, section "Implementing multi-LoRA
-// inference for MoE models in vLLM"). One warp per token; HBM-light.
-#include <climits>
-
-#include "common.cuh"
+// Router top-k + softmax over the chosen logits: the router picks each token's
+// top-k experts (vllm.com.cn, section "Implementing multi-LoRA inference for MoE
+// models in vLLM"). One warp per token; HBM-light.
+#include "route.cuh"
 
 namespace moe_lora {
 
-template <int V>  // logits held per lane: experts lane, lane+32, ..., lane+32(V-1)
+template <int V>
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T,
                                                            int E, int k, int* __restrict__ ids,
                                                            float* __restrict__ w) {
@@ -15,60 +13,8 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
   pdl_trigger();
   pdl_wait();
   const int warps = blockDim.x >> 5;
-  const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps) {
-    float v[V];
-    uint32_t taken = 0;  // bit i: expert lane + 32 i chosen already or out of range
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const int e = lane + 32 * i;
-      float x = -INFINITY;
-      if (e < E) {
-        x = __ldcg(logits + (size_t)t * E + e);
-        if (isnan(x)) x = -INFINITY;  // NaN ranks below every number
-      } else {
-        taken |= 1u << i;
-      }
-      v[i] = x;
-    }
-    float sel_val = 0.f;
-    int sel_id = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int e = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-          bv = v[i];
-          bi = e;
-        }
-      }
-#pragma unroll
-      for (int off = 16; off; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) {
-        sel_val = bv;
-        sel_id = bi;
-      }
-    }
-    const float m = __shfl_sync(0xffffffffu, sel_val, 0);
-    const float ex = lane < k ? expf(sel_val - m) : 0.f;
-    float sum = ex;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane < k) {
-      ids[(size_t)t * k + lane] = sel_id;
-      w[(size_t)t * k + lane] = ex / sum;
-    }
-  }
+  for (int t = blockIdx.x * warps + (threadIdx.x >> 5); t < T; t += gridDim.x * warps)
+    topk_softmax_token<V>(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
 }
 
 int launch_topk_softmax(const float* logits, int T, int E, int k, int* ids, float* w,

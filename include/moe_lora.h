@@ -4,10 +4,9 @@
  * What the layer computes (vLLM blog "multi-LoRA for MoE", vllm.com.cn, section
  * "Implementing multi-LoRA inference for MoE models in vLLM"; and "vLLM Multi-LoRA
  * Serving for MoE Models", agentlenshq.com, section "Multi-LoRA Serving for MoE
- * Models"): a router sends every token to its k most relevant experts; each expert
- * expands the token with a gate_up projection, applies the gated activation and
- * compresses it back with a down projection; the outputs are aggregated with the
- * routing weights. Multi-LoRA adds, per request, a low-rank adapter to both
+ * Models"): each token is routed to its top-k experts; each expert applies a gate_up
+ * projection, the gated activation and a down projection, and the experts' outputs
+ * are summed with the routing weights. Multi-LoRA adds, per request, a low-rank adapter to both
  * projections: y = xW + (xA)B, where the shrink op is z = xA (h_in -> r) and the
  * expand op is zB (r -> h_out). Token routing and adapter selection together pick
  * an (expert, adapter) pair per token-slot ("compound sparsity").
@@ -77,7 +76,7 @@ enum moe_lora_status {
 MOE_LORA_API const char* moe_lora_status_string(int status);
 
 /* ---------------------------------------------------------------------------
- * Routing (the router "sends each token to its most relevant experts").
+ * Routing: the router picks each token's top-k experts.
  *
  * moe_topk_softmax: for each of T tokens, ids[t, 0..k) are the indices of the k
  * largest logits[t, :] in decreasing order (equal logits: lower index first; NaN
@@ -248,7 +247,9 @@ typedef struct moe_lora_layer_opts {
   int32_t disable_pdl;  /* 1: plain stream-ordered launches */
   int32_t num_events;   /* length of `events` (0: none) */
   void** events;        /* cudaEvent_t handles recorded on `stream` before each stage and
-                           after the last: [0] route, [1] align, [2] gather, then for the
+                           after the last: [0] route, [1] align (at few tokens the align
+                           routes them itself: [0] and [1] mark the same point), [2]
+                           gather, then for the
                            chain with a separate expand: [3] gate_up GEMM, [4] gate_up
                            shrink, [5] gate_up expand+SwiGLU, [6] down GEMM, [7] down shrink,
                            [8] down expand+combine; for the fused chain
@@ -353,7 +354,9 @@ MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, 
  *                         launch). The plan checks each: the producer is at least two launches
  *                         back and the launch in between triggers its dependents only after its
  *                         own wait, so the producer has completed when the reader starts; a
- *                         chain that broke this would be refused (MOE_LORA_ERR_UNSUPPORTED). */
+ *                         chain that broke this would be refused (MOE_LORA_ERR_UNSUPPORTED).
+ *   route_in_align        1: routed from logits, the one-CTA align routes the tokens itself
+ *                         (up to 256 tokens, 128 experts): no separate route launch */
 typedef struct moe_lora_layer_plan_t {
   int32_t bm_base;
   int32_t bm_lora;
@@ -361,6 +364,7 @@ typedef struct moe_lora_layer_plan_t {
   int32_t fused_expand;
   int32_t launches;
   int32_t early_reads;
+  int32_t route_in_align;
 } moe_lora_layer_plan_t;
 
 MOE_LORA_API int moe_lora_layer_plan(int T, int k, int E, int L, int H, int I, int r,

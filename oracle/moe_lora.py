@@ -7,12 +7,12 @@ helper with the CUDA path.
 Sources (the pages describing vLLM's multi-LoRA serving for MoE models):
 
 * "vLLM Multi-LoRA Serving for MoE Models" (agentlenshq.com), section
-  "Multi-LoRA Serving for MoE Models": a router sends each token to experts;
-  each expert expands with a gate_up projection and compresses with a down
-  projection; LoRA adds a shrink and an expand op to each projection.
+  "Multi-LoRA Serving for MoE Models": tokens are routed to experts; every
+  expert has a gate_up and a down projection, and LoRA gives each projection a
+  shrink op and an expand op.
 * vLLM blog "multi-LoRA for MoE" (vllm.com.cn), section "Implementing
-  multi-LoRA inference for MoE models in vLLM": the router sends each token to
-  its most relevant experts and aggregates their outputs; for a projection with
+  multi-LoRA inference for MoE models in vLLM": each token goes to its top-k
+  experts, whose outputs are summed with the routing weights; for a projection with
   base weight W (h_in x h_out) LoRA trains A (h_in x r) and B (r x h_out) and
   the output is y = xW + xAB; shrink is z = xA, expand is zB; each expert
   carries four LoRA ops (gate_up shrink/expand, down shrink/expand); tokens
@@ -87,7 +87,7 @@ def swiglu(g: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# Routing: the router sends each token to its most relevant experts.
+# Routing: each token's top-k experts and their softmax weights.
 # ----------------------------------------------------------------------------
 def route_topk_softmax(logits, k: int):
     """Top-k experts per token and their softmax weights.

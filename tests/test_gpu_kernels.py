@@ -229,6 +229,35 @@ def test_shrink_many_blocks(r, T):
     assert_close(Z, oracle.lora_shrink(inp.x, inp.A1, ref, False), KERNEL_RTOL, f"shrink r={r}")
 
 
+@pytest.mark.parametrize("form", ["by_token", "sorted_rows", "ranked"])
+@pytest.mark.parametrize("K,r", [(2880, 16), (2880, 32), (1032, 16), (1032, 24), (1032, 32)])
+def test_shrink_pipelined(K, r, form):
+    """Many blocks of up to 16 rows with long sums (prefill): the shrink that streams A and
+    x through a ring of shared-memory stages by bulk copies. K = 1032 leaves an 8-column
+    last stage; r = 24 half uses its second rank group's rows; adapters of their own ranks
+    with NaN past them (never read); activations by token or in sorted-row order."""
+    m, inp, ids, w, al, ref = _setup(T=3328, H=K, I=8, E=4, k=4, L=8, r=r, seed=31, bm_lora=16)
+    assert len(ref["lora_blocks"]) > 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    if form == "sorted_rows":
+        n = ref["n_valid"]
+        rng = np.random.default_rng(3)
+        h = torch.from_numpy(rng.standard_normal((al.S, K), dtype=np.float32)).to(torch.bfloat16)
+        Z = m.lora_shrink(dev(h), True, dev(inp.A1), al)
+        expect = oracle.lora_shrink(h[:n], inp.A1, ref, rows_are_slots=True)
+    elif form == "ranked":
+        ranks = [[8, 0, 5, 16, r][l % 5] for l in range(8)]
+        A = _poison_A(inp.A1, ranks, r)
+        rk = torch.as_tensor(ranks, dtype=torch.int32)
+        Z = m.lora_shrink(dev(inp.x), False, dev(A), al, adapter_ranks=dev(rk))
+        expect = oracle.lora_shrink(inp.x, A, ref, False, adapter_ranks=rk)
+        assert not torch.isnan(Z).any()
+    else:
+        Z = m.lora_shrink(dev(inp.x), False, dev(inp.A1), al)
+        expect = oracle.lora_shrink(inp.x, inp.A1, ref, False)
+    assert_close(Z, expect, KERNEL_RTOL, f"pipelined shrink K={K} r={r} {form}")
+    assert m.get_error(al.buf) == 0
+
+
 @pytest.mark.parametrize("r", [32, 5])
 def test_expand_short_segments(r):
     """Decode-like routing: about one row per (expert, adapter) pair; the SwiGLU expand walks
