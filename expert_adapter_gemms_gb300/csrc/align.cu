@@ -598,7 +598,7 @@ static int launch_align_t(const int* ids, const int* token_adapter, const moe_lo
 }
 
 bool align_can_route(const AlignLayout& a, int T, int E) {
-  return a.ctas == 0 && a.S <= 4096 && T <= kAlignRouteMaxTokens && E <= 128;
+  return a.ctas == 0 && a.S <= 4096 && T <= kAlignRouteMaxTokens && E <= 64;
 }
 
 int launch_route_align(const float* logits, int* ids, float* w, const int* token_adapter,
@@ -606,8 +606,7 @@ int launch_route_align(const float* logits, int* ids, float* w, const int* token
                        bool pdl) {
   if (!align_can_route(a, al->T, al->E)) return MOE_LORA_ERR_UNSUPPORTED;
   if (al->E <= 32) return launch_align_t<256, 1>(ids, token_adapter, al, a, stream, pdl, logits, w);
-  if (al->E <= 64) return launch_align_t<256, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
-  return launch_align_t<256, 4>(ids, token_adapter, al, a, stream, pdl, logits, w);
+  return launch_align_t<256, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
 }
 
 int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,

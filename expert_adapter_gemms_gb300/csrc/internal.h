@@ -11,7 +11,7 @@ int launch_topk_softmax(const float* logits, int T, int E, int k, int* ids, floa
 
 // The one-CTA align routing the tokens itself (few tokens): ids and w are written by the
 // same launch. align_can_route tells where it applies.
-constexpr int kAlignRouteMaxTokens = 256;
+constexpr int kAlignRouteMaxTokens = 64;
 bool align_can_route(const AlignLayout& a, int T, int E);
 int launch_route_align(const float* logits, int* ids, float* w, const int* token_adapter,
                        const moe_lora_align_t* al, const AlignLayout& a, cudaStream_t stream,

@@ -356,7 +356,7 @@ MOE_LORA_API int moe_lora_layer_tiles(int T, int k, int E, int L, int H, int I, 
  *                         own wait, so the producer has completed when the reader starts; a
  *                         chain that broke this would be refused (MOE_LORA_ERR_UNSUPPORTED).
  *   route_in_align        1: routed from logits, the one-CTA align routes the tokens itself
- *                         (up to 256 tokens, 128 experts): no separate route launch */
+ *                         (up to 64 tokens, 64 experts): no separate route launch */
 typedef struct moe_lora_layer_plan_t {
   int32_t bm_base;
   int32_t bm_lora;

@@ -94,7 +94,7 @@ def test_reference_arm_line(capsys):
 def test_launch_accounting_matches_the_plan():
     """gpu_launches counts kernels per layer call from the library's own plan (host only):
     with the expand fused into the grouped GEMMs, route (folded into the one-CTA align up
-    to 256 tokens), align (one CTA; three kernels from 2048 slots), gather, two shrinks,
+    to 64 tokens), align (one CTA; three kernels from 2048 slots), gather, two shrinks,
     two grouped GEMMs and the combine."""
     from types import SimpleNamespace
     import expert_adapter_gemms_gb300 as m
