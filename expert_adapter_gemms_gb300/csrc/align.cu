@@ -213,9 +213,10 @@ __global__ void __launch_bounds__(NT, 1)
   pdl_trigger();
   pdl_wait();
   if (tid == 0) s_err = 0u;
-  if constexpr (V > 0) {  // 0. routing, one warp per token (its ids are read back below):
-    // eight of a warp's tokens at once, their logits in flight and their selections side
-    // by side
+  // routed here: the ids also stay in shared memory for the keys (T k <= 64 * 32 slots)
+  __shared__ int s_rid[V > 0 ? kAlignRouteMaxTokens * 32 : 1];
+  if constexpr (V > 0) {  // 0. routing, one warp per token: eight of a warp's tokens at
+    // once, their logits in flight and their selections side by side
     constexpr int TB = 8;
     int* ids_out = const_cast<int*>(ids);
     for (int t0 = warp; t0 < T; t0 += NW * TB) {
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int i = 0; i < V; ++i) lv[b][i] = -INFINITY;
       }
-      topk_softmax_select<V, TB>(lv, tok, E, k, ids_out, w_out);
+      topk_softmax_select<V, TB>(lv, tok, E, k, ids_out, w_out, s_rid);
     }
   }
   __syncthreads();
@@ -244,7 +245,8 @@ __global__ void __launch_bounds__(NT, 1)
       ev[u] = 0;
       lv[u] = -1;
       if (s < S) {
-        ev[u] = __ldcg(ids + s);
+        if constexpr (V > 0) ev[u] = s_rid[s];
+        else ev[u] = __ldcg(ids + s);
         if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
       }
     }
@@ -488,11 +490,21 @@ __global__ void __launch_bounds__(NT)
     if (b < nbuckets) {
       v.bucket_start[b] = run;
       v.bucket_count[b] = tot;
-      for (int c = 0; c < ctas; ++c) {
-        int* p = v.counts + (size_t)c * nbuckets + b;
-        const int cnt = __ldcg(p);
-        *p = run;
-        run += cnt;
+      // sixteen counts are loaded before their offsets are stored (a load after a store
+      // that may alias it would wait for it: one round trip per CTA)
+      constexpr int CB = 16;
+      for (int c0 = 0; c0 < ctas; c0 += CB) {
+        int cnt[CB];
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+          cnt[u] = c0 + u < ctas ? __ldcg(v.counts + (size_t)(c0 + u) * nbuckets + b) : 0;
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+          if (c0 + u < ctas) {
+            v.counts[(size_t)(c0 + u) * nbuckets + b] = run;
+            run += cnt[u];
+          }
+        }
       }
     }
     carry += tile_total;

@@ -69,7 +69,9 @@ __device__ __forceinline__ void zpad_put(const ZPadOut& o, int row, int e, int l
 
 // Run by the CTA of rank group 0 of a LoRA block: the zero columns [r, rp16) of its rows
 // in both halves and, for the first (last) block of its pair, the `gap` zero rows before
-// (after) the pair, which a fused-expand tile reads for its rows of other pairs.
+// (after) the pair, which a fused-expand tile reads for its rows of other pairs. When the
+// rows just before belong to the pair of the previous key, that pair's trailing gap is
+// this pair's leading gap (the shifts differ by one gap): it is written once, there.
 __device__ void zpad_extras(const ZPadOut& o, const int* hdr, int row0, int rows, int e, int l,
                             int r) {
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -84,8 +86,13 @@ __device__ void zpad_extras(const ZPadOut& o, const int* hdr, int row0, int rows
   }
   const int n_valid = __ldcg(hdr + HDR_NVALID);
   const int end = row0 + rows;
-  const bool first = row0 == 0 || __ldcg(o.row_expert + row0 - 1) != e ||
-                     __ldcg(o.row_adapter + row0 - 1) != l;
+  bool first = true;
+  if (row0 > 0) {
+    const int pe = __ldcg(o.row_expert + row0 - 1), pl = __ldcg(o.row_adapter + row0 - 1);
+    // a new pair starts here; its leading gap is written unless the previous pair is the
+    // previous key's (whose trailing gap it is)
+    first = (pe != e || pl != l) && !(pl >= 0 && pe * o.L + pl + 1 == e * o.L + l);
+  }
   const bool last = end >= n_valid || __ldcg(o.row_expert + end) != e ||
                     __ldcg(o.row_adapter + end) != l;
   const int groups = o.gap * (o.zw / 8);  // 16-byte groups of `gap` rows
@@ -394,15 +401,15 @@ __global__ void __launch_bounds__(kShrinkWarps * 32, 4)
 // Here the block's rank rows of A and its x rows go through a ring of shared-memory
 // stages (256 columns, 512 bytes a row) filled by 16-byte asynchronous copies
 // (cp.async: the load path, no registers held while in flight; the bulk-copy engine
-// was measured slower for these 512-byte pieces), three stages ahead; four warps form the
-// same mma.sync products from shared memory (warp w takes k-steps w and w + 4 of each
-// stage) and the partials are reduced in warp order. Rows past the block and rank rows
+// was measured slower for these 512-byte pieces), three stages ahead; eight warps form the
+// same mma.sync products from shared memory (warp w takes k-step w of each stage) and the
+// partials are reduced in warp order. Rows past the block and rank rows
 // past the adapter's rank are not copied: their stale stage contents only reach outputs
 // that are not stored (masked ranks are written as zero).
 // ----------------------------------------------------------------------------
 constexpr int kPipeKC = 256;                  // columns per stage
 constexpr int kPipeRow = kPipeKC * 2 + 64;    // bytes per stage row: == 64 (mod 128)
-constexpr int kPipeWarps = 4;
+constexpr int kPipeWarps = 8;  // one 32-column k-step of each stage a warp
 constexpr int kPipeStages = 4;
 __host__ __device__ constexpr size_t pipe_smem(int R) {
   return (size_t)kPipeStages * (R + 16) * kPipeRow + (R + 16) * sizeof(void*);
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32, NT <= 2 ? 3 : 2)
     const uint8_t* st = smem + (size_t)(c % NS) * ROWS * kPipeRow;
     const int cols = min(kPipeKC, K - c * kPipeKC);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kPipeKC / 32 / kPipeWarps; ++h) {
       const int s0 = (warp + kPipeWarps * h) * 32;  // the warp's k-step in the stage
       if (s0 >= cols) continue;  // the whole warp: mma.sync needs all of its lanes
       // K % 8 == 0: a lane's 16-byte group is wholly in or out; out, it feeds zeros
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(kPipeWarps * 32, NT <= 2 ? 3 : 2)
   }
   cp_async_wait<0>();
   __syncthreads();  // every warp is done with the stages
-  // reduce the four warps' partials in warp order, in the first stage
+  // reduce the warps' partials in warp order, in the first stage
   float (*red)[16][R + 1] = reinterpret_cast<float (*)[16][R + 1]>(smem);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {

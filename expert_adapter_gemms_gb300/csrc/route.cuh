@@ -23,12 +23,14 @@ __device__ __forceinline__ void topk_softmax_load(const float* __restrict__ lrow
 }
 
 // The choice from loaded logits for TB tokens at once: token b (tok[b] >= 0) writes choice
-// j < k to ids[tok[b] k + j] and w[tok[b] k + j]. Each token takes exactly the steps of a
-// single token; running TB of them side by side lets their dependent shuffle chains overlap.
+// j < k to ids[tok[b] k + j] and w[tok[b] k + j] (and, given, ids_copy[tok[b] k + j]).
+// Each token takes exactly the steps of a single token; running TB of them side by side
+// lets their dependent shuffle chains overlap.
 template <int V, int TB>
 __device__ __forceinline__ void topk_softmax_select(const float (&vin)[TB][V], const int (&tok)[TB],
                                                     int E, int k, int* __restrict__ ids,
-                                                    float* __restrict__ w) {
+                                                    float* __restrict__ w,
+                                                    int* ids_copy = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[TB][V];
   uint32_t taken[TB];  // bit i: expert lane + 32 i chosen already or out of range
@@ -108,6 +110,7 @@ __device__ __forceinline__ void topk_softmax_select(const float (&vin)[TB][V], c
     if (tok[b] >= 0 && lane < k) {
       ids[(size_t)tok[b] * k + lane] = sel_id[b];
       w[(size_t)tok[b] * k + lane] = ex[b] / sum[b];
+      if (ids_copy) ids_copy[(size_t)tok[b] * k + lane] = sel_id[b];
     }
   }
 }
