@@ -171,3 +171,40 @@ def test_align_multi_cta_cases():
     _check_align(m, np.full((2048, 2), 1), np.full(2048, 0), 4, 2, 256, 16)
     # exactly four full CTAs, no adapters
     _check_align(m, rng.integers(0, 32, size=(512, 4)), None, 32, 0, 128, 16)
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_decode", "tiny"])
+def test_align_routes_in_layer(name):
+    """Up to 64 tokens the layer's one-CTA align routes the tokens itself (no route
+    launch): the align tables it leaves at the start of the workspace -- the stable sort
+    of the routed slots by (expert, adapter, slot), tiles and LoRA blocks -- equal the
+    oracle's routing and alignment, bit for bit; so do the routing weights the combine
+    read (y against the layer with the route kernel's ids and weights passed in)."""
+    m = need_gpu()
+    from workloads import make_workload_inputs
+    inp = make_workload_inputs(name)
+    plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    assert plan["route_in_align"] == 1, plan
+    lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
+    ws = m.new_workspace(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
+    args = (dev(inp.x), dev(inp.W1), dev(inp.W2))
+    y = m.moe_lora_layer(*args, logits=dev(inp.logits), k=inp.k, token_adapter=dev(inp.token_adapter),
+                         workspace=ws, y_fp32=True, **lora)
+    torch.cuda.synchronize()
+    al = m.Align(ws, inp.T, inp.k, inp.E, inp.L, plan["bm_base"], plan["bm_lora"])
+    ids, w = oracle.route_topk_softmax(inp.logits, inp.k)
+    ids_t = torch.as_tensor(np.asarray(ids), dtype=torch.int32)
+    ref = oracle.align(ids_t, inp.token_adapter, inp.E, inp.L, plan["bm_base"], plan["bm_lora"])
+    h = al.header()
+    n = ref["n_valid"]
+    assert h["err"] == 0 and h["n_valid"] == n
+    assert al.sorted_slots().cpu().numpy().tolist() == ref["sorted_slots"].tolist()
+    assert al.expert_begin().cpu().numpy().tolist() == ref["expert_begin"].tolist()
+    assert al.row_adapter().cpu().numpy()[:n].tolist() == ref["row_adapter"].tolist()
+    blocks = al.lora_blocks().cpu().numpy()[: h["n_lora_blocks"]].tolist()
+    assert blocks == [list(b) for b in ref["lora_blocks"]]
+    # the same layer fed the route kernel's ids and weights: identical y
+    rid, rw = m.moe_topk_softmax(dev(inp.logits), inp.k)
+    y2 = m.moe_lora_layer(*args, topk_ids=rid, topk_w=rw, token_adapter=dev(inp.token_adapter),
+                          y_fp32=True, **lora)
+    assert torch.equal(y, y2)
