@@ -2,7 +2,9 @@
 
 Every mbarrier wait in the grouped GEMMs (and in the short-K shrink) gives up after a
 wall-time limit, records MOE_LORA_DEVERR_TIMEOUT in the sticky error word, drains its
-CTA's copies and tensor-core work, frees its tensor memory and exits. The test makes the
+CTA's copies and tensor-core work, frees its tensor memory and exits; a CTA pair (the
+fused GEMM at 256-row token tiles) also mirrors the abort into the other CTA and meets
+it at cluster barriers before either frees anything. The test makes the
 main waits give up at their first unsuccessful poll (wait_limit_ns < 0), reads the
 status through moe_lora_get_error, then clears the word and checks that the next normal
 call on the same workspace matches the oracle: the context stays usable.
@@ -24,13 +26,15 @@ DEVERR_TIMEOUT = 0x4
 
 
 @pytest.mark.parametrize("expand_mode", [0, 1])
-@pytest.mark.parametrize("shape", ["small", "many_adapters"])
+@pytest.mark.parametrize("shape", ["small", "many_adapters", "cta_pairs"])
 def test_bounded_waits_give_up_and_recover(expand_mode, shape):
     m = need_gpu()
     if shape == "small":
         kw = dict(T=16, H=256, I=128, E=4, k=2, L=2, r=16)
-    else:  # many short LoRA blocks and K <= 832: the down shrink stages A in shared memory
-        kw = dict(T=256, H=256, I=128, E=64, k=8, L=32, r=32, adapters="zipf1.1")
+    elif shape == "many_adapters":  # many short LoRA blocks and K <= 832: the down shrink
+        kw = dict(T=256, H=256, I=128, E=64, k=8, L=32, r=32, adapters="zipf1.1")  # stages A
+    else:  # 256-row token tiles: the fused chain's GEMMs run on CTA pairs (cluster barriers,
+        kw = dict(T=800, H=256, I=128, E=3, k=2, L=2, r=16)  # copies on the leader's barriers)
     inp = make_layer_inputs(seed=41, lora_std=None, **kw)
     lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
     args = (dev(inp.x), dev(inp.W1), dev(inp.W2))

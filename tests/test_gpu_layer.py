@@ -443,3 +443,24 @@ def test_layer_host_staged(name, with_adapter, y_fp32):
     no_adapter = np.full(inp.T, -1, dtype=np.int32)
     ref = oracle_layer(inp, tokens, token_adapter=None if with_adapter else no_adapter)
     assert_close(y_host[tokens], ref, LAYER_RTOL, f"host-staged {name}")
+
+
+@pytest.mark.parametrize("y_fp32", [True, False])
+def test_layer_output_any_alignment(y_fp32):
+    """y is a caller buffer with no alignment rule: one offset by a single element (4- or
+    2-byte aligned) takes the combine's scalar form instead of its 16-byte one, with the
+    same sums in the same order, so the same bits."""
+    m = need_gpu()
+    inp = make_workload_inputs("gptoss20b_decode")
+    dt = torch.float32 if y_fp32 else torch.bfloat16
+    lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
+    args = (dev(inp.x), dev(inp.W1), dev(inp.W2))
+    kw = dict(logits=dev(inp.logits), k=inp.k, token_adapter=dev(inp.token_adapter),
+              y_fp32=y_fp32, **lora)
+    y = m.moe_lora_layer(*args, **kw)
+    raw = torch.zeros(inp.T * inp.H + 1, dtype=dt, device="cuda")
+    y_odd = raw[1:].view(inp.T, inp.H)
+    assert y_odd.data_ptr() % 16 != 0
+    m.moe_lora_layer(*args, y=y_odd, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_odd)
