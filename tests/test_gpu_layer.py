@@ -99,13 +99,14 @@ def test_fused_chain_is_picked_where_it_applies():
 
 @pytest.mark.parametrize("shape", ["r8_expert_major", "r24_expert_major", "r64_chunked",
                                    "r128_chunked", "tiles_many_runs", "persistent_r32",
-                                   "base_only_tiles"])
+                                   "base_only_tiles", "expert_major_k_tail"])
 def test_fused_expand_shapes(shape):
     """The fused chain on shapes that exercise its cases: ranks that need zero padding to a
     multiple of 16 (8, 24), ranks whose high and low z parts take separate 64-column chunks
     (64, 128), expert-major chunks, token tiles holding many adapter runs (one adapter per
-    request of 64 tokens), persistent 128-row tiles, and no adapters at all. Every token is
-    compared with the oracle and with the chain of separate expand kernels."""
+    request of 64 tokens), persistent 128-row tiles, no adapters at all, and expert-major
+    64-row chunks with a K tail. Every token is compared with the oracle and with the chain
+    of separate expand kernels."""
     m = need_gpu()
     kw = {"r8_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=8),
           "r24_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=24),
@@ -114,7 +115,10 @@ def test_fused_expand_shapes(shape):
           "tiles_many_runs": dict(T=1024, H=256, I=256, E=8, k=2, L=16, r=16,
                                   adapters="one_per_request16"),
           "persistent_r32": dict(T=700, H=128, I=256, E=4, k=2, L=3, r=32),
-          "base_only_tiles": dict(T=300, H=256, I=192, E=4, k=2, L=0, r=16)}[shape]
+          "base_only_tiles": dict(T=300, H=256, I=192, E=4, k=2, L=0, r=16),
+          # 64-row chunks (experts of more than 32 rows) and K = 200: the last 64-column
+          # stage has 8 columns, the rest read as zeros
+          "expert_major_k_tail": dict(T=64, H=200, I=96, E=4, k=2, L=3, r=16)}[shape]
     inp = make_layer_inputs(seed=120 + len(shape), lora_std=None, **kw)
     plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
     assert plan["fused_expand"] == 1, plan
