@@ -35,7 +35,10 @@
 // of rows with an adapter in the tile; their MMAs stop at the run's last row. Warp roles
 // (a TMA producer, one MMA-issuing thread, four epilogue warps), TMEM double buffering,
 // bounded waits and the work decompositions (expert-major, per tile, persistent) follow
-// the plain grouped GEMM.
+// the plain grouped GEMM; token-tile jobs go expert by expert, weight block by weight
+// block over groups of the expert's tiles, so a weight block is read from memory about
+// once. At 256-row tiles a cluster of two CTAs computes each job as one
+// tcgen05.mma.cta_group::2 of M = 256 (kPair).
 #include <algorithm>
 #include <atomic>
 
