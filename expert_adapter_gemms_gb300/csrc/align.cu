@@ -3,7 +3,7 @@
 // multi-LoRA inference for MoE models in vLLM"; agentlenshq.com, section
 // "Multi-LoRA Serving for MoE Models").
 //
-// One CTA (256 threads up to 4096 slots, 1024 beyond). Each slot s gets the
+// One CTA (1024 threads up to 512 slots, 256 up to 4096, 1024 beyond). Each slot s gets the
 // packed word (key << slot_bits) | s with key = e * (L + 1) + (l + 1) (dropped
 // slots use the last bucket). A stable least-significant-digit radix sort on the
 // key bits (8-bit digits, per-warp digit histograms, ranks inside a warp from
@@ -146,16 +146,36 @@ __device__ uint32_t* block_radix_sort(uint32_t* a, uint32_t* b, int n, int lo, i
 // The words are unique ((key, slot) with distinct slots), so the stable key order of the
 // radix sort is their ascending order, and a word's place is the number of smaller words:
 // for a few hundred words one pass of broadcast shared-memory reads per thread, without
-// the radix sort's barriers. The same result, bit for bit.
-template <int NT>
-__device__ uint32_t* block_rank_sort(const uint32_t* a, uint32_t* b, int n) {
-  for (int i = threadIdx.x; i < n; i += NT) {
+// the radix sort's barriers. The same result, bit for bit. P lanes of a warp share a word
+// (as many as the threads allow, up to 8), each counting over every P-th 16-byte group of
+// words (P consecutive groups per step: one wavefront), and add their counts with
+// shuffles inside the group. The buffer is padded to whole groups with all-ones words,
+// which are smaller than no word.
+template <int NT, int P>
+__device__ void rank_place(const uint32_t* a, uint32_t* b, int n) {
+  const int lane = threadIdx.x & 31, part = lane & (P - 1);
+  const unsigned group = ((1u << P) - 1u) << (lane & ~(P - 1));  // the word's P lanes
+  const uint4* a4 = reinterpret_cast<const uint4*>(a);
+  const int n4 = (n + 3) >> 2;
+  for (int i = threadIdx.x / P; i < n; i += NT / P) {  // the same i for a group's lanes
     const uint32_t x = a[i];
     int pos = 0;
-#pragma unroll 8
-    for (int j = 0; j < n; ++j) pos += a[j] < x ? 1 : 0;
-    b[pos] = x;
+#pragma unroll 4
+    for (int q = part; q < n4; q += P) {
+      const uint4 y = a4[q];
+      pos += (y.x < x ? 1 : 0) + (y.y < x ? 1 : 0) + (y.z < x ? 1 : 0) + (y.w < x ? 1 : 0);
+    }
+#pragma unroll
+    for (int o = 1; o < P; o <<= 1) pos += __shfl_xor_sync(group, pos, o);
+    if (part == 0) b[pos] = x;
   }
+}
+template <int NT>
+__device__ uint32_t* block_rank_sort(const uint32_t* a, uint32_t* b, int n) {
+  if (8 * n <= NT) rank_place<NT, 8>(a, b, n);
+  else if (4 * n <= NT) rank_place<NT, 4>(a, b, n);
+  else if (2 * n <= NT) rank_place<NT, 2>(a, b, n);
+  else rank_place<NT, 1>(a, b, n);
   __syncthreads();
   return b;
 }
@@ -173,7 +193,8 @@ __host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nt
   p.hist_off = 0;
   p.tmp_off = 256 * (nw + 1);
   int o = p.tmp_off + 64;
-  const size_t sort_b = (size_t)2 * S * 4;
+  const int S4 = (S + 3) & ~3;  // each sort buffer in whole 16-byte groups
+  const size_t sort_b = (size_t)2 * S4 * 4;
   const size_t bucket_b = (size_t)2 * nbuckets * 4;
   p.smem_sort = S <= kSmemSortMaxSlots;
   const size_t base = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
@@ -181,6 +202,7 @@ __host__ __device__ inline AlignSmem align_smem_plan(int S, int nbuckets, int nt
   p.bcount_off = o;
   p.bstart_off = o + (p.smem_buckets ? nbuckets : 0);
   o = p.bstart_off + (p.smem_buckets ? nbuckets : 0);
+  o = (o + 3) & ~3;
   p.sort_off = o;
   p.bytes = (size_t)o * 4 + (p.smem_sort ? sort_b : 0);
   return p;
@@ -202,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1)
   int* bcount = plan.smem_buckets ? smem + plan.bcount_off : v.bucket_count;
   int* bstart = plan.smem_buckets ? smem + plan.bstart_off : v.bucket_start;
   uint32_t* bufA = plan.smem_sort ? reinterpret_cast<uint32_t*>(smem + plan.sort_off) : v.sort0;
-  uint32_t* bufB = plan.smem_sort ? bufA + S : v.sort1;
+  uint32_t* bufB = plan.smem_sort ? bufA + ((S + 3) & ~3) : v.sort1;
   __shared__ unsigned int s_err;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -213,11 +235,19 @@ __global__ void __launch_bounds__(NT, 1)
   pdl_trigger();
   pdl_wait();
   if (tid == 0) s_err = 0u;
+  // routing here: the adapter ids of this thread's first four slots, in flight with the
+  // logits
+  int lv0[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int s = tid + u * NT;
+    lv0[u] = V > 0 && token_adapter && s < S ? __ldcg(token_adapter + s / k) : -1;
+  }
   // routed here: the ids also stay in shared memory for the keys (T k <= 64 * 32 slots)
   __shared__ int s_rid[V > 0 ? kAlignRouteMaxTokens * 32 : 1];
-  if constexpr (V > 0) {  // 0. routing, one warp per token: eight of a warp's tokens at
-    // once, their logits in flight and their selections side by side
-    constexpr int TB = 8;
+  if constexpr (V > 0) {  // 0. routing, one warp per token: TB of a warp's tokens at
+    // once (64 tokens in one round), their logits in flight and their selections side by side
+    constexpr int TB = NT >= 1024 ? 2 : 8;
     int* ids_out = const_cast<int*>(ids);
     for (int t0 = warp; t0 < T; t0 += NW * TB) {
       float lv[TB][V];
@@ -247,7 +277,8 @@ __global__ void __launch_bounds__(NT, 1)
       if (s < S) {
         if constexpr (V > 0) ev[u] = s_rid[s];
         else ev[u] = __ldcg(ids + s);
-        if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
+        if (V > 0 && s0 == tid) lv[u] = lv0[u];
+        else if (token_adapter) lv[u] = __ldcg(token_adapter + s / k);
       }
     }
 #pragma unroll
@@ -264,6 +295,7 @@ __global__ void __launch_bounds__(NT, 1)
       bufA[s] = (static_cast<uint32_t>(key) << slot_bits) | static_cast<uint32_t>(s);
     }
   }
+  if (plan.smem_sort && tid < ((S + 3) & ~3) - S) bufA[S + tid] = 0xffffffffu;  // group padding
   __syncthreads();
 
   // 2. stable LSD radix sort on the key bits (8-bit digits)
@@ -340,10 +372,21 @@ __global__ void __launch_bounds__(NT, 1)
     nb += __popc(__ballot_sync(0xffffffffu, fb));
     nl += __popc(__ballot_sync(0xffffffffu, fl));
   }
-  int tot_t, tot_b, tot_l;
-  int ti = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nt : 0, tmp, &tot_t), 0);
-  int bi = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nb : 0, tmp, &tot_b), 0);
-  block_exclusive_scan<NW>(lane == 0 ? nl : 0, tmp, &tot_l);
+  int tot_t, tot_b, tot_l, ti, bi;
+  if (S < 1024) {  // the three counts (each <= S) in 10-bit fields of one scan
+    int tot;
+    const int pre = __shfl_sync(
+        0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nt | nb << 10 | nl << 20 : 0, tmp, &tot), 0);
+    ti = pre & 1023;
+    bi = (pre >> 10) & 1023;
+    tot_t = tot & 1023;
+    tot_b = (tot >> 10) & 1023;
+    tot_l = tot >> 20;
+  } else {
+    ti = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nt : 0, tmp, &tot_t), 0);
+    bi = __shfl_sync(0xffffffffu, block_exclusive_scan<NW>(lane == 0 ? nb : 0, tmp, &tot_b), 0);
+    block_exclusive_scan<NW>(lane == 0 ? nl : 0, tmp, &tot_l);
+  }
   for (int base = wb5; base < we5; base += 32) {
     const int i = base + lane;
     int e, l, key;
@@ -617,6 +660,11 @@ int launch_route_align(const float* logits, int* ids, float* w, const int* token
                        const moe_lora_align_t* al, const AlignLayout& a, cudaStream_t stream,
                        bool pdl) {
   if (!align_can_route(a, al->T, al->E)) return MOE_LORA_ERR_UNSUPPORTED;
+  // the rank sort's words: 1024 threads (two tokens a warp, up to four lanes a word); the
+  // radix sort's: 256, whose barriers are cheaper
+  if (a.S <= kRankSortMaxSlots)
+    return al->E <= 32 ? launch_align_t<1024, 1>(ids, token_adapter, al, a, stream, pdl, logits, w)
+                       : launch_align_t<1024, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
   if (al->E <= 32) return launch_align_t<256, 1>(ids, token_adapter, al, a, stream, pdl, logits, w);
   return launch_align_t<256, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
 }
@@ -634,7 +682,9 @@ int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_
     return launch_pdl(align_place_kernel<256>, a.ctas, 256, 0, stream, pdl, v, al->L, a.S,
                       a.nbuckets, a.slot_bits, a.ctas);
   }
-  // few slots: a small CTA keeps the many barriers of the sort cheap
+  // few slots: the rank sort spreads over 1024 threads; up to 4096, a small CTA keeps the
+  // many barriers of the radix sort cheap
+  if (a.S <= kRankSortMaxSlots) return launch_align_t<1024, 0>(ids, token_adapter, al, a, stream, pdl);
   if (a.S <= 4096) return launch_align_t<256, 0>(ids, token_adapter, al, a, stream, pdl);
   return launch_align_t<1024, 0>(ids, token_adapter, al, a, stream, pdl);
 }

@@ -83,9 +83,10 @@ int launch_fused_gemm(const void* a_sorted, const void* W, const void* B, const 
 
 // y[t] = sum_j w[t, j] O[row(t, j)] (j ascending) over O [S, N] fp32 by sorted row; with
 // nparts > 1, O holds nparts partial outputs part_stride elements apart, summed in order.
+// early: the slot rows and the weights are read before griddepcontrol.wait.
 int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
                    const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl,
-                   int nparts = 1, size_t part_stride = 0);
+                   int nparts = 1, size_t part_stride = 0, bool early = false);
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,
                   int N, int r, int epilogue, float* base, void* out, int out_fp32,

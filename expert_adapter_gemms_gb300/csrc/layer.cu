@@ -267,6 +267,7 @@ static Chain layer_chain(const LayerPlan& p, int T, int k, int E, int L, bool ha
     add(kGemm2, 1, true);
     if (lora) reads(kGemm2, kGemm1, kAlign);    // h, tables; z only after the wait
     add(kCombine, 1, true);
+    reads(kCombine, kAlign, kRoute);            // slot rows, routing weights
     return c;
   }
   const bool em = p.em_bn > 0;
@@ -511,7 +512,7 @@ extern "C" int moe_lora_layer_ex(const void* x, const float* logits, const int32
                               o.mma_pairs >= 0));
     ML_STEP(mark(8));
     ML_STEP(launch_combine(O, w, &al, p.al, H, y, y_fp32, stream, pdl, p.ksplit,
-                           (size_t)T * k * H));
+                           (size_t)T * k * H, ch.early(kCombine)));
     ML_STEP(mark(9));
     return MOE_LORA_OK;
   }

@@ -774,7 +774,8 @@ __global__ void __launch_bounds__(kExpandThreads)
 // ----------------------------------------------------------------------------
 // Weighted top-k combine after an in-place expand over LoRA blocks:
 //   y[t, n] = sum_j w[t, j] * O[row(t, j), n], j ascending.
-// The CTA's slot rows and weights are staged in shared memory first; then each
+// The CTA's slot rows and weights are staged in shared memory first (with `early`,
+// before the wait: the align and the routing are two or more launches back); then each
 // thread issues the O values of all of a token's slots (eight at a time) before
 // it sums them, in j order.
 // ----------------------------------------------------------------------------
@@ -782,18 +783,24 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(kExpandThreads)
     combine_kernel(const float* __restrict__ O, const float* __restrict__ w,
                    const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
-                   int tokens_per_cta, int nparts, size_t part_stride) {
+                   int tokens_per_cta, int nparts, size_t part_stride, int early) {
   constexpr int KM = 8;
   __shared__ int s_row[kExpandThreads];
   __shared__ float s_w[kExpandThreads];
-  pdl_wait();
-  pdl_trigger();
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int t0 = blockIdx.x * tokens_per_cta;
   const int t1 = min(T, t0 + tokens_per_cta);
   const int ns = (t1 - t0) * k;  // the host keeps tokens_per_cta * k <= 256
   for (int i = threadIdx.x; i < ns; i += blockDim.x) {
     s_row[i] = __ldcg(slot_row + (size_t)t0 * k + i);
     s_w[i] = __ldcg(w + (size_t)t0 * k + i);
+  }
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
   }
   __syncthreads();
   const int n = blockIdx.y * kExpandThreads + threadIdx.x;
@@ -832,18 +839,24 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(kExpandThreads)
     combine4_kernel(const float* __restrict__ O, const float* __restrict__ w,
                     const int* __restrict__ slot_row, int T, int k, int N, void* __restrict__ y,
-                    int tokens_per_cta, int nparts, size_t part_stride) {
+                    int tokens_per_cta, int nparts, size_t part_stride, int early) {
   constexpr int KM = 8;
   __shared__ int s_row[kExpandThreads];
   __shared__ float s_w[kExpandThreads];
-  pdl_wait();
-  pdl_trigger();
+  if (!early) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int t0 = blockIdx.x * tokens_per_cta;
   const int t1 = min(T, t0 + tokens_per_cta);
   const int ns = (t1 - t0) * k;  // the host keeps tokens_per_cta * k <= 256
   for (int i = threadIdx.x; i < ns; i += blockDim.x) {
     s_row[i] = __ldcg(slot_row + (size_t)t0 * k + i);
     s_w[i] = __ldcg(w + (size_t)t0 * k + i);
+  }
+  if (early) {
+    pdl_wait();
+    pdl_trigger();
   }
   __syncthreads();
   const int n = 4 * (blockIdx.y * kExpandThreads + threadIdx.x);
@@ -1126,8 +1139,9 @@ int launch_expand_impl(const float* Z, const void* B, const moe_lora_align_t* al
 
 int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* al,
                    const AlignLayout& a, int N, void* y, int y_fp32, cudaStream_t stream, bool pdl,
-                   int nparts, size_t part_stride) {
+                   int nparts, size_t part_stride, bool early) {
   if (a.S == 0 || al->T == 0) return MOE_LORA_OK;
+  const int ea = early ? 1 : 0;
   AlignView v = align_view(al->buf, a);
   const int sms = num_sms();
   // four columns a thread where the row width and y's address allow 16-byte (8-byte) access
@@ -1145,13 +1159,13 @@ int launch_combine(const float* O, const float* topk_w, const moe_lora_align_t* 
   const dim3 g2(ceil_div(al->T, tpc), ncol);
   if (vec)
     return y_fp32 ? launch_pdl(combine4_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride)
+                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride, ea)
                   : launch_pdl(combine4_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride);
+                               (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride, ea);
   return y_fp32 ? launch_pdl(combine_kernel<true>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride)
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride, ea)
                 : launch_pdl(combine_kernel<false>, g2, kExpandThreads, 0, stream, pdl, O, topk_w,
-                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride);
+                             (const int*)v.slot_row, al->T, al->k, N, y, tpc, nparts, part_stride, ea);
 }
 
 int launch_expand(const float* Z, const void* B, const moe_lora_align_t* al, const AlignLayout& a,

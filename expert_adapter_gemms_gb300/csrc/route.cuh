@@ -4,7 +4,6 @@
 // then the softmax over the chosen values. Shared by the routing kernel
 // and the one-CTA align that routes for itself, so both give the same bits.
 #pragma once
-#include <climits>
 
 #include "common.cuh"
 
@@ -22,10 +21,21 @@ __device__ __forceinline__ void topk_softmax_load(const float* __restrict__ lrow
   }
 }
 
+// The order of a logit as an unsigned key: a larger number gets a larger key, -0 and +0 the
+// same one, and every key of a number (-inf included) is above 0, the key of an expert
+// already chosen or out of range.
+__device__ __forceinline__ uint32_t topk_order_key(float x) {
+  if (x == 0.f) x = 0.f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // The choice from loaded logits for TB tokens at once: token b (tok[b] >= 0) writes choice
 // j < k to ids[tok[b] k + j] and w[tok[b] k + j] (and, given, ids_copy[tok[b] k + j]).
-// Each token takes exactly the steps of a single token; running TB of them side by side
-// lets their dependent shuffle chains overlap.
+// Choice j is the largest key not chosen before (one warp-wide integer max) and, among the
+// experts holding it, the lowest id (one ballot per value a lane holds): the k largest
+// logits with ties to the lower expert id, NaN below every number. Running TB tokens side
+// by side lets their dependent steps overlap.
 template <int V, int TB>
 __device__ __forceinline__ void topk_softmax_select(const float (&vin)[TB][V], const int (&tok)[TB],
                                                     int E, int k, int* __restrict__ ids,
@@ -33,20 +43,16 @@ __device__ __forceinline__ void topk_softmax_select(const float (&vin)[TB][V], c
                                                     int* ids_copy = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[TB][V];
-  uint32_t taken[TB];  // bit i: expert lane + 32 i chosen already or out of range
+  uint32_t key[TB][V];  // 0: chosen already or out of range
 #pragma unroll
   for (int b = 0; b < TB; ++b) {
-    taken[b] = 0;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = lane + 32 * i;
       float x = vin[b][i];
-      if (e < E) {
-        if (isnan(x)) x = -INFINITY;  // NaN ranks below every number
-      } else {
-        taken[b] |= 1u << i;
-      }
+      if (isnan(x)) x = -INFINITY;  // NaN ranks below every number
       v[b][i] = x;
+      key[b][i] = e < E ? topk_order_key(x) : 0u;
     }
   }
   float sel_val[TB];
@@ -57,39 +63,34 @@ __device__ __forceinline__ void topk_softmax_select(const float (&vin)[TB][V], c
     sel_id[b] = 0;
   }
   for (int j = 0; j < k; ++j) {
-    float bv[TB];
-    int bi[TB];
+    uint32_t m[TB];
 #pragma unroll
     for (int b = 0; b < TB; ++b) {
-      bv[b] = -INFINITY;
-      bi[b] = INT_MAX;
+      uint32_t lm = key[b][0];
+#pragma unroll
+      for (int i = 1; i < V; ++i) lm = max(lm, key[b][i]);
+      m[b] = __reduce_max_sync(0xffffffffu, lm);
+    }
+#pragma unroll
+    for (int b = 0; b < TB; ++b) {
+      // the lowest id e = lane + 32 i holding the maximum: the lowest i first, then lane
+      int win = -1;
+      float wv = 0.f;
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        const int e = lane + 32 * i;
-        if (!((taken[b] >> i) & 1u) && (v[b][i] > bv[b] || (v[b][i] == bv[b] && e < bi[b]))) {
-          bv[b] = v[b][i];
-          bi[b] = e;
+        const unsigned bal = __ballot_sync(0xffffffffu, key[b][i] == m[b]);
+        if (win < 0 && bal) {
+          const int src = __ffs(bal) - 1;
+          win = src + 32 * i;
+          wv = __shfl_sync(0xffffffffu, v[b][i], src);
         }
       }
-    }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) {
-#pragma unroll
-      for (int b = 0; b < TB; ++b) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv[b], off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi[b], off);
-        if (ov > bv[b] || (ov == bv[b] && oi < bi[b])) {
-          bv[b] = ov;
-          bi[b] = oi;
-        }
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < TB; ++b) {
-      if ((bi[b] & 31) == lane) taken[b] |= 1u << (bi[b] >> 5);
+      for (int i = 0; i < V; ++i)
+        if (win == lane + 32 * i) key[b][i] = 0u;
       if (lane == j) {
-        sel_val[b] = bv[b];
-        sel_id[b] = bi[b];
+        sel_val[b] = wv;
+        sel_id[b] = win;
       }
     }
   }

@@ -222,13 +222,15 @@ def test_chain_early_reads_come_from_completed_launches(L):
     and refuses a chain that breaks the rule; here every shape and option combination is
     planned and the number of checked reads is pinned per chain:
       fused, adapters: shrink1 <- align; GEMM1 <- gather, align; shrink2 <- align (its
-        block, before prefetching A); GEMM2 <- GEMM1, align = 6
+        block, before prefetching A); GEMM2 <- GEMM1, align; combine <- align, route
+        = 8 (7 where the align routes the tokens itself)
       separate expand, expert-major: shrink1 <- gather, align; expand1 <- GEMM1, align;
         shrink2 <- expand1, align; expand2 <- GEMM2, align, route = 9 (8 where the align
         routes the tokens itself: the weights then come from the align)
       separate expand, token tiles: + GEMM1 <- align, GEMM2 <- align, shrink1 by token
         (no gather) = 10
-      no adapters: the GEMMs read token tiles early only in tile mode."""
+      no adapters: the GEMMs read token tiles early only in tile mode (the fused
+        chain's combine reads the align's and the route's outputs early)."""
     import itertools
     import expert_adapter_gemms_gb300 as m
     shapes = [(8, 2, 4, 2, 256, 512, 8), (64, 4, 32, 8, 2880, 2880, 32),
@@ -242,9 +244,11 @@ def test_chain_early_reads_come_from_completed_launches(L):
             assert p["early_reads"] == 0
             continue
         if Ln == 0:
-            assert p["early_reads"] == (0 if p["fused_expand"] or p["expert_major_rows"] else 2)
+            fused = 2 - p["route_in_align"]  # the combine's slot rows and weights
+            assert p["early_reads"] == (fused if p["fused_expand"] else
+                                        0 if p["expert_major_rows"] else 2), (T, mode, p)
         elif p["fused_expand"]:
-            assert p["early_reads"] == 6, (T, mode, p)
+            assert p["early_reads"] == 8 - p["route_in_align"], (T, mode, p)
         elif p["expert_major_rows"]:
             assert p["early_reads"] == 9 - p["route_in_align"], (T, mode, p)
         else:
