@@ -3,7 +3,7 @@
 // multi-LoRA inference for MoE models in vLLM"; agentlenshq.com, section
 // "Multi-LoRA Serving for MoE Models").
 //
-// One CTA (1024 threads up to 512 slots, 256 up to 4096, 1024 beyond). Each slot s gets the
+// One CTA of 1024 threads (up to a few thousand slots). Each slot s gets the
 // packed word (key << slot_bits) | s with key = e * (L + 1) + (l + 1) (dropped
 // slots use the last bucket). A stable least-significant-digit radix sort on the
 // key bits (8-bit digits, per-warp digit histograms, ranks inside a warp from
@@ -660,13 +660,9 @@ int launch_route_align(const float* logits, int* ids, float* w, const int* token
                        const moe_lora_align_t* al, const AlignLayout& a, cudaStream_t stream,
                        bool pdl) {
   if (!align_can_route(a, al->T, al->E)) return MOE_LORA_ERR_UNSUPPORTED;
-  // the rank sort's words: 1024 threads (two tokens a warp, up to four lanes a word); the
-  // radix sort's: 256, whose barriers are cheaper
-  if (a.S <= kRankSortMaxSlots)
-    return al->E <= 32 ? launch_align_t<1024, 1>(ids, token_adapter, al, a, stream, pdl, logits, w)
-                       : launch_align_t<1024, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
-  if (al->E <= 32) return launch_align_t<256, 1>(ids, token_adapter, al, a, stream, pdl, logits, w);
-  return launch_align_t<256, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
+  // 1024 threads: two tokens a warp, up to eight lanes a word of the rank sort
+  return al->E <= 32 ? launch_align_t<1024, 1>(ids, token_adapter, al, a, stream, pdl, logits, w)
+                     : launch_align_t<1024, 2>(ids, token_adapter, al, a, stream, pdl, logits, w);
 }
 
 int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_t* al,
@@ -682,10 +678,8 @@ int launch_align(const int* ids, const int* token_adapter, const moe_lora_align_
     return launch_pdl(align_place_kernel<256>, a.ctas, 256, 0, stream, pdl, v, al->L, a.S,
                       a.nbuckets, a.slot_bits, a.ctas);
   }
-  // few slots: the rank sort spreads over 1024 threads; up to 4096, a small CTA keeps the
-  // many barriers of the radix sort cheap
-  if (a.S <= kRankSortMaxSlots) return launch_align_t<1024, 0>(ids, token_adapter, al, a, stream, pdl);
-  if (a.S <= 4096) return launch_align_t<256, 0>(ids, token_adapter, al, a, stream, pdl);
+  // one CTA of 1024 threads (at 1024 and 2048 slots, with the radix sort: 15.3 and 25.7 us
+  // against 17.5 and 33.8 us with 256 threads)
   return launch_align_t<1024, 0>(ids, token_adapter, al, a, stream, pdl);
 }
 
