@@ -728,8 +728,8 @@ def run_ours(args):
     # every other configuration of the pages' workloads: throughput and per-stage roofline
     # fractions (fewer steps; no CPU baseline)
     if rank == 0 and args.workloads != "none":
-        from workloads import WORKLOAD_NAMES
-        names = WORKLOAD_NAMES if args.workloads == "all" else args.workloads.split(",")
+        from workloads import ALL_WORKLOAD_NAMES
+        names = ALL_WORKLOAD_NAMES if args.workloads == "all" else args.workloads.split(",")
         wl = {inp.name: {k: v for k, v in head.items()}}
         del layer
         torch.cuda.empty_cache()

@@ -102,10 +102,32 @@ static void pick_tiles(int T, int k, int E, int L, int32_t* bm_base, int32_t* bm
 
 // Rows per expert-major chunk: with few rows per expert (decode) each grouped-GEMM CTA
 // takes one (expert, weight block) and all of the expert's rows, so it can stream its
-// weights before routing and alignment have finished; 0: token tiles.
+// weights before routing and alignment have finished; 0: token tiles. An expert with more
+// rows than the chunk streams its weights once per chunk, so chunks of 64 rows are taken
+// up to 32 rows per expert on average, and up to 64 where the count is exact (one expert:
+// a dense layer). At 48 and 64 rows per expert of 32 experts (GPT-OSS dims), 64-row chunks
+// ran 0.352 against 0.363 ms and 0.488 against 0.377 ms for token tiles.
 static int expert_major_rows(int T, int k, int E) {
   const int64_t per_expert = ((int64_t)T * k + E - 1) / E;
-  return per_expert <= 16 ? 32 : per_expert <= 32 ? 64 : 0;
+  return per_expert <= 16 ? 32 : per_expert <= 32 || (E == 1 && per_expert <= 64) ? 64 : 0;
+}
+
+// The expert-major down GEMM's K shares (partial outputs the combine sums): two where the
+// (expert, weight block) CTAs already fill the SMs' slots (2.4 -> 4.8 waves at the GPT-OSS
+// decode shape, where one and three shares were slower), else as many as fill about one
+// wave of two CTAs per SM (dense, E = 1: 8 shares at H = 4096, 4 at H = 8192 were the best
+// measured), at most 8 and at least two k-blocks each. Shape-only (a fixed 304 slots), so
+// the workspace layout does not depend on the device.
+static int down_ksplit(int E, int H, int I) {
+  const int64_t blocks = (int64_t)E * ((H + 127) / 128);
+  const int nk = (I + 63) / 64;
+  if (nk < 4) return 1;
+  int s = blocks >= 304 ? 2 : (int)std::min<int64_t>(8, std::max<int64_t>(2, 304 / blocks));
+  s = std::min(s, nk / 2);
+  // the kernel gives share i the k-blocks [i q, (i + 1) q), q = ceil(nk / s): every share
+  // must hold some (an empty one would publish an accumulator it never wrote)
+  while (s > 1 && (s - 1) * ((nk + s - 1) / s) >= nk) --s;
+  return s;
 }
 
 // The fused expand's token tile (and so the zero gap of its shifted z buffers) that the
@@ -163,10 +185,9 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r,
   p.bm_lora = opt.bm_lora > 0 ? opt.bm_lora : hl;
   const int chunk = p.em_bn > 0 ? p.em_bn : p.bm_base;
   p.fused = want && chunk <= gap;
-  // few rows per expert: the down GEMM's (expert, weight block) CTAs are few against the
-  // SMs' slots (2.4 waves at the GPT-OSS decode shape), so each block's K range is split in
-  // two and the combine sums both partial outputs (4.8 waves)
-  p.ksplit = p.fused && p.em_bn > 0 && (I + 63) / 64 >= 4 ? 2 : 1;
+  // few rows per expert: each down weight block's K range is split (down_ksplit) and the
+  // combine sums the partial outputs
+  p.ksplit = p.fused && p.em_bn > 0 ? down_ksplit(E, H, I) : 1;
   p.al = align_layout(T, k, E, L, p.bm_base, p.bm_lora);
   // the align region is sized for the smallest tiles so any tile choice fits
   AlignLayout worst = align_layout(T, k, E, L, 16, 1);
@@ -183,7 +204,7 @@ static LayerPlan plan_layer(int T, int k, int E, int L, int H, int I, int r,
   p.off_Z1 = take(S * 2 * rr * 4);  // two z slices with separate gate and up adapters
   p.off_h = take(S * (int64_t)I * 2);
   p.off_Z2 = take(S * rr * 4);
-  p.off_O = take(S * (int64_t)H * 4 * (em_shape > 0 ? 2 : 1));  // room for two partial outputs
+  p.off_O = take(S * (int64_t)H * 4 * (em_shape > 0 ? down_ksplit(E, H, I) : 1));  // partial outputs
   p.total = o;
   p.valid = true;
   return p;

@@ -79,6 +79,18 @@ def test_layer_workloads(name, chunk, expand_mode):
     assert_close(y[tokens], _REF_Y[key], LAYER_RTOL, f"{name} chunk {chunk} plan {plan}")
 
 
+@pytest.mark.parametrize("expand_mode", [0, 1])
+def test_dense_multi_lora_workload(expand_mode):
+    """Dense multi-LoRA (one expert, top-1) at an 8B-class dense model's size: hidden 4096,
+    intermediate 14336, 64 decode tokens over 8 adapters of rank 16 -- the workload the
+    bench measures beside the five -- through both chains, every token against the oracle."""
+    m = need_gpu()
+    inp = _inputs("dense_4096_14336")
+    y, plan = _workload_y(m, "dense_4096_14336", expand_mode)
+    ref = oracle_layer(inp)
+    assert_close(y, ref, LAYER_RTOL, f"dense plan {plan}")
+
+
 def test_fused_chain_is_picked_where_it_applies():
     """The plan fuses the expand into the grouped GEMMs for the decode and prefill workloads
     (few rows per expert, or long (expert, adapter) runs), not for the 4096/11008 example
@@ -99,14 +111,16 @@ def test_fused_chain_is_picked_where_it_applies():
 
 @pytest.mark.parametrize("shape", ["r8_expert_major", "r24_expert_major", "r64_chunked",
                                    "r128_chunked", "tiles_many_runs", "persistent_r32",
-                                   "base_only_tiles", "expert_major_k_tail"])
+                                   "base_only_tiles", "expert_major_k_tail",
+                                   "dense_ksplit8_k_tail"])
 def test_fused_expand_shapes(shape):
     """The fused chain on shapes that exercise its cases: ranks that need zero padding to a
     multiple of 16 (8, 24), ranks whose high and low z parts take separate 64-column chunks
     (64, 128), expert-major chunks, token tiles holding many adapter runs (one adapter per
     request of 64 tokens), persistent 128-row tiles, no adapters at all, and expert-major
-    64-row chunks with a K tail. Every token is compared with the oracle and with the chain
-    of separate expand kernels."""
+    64-row chunks with a K tail, and one expert (dense) whose down GEMM splits its K range in
+    eight shares of two k-blocks, the last with a 40-column tail. Every token is compared
+    with the oracle and with the chain of separate expand kernels."""
     m = need_gpu()
     kw = {"r8_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=8),
           "r24_expert_major": dict(T=40, H=128, I=96, E=4, k=2, L=3, r=24),
@@ -118,7 +132,8 @@ def test_fused_expand_shapes(shape):
           "base_only_tiles": dict(T=300, H=256, I=192, E=4, k=2, L=0, r=16),
           # 64-row chunks (experts of more than 32 rows) and K = 200: the last 64-column
           # stage has 8 columns, the rest read as zeros
-          "expert_major_k_tail": dict(T=64, H=200, I=96, E=4, k=2, L=3, r=16)}[shape]
+          "expert_major_k_tail": dict(T=64, H=200, I=96, E=4, k=2, L=3, r=16),
+          "dense_ksplit8_k_tail": dict(T=20, H=256, I=1000, E=1, k=1, L=3, r=16)}[shape]
     inp = make_layer_inputs(seed=120 + len(shape), lora_std=None, **kw)
     plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
     assert plan["fused_expand"] == 1, plan

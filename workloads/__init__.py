@@ -8,6 +8,8 @@ path can consume the very same inputs without sharing any computation.
 from .generators import (  # noqa: F401
     WORKLOADS,
     WORKLOAD_NAMES,
+    EXTRA_WORKLOADS,
+    ALL_WORKLOAD_NAMES,
     LayerInputs,
     workload_by_name,
     make_workload_inputs,

@@ -49,9 +49,33 @@ WORKLOADS = [
 
 WORKLOAD_NAMES = [w["name"] for w in WORKLOADS]
 
+# Measured beside the five: a dense model served with multi-LoRA, the degenerate MoE of one
+# expert taken by every token (E = 1, k = 1), at the size of an 8B-class dense model's MLP
+# (hidden 4096, intermediate 14336), 64 decode tokens over 8 adapters of rank 16. Workload j
+# of this list is seeded with 2000 + j.
+EXTRA_WORKLOADS = [
+    dict(name="dense_4096_14336", T=64, H=4096, I=14336, E=1, k=1, L=8, r=16,
+         routing="gaussian", adapters="round_robin_shuffled"),
+]
+ALL_WORKLOAD_NAMES = WORKLOAD_NAMES + [w["name"] for w in EXTRA_WORKLOADS]
+
+
+def _config_and_seed(index_or_name: Union[int, str]):
+    """A workload's configuration and default seed: 1000 + i for the i-th of the five,
+    2000 + j for the j-th extra one."""
+    if isinstance(index_or_name, int):
+        return WORKLOADS[index_or_name], 1000 + index_or_name
+    names = [c["name"] for c in WORKLOADS]
+    if index_or_name in names:
+        i = names.index(index_or_name)
+        return WORKLOADS[i], 1000 + i
+    extra = [c["name"] for c in EXTRA_WORKLOADS]
+    j = extra.index(index_or_name)  # ValueError for an unknown name
+    return EXTRA_WORKLOADS[j], 2000 + j
+
 
 def workload_by_name(name: str) -> dict:
-    for c in WORKLOADS:
+    for c in WORKLOADS + EXTRA_WORKLOADS:
         if c["name"] == name:
             return dict(c)
     raise KeyError(name)
@@ -213,14 +237,11 @@ def make_layer_inputs(T: int, H: int, I: int, E: int, k: int, L: int, r: int, se
 
 
 def make_workload_inputs(index_or_name: Union[int, str], seed: Optional[int] = None) -> LayerInputs:
-    """Inputs of one of the five named workloads; workload i is seeded with 1000 + i."""
-    if isinstance(index_or_name, int):
-        idx = index_or_name
-    else:
-        idx = [c["name"] for c in WORKLOADS].index(index_or_name)
-    c = WORKLOADS[idx]
+    """Inputs of a named workload (one of the five, or an extra one); the i-th of the five
+    is seeded with 1000 + i, the j-th extra one with 2000 + j."""
+    c, s0 = _config_and_seed(index_or_name)
     return make_layer_inputs(c["T"], c["H"], c["I"], c["E"], c["k"], c["L"], c["r"],
-                             seed=1000 + idx if seed is None else seed,
+                             seed=s0 if seed is None else seed,
                              routing=c["routing"], adapters=c["adapters"], name=c["name"])
 
 
@@ -230,12 +251,8 @@ def make_workload_routing(index_or_name: Union[int, str], seed: Optional[int] = 
     Same generator and draw order as :func:`make_workload_inputs`, stopped before
     the activations and weights, so the values equal that function's.
     """
-    if isinstance(index_or_name, int):
-        idx = index_or_name
-    else:
-        idx = [c["name"] for c in WORKLOADS].index(index_or_name)
-    c = WORKLOADS[idx]
-    rng = np.random.default_rng(1000 + idx if seed is None else seed)
+    c, s0 = _config_and_seed(index_or_name)
+    rng = np.random.default_rng(s0 if seed is None else seed)
     logits = _routing_logits(rng, c["T"], c["E"], c["routing"])
     token_adapter = _adapters(rng, c["T"], c["L"], c["adapters"])
     return logits, token_adapter, dict(c)
