@@ -173,7 +173,27 @@ def test_align_multi_cta_cases():
     _check_align(m, rng.integers(0, 32, size=(512, 4)), None, 32, 0, 128, 16)
 
 
-@pytest.mark.parametrize("name", ["gptoss20b_decode", "tiny"])
+@pytest.mark.parametrize("S", [1, 3, 5, 127, 128, 129, 255, 256, 257, 510, 511, 512, 513, 600])
+def test_align_rank_sort_sizes(S):
+    """Up to 512 slots the one-CTA align places each word by its rank, with up to eight
+    lanes sharing a word (8 up to 128 words, 4 up to 256, 2 up to 512) and the words
+    padded to whole 16-byte groups; above, the radix sort. Bit-exact with the oracle at
+    and around each boundary, at word counts with one to three padding words."""
+    m = need_gpu()
+    rng = np.random.default_rng(300 + S)
+    ids = rng.integers(0, 7, size=(S, 1))
+    _check_align(m, ids, rng.integers(-1, 3, size=S), 7, 3, 16, 4)
+
+
+_ROUTED_SHAPES = {
+    # 64 tokens, top-8 of 64 experts (two logits a lane): 512 slots, two lanes a word
+    "k8_E64": dict(T=64, H=256, I=128, E=64, k=8, L=4, r=16),
+    # 37 tokens, top-3 of 40 experts: 111 slots (one padding word), eight lanes a word
+    "T37_k3_E40": dict(T=37, H=256, I=128, E=40, k=3, L=5, r=16),
+}
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_decode", "tiny", "k8_E64", "T37_k3_E40"])
 def test_align_routes_in_layer(name):
     """Up to 64 tokens the layer's one-CTA align routes the tokens itself (no route
     launch): the align tables it leaves at the start of the workspace -- the stable sort
@@ -181,8 +201,9 @@ def test_align_routes_in_layer(name):
     oracle's routing and alignment, bit for bit; so do the routing weights the combine
     read (y against the layer with the route kernel's ids and weights passed in)."""
     m = need_gpu()
-    from workloads import make_workload_inputs
-    inp = make_workload_inputs(name)
+    from workloads import make_layer_inputs, make_workload_inputs
+    inp = (make_layer_inputs(seed=310 + len(name), **_ROUTED_SHAPES[name])
+           if name in _ROUTED_SHAPES else make_workload_inputs(name))
     plan = m.moe_lora_layer_plan(inp.T, inp.k, inp.E, inp.L, inp.H, inp.I, inp.r)
     assert plan["route_in_align"] == 1, plan
     lora = dict(A1=dev(inp.A1), B1=dev(inp.B1), A2=dev(inp.A2), B2=dev(inp.B2))
