@@ -479,14 +479,25 @@ __global__ void __launch_bounds__(kPipeWarps * 32, NT <= 2 ? 3 : 2)
   __syncthreads();
 
   const int nchunks = (K + kPipeKC - 1) / kPipeKC;
+  // Lane q copies the 16-byte group q of stage rows warp, warp + 8, ... (a warp moves one
+  // whole 512-byte row a step); the rows' sources stay in registers for every chunk.
+  static_assert(GROUPS == 32, "one 16-byte group of a stage row a lane");
+  constexpr int NPC = (ROWS + kPipeWarps - 1) / kPipeWarps;
+  const __nv_bfloat16* psrc[NPC];
+#pragma unroll
+  for (int u = 0; u < NPC; ++u) {
+    const int i = warp + u * kPipeWarps;
+    const __nv_bfloat16* src = i < ROWS ? s_src[i] : nullptr;
+    psrc[u] = src ? src + lane * 8 : nullptr;
+  }
   auto issue = [&](int c) {  // chunk c into its stage (an empty group past the last chunk)
     if (c < nchunks) {
-      uint8_t* st = smem + (size_t)(c % NS) * ROWS * kPipeRow;
-      for (int it = threadIdx.x; it < ROWS * GROUPS; it += blockDim.x) {
-        const int i = it / GROUPS, grp = it - i * GROUPS;
-        const int col = c * kPipeKC + grp * 8;
-        const __nv_bfloat16* src = s_src[i];
-        if (src && col < K) cp_async16(st + (size_t)i * kPipeRow + grp * 16, src + col);
+      uint8_t* st = smem + (size_t)(c % NS) * ROWS * kPipeRow + lane * 16;
+      const int c0 = c * kPipeKC;
+      if (c0 + lane * 8 < K) {
+#pragma unroll
+        for (int u = 0; u < NPC; ++u)
+          if (psrc[u]) cp_async16(st + (size_t)(warp + u * kPipeWarps) * kPipeRow, psrc[u] + c0);
       }
     }
     cp_async_commit();
