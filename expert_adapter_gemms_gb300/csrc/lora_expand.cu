@@ -566,8 +566,10 @@ __global__ void __launch_bounds__(kExpandThreads)
     // keeps several KB of G in flight without spending registers on it. A tile's G
     // part is [16 rows][8 columns] fp32 for gate and for up: lane -> (row lane / 2,
     // columns 4 (lane % 2) .. +3), one 16-byte copy per part.
-    uint4 bg[KC], bu[KC];
-    auto fetch_b = [&](int t) {
+    // B fragments two tiles ahead: the warp's tiles alternate between two register sets
+    uint4 bg0[KC], bu0[KC], bg1[KC], bu1[KC];
+    auto fetch_b = [&](int t, uint4 (&bg)[KC], uint4 (&bu)[KC]) {
+      if (t >= ntiles) return;
       const int nl = t * 8 + gid;
 #pragma unroll
       for (int c = 0; c < KC; ++c) {
@@ -592,7 +594,8 @@ __global__ void __launch_bounds__(kExpandThreads)
     int t = t_begin + warp;
 #pragma unroll
     for (int d = 0; d < kGStages - 1; ++d) fetch_g(t + d * kWarps, d);
-    if (t < ntiles) fetch_b(t);
+    fetch_b(t, bg0, bu0);
+    fetch_b(t + kWarps, bg1, bu1);
     if (early) pdl_wait();
     pdl_trigger();
     __nv_bfloat16* zbu = zb + zsmem_bytes(KC) / sizeof(__nv_bfloat16);
@@ -603,7 +606,9 @@ __global__ void __launch_bounds__(kExpandThreads)
     z.load(zb, r_pad);
     if (kTwo) z2.load(zbu, r_pad);
     const ZFrag<KC>& zu = kTwo ? z2 : z;
-    for (int j = 0; t < ntiles; t += kWarps, ++j) {
+    // tile t (the j-th of this warp) from the register set (bg, bu), which then takes tile
+    // t + 2 kWarps
+    auto tile = [&](int t, int j, uint4 (&bg)[KC], uint4 (&bu)[KC]) {
       fetch_g(t + (kGStages - 1) * kWarps, (j + kGStages - 1) % kGStages);
       cp_async_wait<kGStages - 1>();  // this tile's copies have landed
       __syncwarp();                   // ... every lane's
@@ -613,7 +618,7 @@ __global__ void __launch_bounds__(kExpandThreads)
         tg[c] = bg[c];
         tu[c] = bu[c];
       }
-      if (t + kWarps < ntiles) fetch_b(t + kWarps);  // next tile's B in flight
+      fetch_b(t + 2 * kWarps, bg, bu);  // B two tiles ahead in flight
       if (kRanked) {
 #pragma unroll
         for (int c = 0; c < KC; ++c) {  // entries past the adapter's rank
@@ -642,6 +647,10 @@ __global__ void __launch_bounds__(kExpandThreads)
         }
       }
       __syncwarp();  // the stage is read by every lane before it is refilled
+    };
+    for (int j = 0; t < ntiles; t += 2 * kWarps, j += 2) {
+      tile(t, j, bg0, bu0);
+      if (t + kWarps < ntiles) tile(t + kWarps, j + 1, bg1, bu1);
     }
     cp_async_wait<0>();
   } else {
