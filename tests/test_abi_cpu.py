@@ -117,6 +117,30 @@ def test_layer_tiles_heuristic(L):
         assert b in (16, 32, 64, 128, 256) and 1 <= l <= 16
 
 
+def test_expert_major_and_down_shares_heuristic(L):
+    """Expert-major chunks where each expert's rows fit one chunk: up to 32 rows per expert
+    on average, up to 64 where the count is exact (one expert: a dense layer); MoE at 48 or
+    64 rows per expert keeps token tiles (an expert above the chunk would stream its
+    weights once per chunk). The dense layer's down GEMM splits its K range into up to eight
+    shares (each a partial output in the workspace), the MoE decode shape into two."""
+    import expert_adapter_gemms_gb300 as m
+    plan = m.moe_lora_layer_plan
+    assert plan(64, 1, 1, 8, 4096, 14336, 16)["expert_major_rows"] == 64
+    assert plan(64, 1, 1, 8, 4096, 14336, 16)["fused_expand"] == 1
+    assert plan(65, 1, 1, 8, 4096, 14336, 16)["expert_major_rows"] == 0
+    assert plan(64, 4, 32, 8, 2880, 2880, 32)["expert_major_rows"] == 32
+    assert plan(256, 4, 32, 8, 2880, 2880, 32)["expert_major_rows"] == 64
+    assert plan(384, 4, 32, 8, 2880, 2880, 32)["expert_major_rows"] == 0
+    assert plan(512, 4, 32, 8, 2880, 2880, 32)["expert_major_rows"] == 0
+    # the partial outputs: S H fp32 per share (8 for the dense 4096-wide layer, 2 at the
+    # GPT-OSS decode shape), so the dense workspace grows by 6 S H 4 bytes over two shares
+    S, H = 64, 4096
+    dense = m.moe_lora_workspace_size(64, 1, 1, 8, 4096, 14336, 16)
+    assert dense >= S * H * 4 * 8
+    moe = m.moe_lora_workspace_size(64, 4, 32, 8, 2880, 2880, 32)
+    assert 256 * 2880 * 4 * 2 < moe < 256 * 2880 * 4 * 8  # two shares, not eight
+
+
 def test_host_validation_before_any_cuda_call(L):
     P = ctypes.c_void_p
     fake = P(0x1000)  # never dereferenced: every call below fails validation first
